@@ -1,0 +1,327 @@
+"""Pins of the CPU oracle against things other than itself: hand-worked
+golden cases, brute-force loops, closed forms, invariants, central finite
+differences, autograd of a dense formulation, and planted mistakes that the
+pins must catch.  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.moe_oracle as O
+from mixture_experts_atomic_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            out[k] = [float(t) if ("." in t or "e" in t) else int(t) for t in v]
+    return out
+
+
+def _rand_problem(L, d, h, E, K, act, seed, one_expert=None):
+    ids, gates = I.random_routing(L, E, K, seed, one_expert=one_expert)
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((L, d))
+    W1 = rng.standard_normal((E, d, h)) / math.sqrt(d)
+    W2 = rng.standard_normal((E, d, h)) / math.sqrt(d) if act == "swiglu" else None
+    W3 = rng.standard_normal((E, h, d)) / math.sqrt(h)
+    dY = rng.standard_normal((L, d))
+    if act == "identity":
+        W1 = W2 = W3 = None
+    return ids.numpy(), gates.numpy().astype(np.float64), x, W1, W2, W3, dY
+
+
+# ---------------------------------------------------------------- dispatch
+
+def _dispatch_bruteforce(ids, E):
+    """Per-slot loops, no sort: walk experts, then tokens in ascending order."""
+    L, K = ids.shape
+    D1, D2 = [], [0]
+    D4 = [[-1] * K for _ in range(L)]
+    for e in range(E):
+        for t in range(L):
+            for k in range(K):
+                if ids[t][k] == e:
+                    D4[t][k] = len(D1)
+                    D1.append(t)
+        D2.append(len(D1))
+    return np.array(D1, dtype=np.int64), np.array(D2), np.array(ids), np.array(D4)
+
+
+def test_dispatch_golden_hand_worked():
+    g = _read_golden("dispatch_L5_E4_K2.txt")
+    L, E, K = g["L"][0], g["E"][0], g["K"][0]
+    ids = np.array(g["topk_ids"]).reshape(L, K)
+    D1, D2, D3, D4 = O.dispatch(ids, E)
+    assert D1.tolist() == g["expert_token_indices"]
+    assert D2.tolist() == g["expert_token_offsets"]
+    assert D3.reshape(-1).tolist() == g["token_expert_indices"]
+    assert D4.reshape(-1).tolist() == g["token_index_map"]
+
+
+@pytest.mark.parametrize("L,E,K,seed", [(1, 1, 1, 0), (7, 3, 2, 1), (16, 4, 4, 2),
+                                        (33, 8, 3, 3), (40, 5, 1, 4), (12, 6, 6, 5)])
+def test_dispatch_matches_bruteforce(L, E, K, seed):
+    ids, _ = I.random_routing(L, E, K, seed)
+    ids = ids.numpy()
+    got = O.dispatch(ids, E)
+    ref = _dispatch_bruteforce(ids, E)
+    for a, b in zip(got, ref):
+        assert np.array_equal(a.reshape(-1), b.reshape(-1))
+
+
+def test_dispatch_invariants_and_edge_cases():
+    # empty input
+    D1, D2, D3, D4 = O.dispatch(np.zeros((0, 2), dtype=np.int64), 4)
+    assert D1.size == 0 and D2.tolist() == [0] * 5
+    # every token on one expert with K = 1: D1 is 0..L-1
+    L = 37
+    D1, D2, _, D4 = O.dispatch(np.full((L, 1), 2), 5)
+    assert D1.tolist() == list(range(L))
+    assert D2.tolist() == [0, 0, 0, L, L, L]
+    # randomised invariants with skewed loads and empty experts
+    ids, _ = I.random_routing(500, 9, 3, 7, one_expert=4)
+    ids = ids.numpy()
+    E = 12  # experts 9..11 receive no token
+    D1, D2, D3, D4 = O.dispatch(ids, E)
+    L, K = ids.shape
+    assert D2[-1] == L * K and D2[0] == 0 and np.all(np.diff(D2) >= 0)
+    assert np.array_equal(D2[10:], [L * K] * 3)
+    assert sorted(D4.reshape(-1).tolist()) == list(range(L * K))  # every slot once
+    assert np.array_equal(D1[D4], np.repeat(np.arange(L)[:, None], K, 1))
+    assert np.array_equal(D3, ids)
+    for e in range(E):
+        seg = D1[D2[e]:D2[e + 1]]
+        assert np.all(np.diff(seg) > 0)  # ascending token ids
+        assert np.all((ids[seg] == e).any(axis=1))
+    with pytest.raises(ValueError):
+        O.dispatch(np.array([[0, 5]]), 4)
+    assert not O.check_distinct(np.array([[1, 1]]))
+    assert O.check_distinct(np.array([[1, 2]]))
+
+
+# ---------------------------------------------------------------- forward
+
+def _bruteforce_token(xrow, e, W1, W2, W3, act):
+    """One token through one expert with scalar Python loops and math.exp."""
+    d = len(xrow)
+    if act == "identity":
+        return list(xrow)
+    h = len(W1[e][0])
+    H = []
+    for j in range(h):
+        a = sum(xrow[i] * W1[e][i][j] for i in range(d))
+        s = a / (1.0 + math.exp(-a))
+        if act == "swiglu":
+            b = sum(xrow[i] * W2[e][i][j] for i in range(d))
+            H.append(s * b)
+        else:
+            H.append(s)
+    return [sum(H[j] * W3[e][j][c] for j in range(h)) for c in range(d)]
+
+
+@pytest.mark.parametrize("act", ["swiglu", "silu", "identity"])
+def test_forward_matches_per_token_bruteforce(act):
+    L, d, h, E, K = 9, 5, 4, 4, 2
+    ids, g, x, W1, W2, W3, _ = _rand_problem(L, d, h, E, K, act, 11)
+    y = O.forward(ids, g, x, W1, W2, W3, act, E=E)
+    for t in range(L):
+        ref = [0.0] * d
+        for k in range(K):
+            out = _bruteforce_token(x[t].tolist(), int(ids[t, k]),
+                                    None if W1 is None else W1.tolist(),
+                                    None if W2 is None else W2.tolist(),
+                                    None if W3 is None else W3.tolist(), act)
+            ref = [r + g[t, k] * o for r, o in zip(ref, out)]
+        np.testing.assert_allclose(y[t], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_identity_closed_form():
+    # identity experts: y = (sum_k g) x = x for Dirichlet gates (sum to 1)
+    L, d, E, K = 64, 8, 16, 4
+    ids, g = I.random_routing(L, E, K, 3)
+    x = np.random.default_rng(0).standard_normal((L, d))
+    y = O.forward(ids, g, x, act="identity", E=E)
+    np.testing.assert_allclose(y, g.numpy().astype(np.float64).sum(1)[:, None] * x, rtol=1e-14)
+    np.testing.assert_allclose(y, x, rtol=1e-6, atol=1e-6)  # gates are fp32-rounded
+
+
+def test_forward_single_expert_silu_is_dense_mlp():
+    # one expert, K = 1, gate 1: y = SiLU(x W1) W3 (torch.nn.functional.silu)
+    L, d, h = 20, 6, 10
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((L, d)); W1 = rng.standard_normal((1, d, h)); W3 = rng.standard_normal((1, h, d))
+    y = O.forward(np.zeros((L, 1), dtype=np.int64), np.ones((L, 1)), x, W1, None, W3, "silu", E=1)
+    ref = torch.nn.functional.silu(torch.from_numpy(x) @ torch.from_numpy(W1[0])) @ torch.from_numpy(W3[0])
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_swiglu_scalar_golden():
+    gd = _read_golden("swiglu_scalar_closed_form.txt")
+    f = lambda k: np.array(gd[k], dtype=np.float64)
+    x = f("x").reshape(1, 1)
+    W1 = f("W1").reshape(1, 1, 1); W2 = f("W2").reshape(1, 1, 1); W3 = f("W3").reshape(1, 1, 1)
+    ids = np.zeros((1, 1), dtype=np.int64); g = f("g").reshape(1, 1); dY = f("dY").reshape(1, 1)
+    y = O.forward(ids, g, x, W1, W2, W3, "swiglu", E=1)
+    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, "swiglu", E=1)
+    for name, v in [("y", y), ("dX", dX), ("dW1", dW1), ("dW2", dW2), ("dW3", dW3)]:
+        assert float(v.reshape(-1)[0]) == pytest.approx(gd[name][0], rel=1e-14), name
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(ids, g, x, W1, W2, W3, dY, act, E):
+    return float(np.sum(O.forward(ids, g, x, W1, W2, W3, act, E=E) * dY))
+
+
+def _fd_errors(ids, g, x, W1, W2, W3, dY, act, E, eps=1e-5, n_samples=None, seed=0):
+    """max relative error of the oracle's backward vs central differences."""
+    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    rng = np.random.default_rng(seed)
+    errs = {}
+    for name, arr, grad in [("x", x, dX), ("W1", W1, dW1), ("W2", W2, dW2), ("W3", W3, dW3)]:
+        if arr is None:
+            continue
+        flat = arr.reshape(-1)
+        idxs = range(flat.size) if n_samples is None else rng.choice(flat.size, n_samples, replace=False)
+        fd = []
+        an = []
+        for i in idxs:
+            old = flat[i]
+            flat[i] = old + eps
+            lp = _loss(ids, g, x, W1, W2, W3, dY, act, E)
+            flat[i] = old - eps
+            lm = _loss(ids, g, x, W1, W2, W3, dY, act, E)
+            flat[i] = old
+            fd.append((lp - lm) / (2 * eps))
+            an.append(grad.reshape(-1)[i])
+        fd = np.array(fd); an = np.array(an)
+        errs[name] = float(np.max(np.abs(fd - an)) / max(np.max(np.abs(fd)), 1e-30))
+    return errs
+
+
+@pytest.mark.parametrize("act", ["swiglu", "silu", "identity"])
+def test_backward_central_finite_differences(act):
+    L, d, h, E, K = 7, 4, 3, 3, 2
+    ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, act, 21)
+    errs = _fd_errors(ids, g, x, W1, W2, W3, dY, act, E)
+    assert max(errs.values()) < 1e-7, errs  # the benchmark spec's bound is 1e-3
+
+
+def test_backward_fd_config0_shape_sampled():
+    # the fp32 config's shape class with a smaller L; sampled entries
+    cfg = I.CONFIGS[0].scaled(L=24)
+    inp = I.make_inputs(cfg)
+    args = [inp["ids"].numpy(), inp["gates"].numpy().astype(np.float64),
+            O._f64(inp["x"]), O._f64(inp["W1"]), O._f64(inp["W2"]), O._f64(inp["W3"]), O._f64(inp["dY"])]
+    errs = _fd_errors(*args, "swiglu", cfg.E, eps=1e-5, n_samples=12)
+    assert max(errs.values()) < 1e-6, errs
+
+
+@pytest.mark.parametrize("act", ["swiglu", "silu"])
+def test_backward_matches_autograd_dense(act):
+    """torch.autograd (fp64) of a dense formulation in which every token runs
+    through every expert, masked by a dense gate matrix."""
+    L, d, h, E, K = 11, 6, 5, 4, 2
+    ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, act, 31)
+    T = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    xt, w1, w3 = T(x), T(W1), T(W3)
+    w2 = T(W2) if act == "swiglu" else None
+    Gd = torch.zeros(L, E, dtype=torch.float64)
+    for t in range(L):
+        for k in range(K):
+            Gd[t, ids[t, k]] += g[t, k]
+    a = torch.einsum("ld,edh->leh", xt, w1)
+    H = torch.nn.functional.silu(a)
+    if act == "swiglu":
+        H = H * torch.einsum("ld,edh->leh", xt, w2)
+    Y = torch.einsum("leh,ehd->led", H, w3)
+    y = (Gd[:, :, None] * Y).sum(1)
+    (y * torch.tensor(dY)).sum().backward()
+    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    np.testing.assert_allclose(dX, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dW1, w1.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dW3, w3.grad.numpy(), rtol=1e-10, atol=1e-12)
+    if act == "swiglu":
+        np.testing.assert_allclose(dW2, w2.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(O.forward(ids, g, x, W1, W2, W3, act, E=E), y.detach().numpy(),
+                               rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sampled helpers
+
+@pytest.mark.parametrize("act", ["swiglu", "silu", "identity"])
+def test_sampled_helpers_agree_with_full_oracle(act):
+    L, d, h, E, K = 30, 8, 6, 5, 3
+    ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, act, 41)
+    y = O.forward(ids, g, x, W1, W2, W3, act, E=E)
+    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    toks = [0, 3, 17, 29]
+    np.testing.assert_allclose(O.forward_rows(toks, ids, g, x[toks], W1, W2, W3, act), y[toks], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(O.backward_rows(toks, ids, g, x[toks], dY[toks], W1, W2, W3, act), dX[toks],
+                               rtol=1e-12, atol=1e-13)
+    if act == "identity":
+        return
+    D1, D2, D3, D4 = O.dispatch(ids, E)
+    gr = np.zeros(L * K)
+    for k in range(K):
+        gr[D4[:, k]] = g[:, k]
+    for e in range(E):
+        seg = D1[D2[e]:D2[e + 1]]
+        c1, c2, r3 = O.weight_grad_slices(e, seg, gr[D2[e]:D2[e + 1]], x[seg], dY[seg], W1, W2, W3, act,
+                                          h_cols=[0, h - 1], w3_rows=[1, 2])
+        np.testing.assert_allclose(c1, dW1[e][:, [0, h - 1]], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(r3, dW3[e][[1, 2], :], rtol=1e-12, atol=1e-13)
+        if act == "swiglu":
+            np.testing.assert_allclose(c2, dW2[e][:, [0, h - 1]], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """A plausible mistake in the oracle makes at least one pin fail."""
+    L, d, h, E, K = 6, 3, 4, 3, 2
+    ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, "swiglu", 51)
+
+    # 1) dropped term in SiLU' -> finite differences disagree
+    with monkeypatch.context() as m:
+        m.setattr(O, "silu_grad", lambda a: O.sigmoid(a))
+        assert max(_fd_errors(ids, g, x, W1, W2, W3, dY, "swiglu", E).values()) > 1e-3
+
+    # 2) W1 and W2 swapped in the expert -> per-token brute force disagrees
+    orig = O.expert_forward
+    with monkeypatch.context() as m:
+        m.setattr(O, "expert_forward", lambda X, a, b, c, act: orig(X, b, a, c, act))
+        y = O.forward(ids, g, x, W1, W2, W3, "swiglu", E=E)
+        out = _bruteforce_token(x[0].tolist(), int(ids[0, 0]), W1.tolist(), W2.tolist(), W3.tolist(), "swiglu")
+        out2 = _bruteforce_token(x[0].tolist(), int(ids[0, 1]), W1.tolist(), W2.tolist(), W3.tolist(), "swiglu")
+        ref0 = g[0, 0] * np.array(out) + g[0, 1] * np.array(out2)
+        assert np.max(np.abs(y[0] - ref0)) > 1e-6
+
+    # 3) descending tokens inside an expert -> brute-force dispatch disagrees
+    D1, D2, D3, D4 = O.dispatch(ids, E)
+    bad = D1.copy()
+    for e in range(E):
+        bad[D2[e]:D2[e + 1]] = bad[D2[e]:D2[e + 1]][::-1]
+    assert not np.array_equal(bad, _dispatch_bruteforce(ids, E)[0])
+
+    # 4) wrong sign of SiLU(a) in the gate-branch gradient dB = dH * SiLU(a)
+    #    (the backward reads SiLU(a) as out["s"]) -> finite differences disagree
+    with monkeypatch.context() as m:
+        def bad_ef(X, a, b, c, act):
+            out = orig(X, a, b, c, act)
+            if "s" in out:
+                out = dict(out); out["s"] = -out["s"]
+            return out
+        m.setattr(O, "expert_forward", bad_ef)
+        errs = _fd_errors(ids, g, x, W1, W2, W3, dY, "swiglu", E)
+        assert max(errs.values()) > 1e-3
