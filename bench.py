@@ -1,0 +1,397 @@
+"""Benchmark of one MoE layer training step (dispatch build + forward +
+backward) on synthetic inputs shaped like the workload, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` = tokens/s of the whole job with
+inputs resident in HBM (device-timed with CUDA events, max over ranks, L2
+flushed between steps); `e2e` = the same metric through the same C-ABI calls
+with host inputs/outputs (pinned host -> device copies of x, ids, gates, dY
+and device -> host copies of y and dX inside the timed region); `roofline`
+describes the dominant kernel, timed live from the library's stage events;
+`cpu_baseline` times the CPU oracle on a bounded sample of the workload.
+With --gpus N > 1 every rank runs an independent replica on its own batch
+(weak scaling; the step has no cross-rank exchange in the timed region).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_atomic_gb300 import binding as B  # noqa: E402
+from mixture_experts_atomic_gb300 import inputs as I  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s (bf16), tensor-pipe %; dispatch-build HBM GB/s"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = dict(FALLBACK)
+            for k in FALLBACK:
+                for kk, v in d.items():
+                    if kk == k or kk.startswith(k):
+                        if isinstance(v, (int, float)):
+                            out[k] = float(v)
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def stage_flops(cfg):
+    """Algorithmic FLOPs of each GEMM stage (unpadded routed rows)."""
+    LK, d, h = cfg.L * cfg.K, cfg.d, cfg.h
+    sw = cfg.act == "swiglu"
+    nb = 2 if sw else 1
+    return {"up": 2 * nb * LK * d * h, "down": 2 * LK * h * d, "dh": 2 * LK * d * h,
+            "dx": 2 * nb * LK * h * d, "dw12": 2 * nb * LK * d * h, "dw3": 2 * LK * h * d}
+
+
+def dispatch_bytes(cfg):
+    """Algorithmic bytes of the dispatch build: ids read, three (L,K) maps and
+    the offsets written, the bit-packed bitmap written once and read once."""
+    LK = cfg.L * cfg.K
+    return 4 * LK + 12 * LK + 4 * (cfg.E + 1) + 2 * (cfg.L * cfg.E // 8)
+
+
+def identity_bytes(cfg):
+    """Algorithmic bytes of one identity gather/combine pass: every source
+    row read once, every output row written once, token_index_map,
+    expert_token_indices and gates read once."""
+    s = cfg.elem_bytes
+    return 2 * cfg.L * cfg.d * s + 12 * cfg.L * cfg.K
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.f = open(self.path, "w")
+        self.proc = subprocess.Popen([exe, "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
+                                      "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                     stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(cfg, target_s=12.0, max_tokens=None):
+    """Time the CPU oracle (forward + backward) on the first L' tokens of the
+    workload, growing L' until one run takes about target_s seconds."""
+    import oracle.moe_oracle as O
+    Lp = 64
+    tokens_done, elapsed = 0, 0.0
+    while True:
+        # x, dY and the router are row-wise, so the first Lp rows of the
+        # workload are regenerated exactly (same ids, gates and weights)
+        sub = cfg.scaled(L=Lp)
+        inp = I.make_inputs(sub, "cpu")
+        t0 = time.perf_counter()
+        O.forward(inp["ids"], inp["gates"], inp["x"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        O.backward(inp["ids"], inp["gates"], inp["x"], inp["dY"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        dt = time.perf_counter() - t0
+        tokens_done, elapsed = Lp, dt
+        if dt >= target_s / 3 or Lp >= (max_tokens or cfg.L):
+            break
+        Lp = min(max_tokens or cfg.L, Lp * max(2, int(target_s / 3 / max(dt, 1e-3))))
+    return tokens_done / elapsed, tokens_done, elapsed
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ our arm
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_ours(args, rank, world, local_rank):
+    cfg = I.CONFIGS[args.config]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from mixture_experts_atomic_gb300.layer import MoELayer
+    inp = I.make_inputs(cfg, dev)
+    layer = MoELayer.for_config(cfg, dev)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    identity = cfg.act == "identity"
+    nf, nbk = 4, 6
+
+    def one_step(rec=None):
+        s = torch.cuda.current_stream()
+        if rec is not None:
+            rec["e0"].record(s)
+        layer.dispatch(inp["ids"])
+        if rec is not None:
+            rec["e1"].record(s)
+            with rec["fw"]:
+                layer.forward(inp["x"], inp["gates"], inp.get("W1"), inp.get("W2"), inp.get("W3"))
+            rec["e2"].record(s)
+            with rec["bw"]:
+                layer.backward(inp["dY"], inp["x"], inp["gates"], inp.get("W1"), inp.get("W2"), inp.get("W3"))
+            rec["e3"].record(s)
+        else:
+            layer.forward(inp["x"], inp["gates"], inp.get("W1"), inp.get("W2"), inp.get("W3"))
+            layer.backward(inp["dY"], inp["x"], inp["gates"], inp.get("W1"), inp.get("W2"), inp.get("W3"))
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        one_step()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0, "device error during warm-up"
+
+    recs = [{"e0": torch.cuda.Event(enable_timing=True), "e1": torch.cuda.Event(enable_timing=True),
+             "e2": torch.cuda.Event(enable_timing=True), "e3": torch.cuda.Event(enable_timing=True),
+             "fw": B.StageEvents(nf), "bw": B.StageEvents(nbk)} for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = B.moeblaze_kernel_launches()
+    for r in recs:
+        flush_l2(flush)
+        one_step(r)
+    torch.cuda.synchronize()
+    launches = B.moeblaze_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    assert layer.device_error() == 0, "device error during the timed steps"
+
+    step_ms = [r["e0"].elapsed_time(r["e3"]) for r in recs]
+    disp_ms = [r["e0"].elapsed_time(r["e1"]) for r in recs]
+    fwd_ms = [r["e1"].elapsed_time(r["e2"]) for r in recs]
+    bwd_ms = [r["e2"].elapsed_time(r["e3"]) for r in recs]
+    stages = {}
+    if not identity:
+        fw_names = ["up", "down", "convert_y"]
+        bw_names = ["dh", "dx", "dw12", "dw3", "convert_dx"]
+        per = {n: [] for n in fw_names + bw_names}
+        for r in recs:
+            for n, v in zip(fw_names, r["fw"].elapsed_ms()):
+                per[n].append(v)
+            for n, v in zip(bw_names, r["bw"].elapsed_ms()):
+                per[n].append(v)
+        stages = {n: statistics.mean(v) for n, v in per.items()}
+    stages["dispatch"] = statistics.mean(disp_ms)
+    stages["forward"] = statistics.mean(fwd_ms)
+    stages["backward"] = statistics.mean(bwd_ms)
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * cfg.L / (ms * 1e-3)
+
+    pk, src = peaks()
+    if identity:
+        nbytes = identity_bytes(cfg)
+        t_ms = statistics.mean(fwd_ms)
+        ach = nbytes / (t_ms * 1e-3) / 1e9
+        roof = {"kernel": "identity_combine_kernel (forward pass)", "bound": "hbm", "achieved": ach,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                "peak_source": src, "algorithmic_bytes": nbytes}
+    else:
+        fl = stage_flops(cfg)
+        dom = max(fl, key=lambda n: stages[n])
+        ach = fl[dom] / (stages[dom] * 1e-3) / 1e12
+        roof = {"kernel": f"moe_gemm_kernel<{dom}>", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None, "peak_source": src,
+                "algorithmic_flops": fl[dom],
+                "gemm_tflops_all_stages": sum(fl.values()) / (sum(stages[n] for n in fl) * 1e-3) / 1e12}
+    db = dispatch_bytes(cfg)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "config": {"workload": cfg.name, "L": cfg.L, "d": cfg.d, "h": cfg.h, "E": cfg.E, "K": cfg.K,
+                   "act": cfg.act, "tokens_per_step_per_gpu": cfg.L, "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "stages_ms": stages,
+        "dispatch_build": {"ms": stages["dispatch"], "algorithmic_bytes": db,
+                           "GB_per_s": db / (stages["dispatch"] * 1e-3) / 1e9},
+        "roofline": roof,
+        "gpu_launches": int(launches),
+        "gpu_launches_per_step": launches / max(1, args.steps),
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, cfg, layer, inp, dev, world)
+    del flush
+    return out
+
+
+def run_e2e(args, cfg, layer, inp, dev, world):
+    """Same step through the same C-ABI calls, inputs from pinned host memory
+    and y, dX read back to pinned host memory inside the timed region."""
+    host = {k: inp[k].cpu().pin_memory() for k in ("x", "ids", "gates", "dY")}
+    dbuf = {k: torch.empty_like(inp[k]) for k in host}
+    y_h = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
+    dx_h = torch.empty(layer.dX.shape, dtype=layer.dX.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
+    W = (inp.get("W1"), inp.get("W2"), inp.get("W3"))
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        layer.dispatch(dbuf["ids"])
+        layer.forward(dbuf["x"], dbuf["gates"], *W)
+        layer.backward(dbuf["dY"], dbuf["x"], dbuf["gates"], *W)
+        y_h.copy_(layer.y, non_blocking=True)
+        dx_h.copy_(layer.dX, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * cfg.L / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def run_reference(args, cfg):
+    """The CPU oracle as the reference arm: each step runs it on a bounded
+    sample of the workload's tokens (same shapes otherwise)."""
+    import oracle.moe_oracle as O
+    tps, ntok, dt = oracle_sample(cfg, target_s=6.0)
+    sub = cfg.scaled(L=ntok)
+    inp = I.make_inputs(sub, "cpu")
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        O.forward(inp["ids"], inp["gates"], inp["x"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        O.backward(inp["ids"], inp["gates"], inp["x"], inp["dY"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    v = ntok / statistics.mean(times)
+    cores = cpu_cores()
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded counter-based generator; random-init weights)",
+            "config": {"workload": cfg.name, "L": cfg.L, "d": cfg.d, "h": cfg.h, "E": cfg.E, "K": cfg.K,
+                       "act": cfg.act},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {ntok} tokens of the workload per step (same d, h, E, K)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=1, help="workload index (0..4); default: the SiLU bf16 layer")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = I.CONFIGS[args.config]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    B.lib()
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, ntok, dt = oracle_sample(cfg)
+        out["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                               "sample": f"first {ntok} tokens of the workload (same d, h, E, K), "
+                                         f"{dt:.1f} s of fp64 CPU work"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

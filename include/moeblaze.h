@@ -1,0 +1,208 @@
+/*
+ * moeblaze.h - C ABI of a GB300 (sm_103a) dropless top-K Mixture-of-Experts
+ * layer in the style of MoEBlaze ("MoEBlaze: Breaking the Memory Wall for
+ * Efficient MoE Training on Modern GPUs", MLSys 2026).
+ *
+ * The layer (MoEBlaze, awesome-system-papers page, section "核心方法"):
+ *   y[t] = sum_k g[t,k] * expert_{e}(x[t]),  e = topk_ids[t,k]
+ *   SwiGLU expert:  (SiLU(x W1_e) * (x W2_e)) W3_e
+ *   SiLU expert:    SiLU(x W1_e) W3_e
+ *   identity:       x
+ * computed without a routed (L*K, d) buffer: the dispatch builds integer
+ * index structures only, the expert GEMMs gather rows of x through them, and
+ * the down-projection is gate-weighted and reduced back into (L, d).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument named "device" is device memory owned by the
+ *     caller; the library never allocates or frees device memory and keeps
+ *     no state between calls (apart from a per-device SM count).
+ *   - Every device pointer must be 16-byte aligned (MOEBLAZE_ERR_INVALID_ARG
+ *     otherwise); row-major layouts, no padding between rows.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and is asynchronous, except dispatch_build with
+ *     validate != 0 and moeblaze_device_error, which synchronise `stream`.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned as a status; nothing is thrown across the ABI and there
+ *     is no CPU fallback.
+ *   - dtype: MOEBLAZE_BF16 = bf16 storage, fp32 accumulation (tensor cores,
+ *     needs d % 128 == 0 and h % 128 == 0); MOEBLAZE_F32 = fp32 storage and
+ *     fp32 SIMT arithmetic (no TF32), any d, h with d % 4 == 0 and h % 4 == 0.
+ *   - Limits: 1 <= K <= min(E, 8), 1 <= E <= 512, 0 <= L, L*K < 2^31.
+ */
+#ifndef MOEBLAZE_H
+#define MOEBLAZE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOEBLAZE_API __attribute__((visibility("default")))
+#else
+#define MOEBLAZE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* moeblaze_stream;
+
+typedef enum {
+  MOEBLAZE_OK = 0,
+  MOEBLAZE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, K > E */
+  MOEBLAZE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. bf16 with d % 128 != 0) */
+  MOEBLAZE_ERR_BAD_ROUTING = 3,  /* an id out of [0,E) or repeated within a token */
+  MOEBLAZE_ERR_WORKSPACE = 4,    /* workspace smaller than the matching *_bytes() */
+  MOEBLAZE_ERR_TIMEOUT = 5,      /* a device-side wait ran out; results invalid */
+  MOEBLAZE_ERR_CUDA = 6          /* a CUDA runtime/driver call failed */
+} moeblaze_status;
+
+enum { MOEBLAZE_F32 = 0, MOEBLAZE_BF16 = 1 };
+enum { MOEBLAZE_SWIGLU = 0, MOEBLAZE_SILU = 1, MOEBLAZE_IDENTITY = 2 };
+
+/* Layer shape.  L tokens, model dim d, expert hidden dim h (ignored for the
+ * identity expert), E experts, top-K slots per token. */
+typedef struct {
+  int64_t L;
+  int32_t d, h, E, K;
+  int32_t dtype;  /* MOEBLAZE_F32 | MOEBLAZE_BF16 */
+  int32_t act;    /* MOEBLAZE_SWIGLU | MOEBLAZE_SILU | MOEBLAZE_IDENTITY */
+} moeblaze_shape;
+
+/* The index structures of MoEBlaze (awesome-system-papers page, section
+ * "免物化 token dispatch", data-structure table).  All device, int32,
+ * written by moeblaze_dispatch_build:
+ *   expert_token_indices [L*K]  token ids expert by expert, ascending token id
+ *                                within an expert
+ *   expert_token_offsets [E+1]  expert e owns [off[e], off[e+1]); off[E] = L*K
+ *   token_expert_indices [L*K]  (L,K) row-major: the expert of (t,k) (= topk_ids)
+ *   token_index_map      [L*K]  (L,K) row-major: position of (t,k) in
+ *                                expert_token_indices
+ *   meta                         moeblaze_dispatch_meta_bytes() bytes, 16-byte
+ *                                aligned: per-expert counts, padded row offsets,
+ *                                the GEMM tile table and a device error word;
+ *                                read by forward/backward, opaque to the caller.
+ */
+typedef struct {
+  int32_t* expert_token_indices;
+  int32_t* expert_token_offsets;
+  int32_t* token_expert_indices;
+  int32_t* token_index_map;
+  void* meta;
+} moeblaze_dispatch;
+
+/* Byte sizes.  0 is a valid size (nothing needed).  An invalid shape gives 0;
+ * the matching entry point then reports the error. */
+MOEBLAZE_API size_t moeblaze_dispatch_meta_bytes(const moeblaze_shape* s);
+MOEBLAZE_API size_t moeblaze_dispatch_workspace_bytes(const moeblaze_shape* s);
+/* Activations kept from forward to backward: A = x W1 and (SwiGLU) B = x W2,
+ * expert-major with each expert's rows padded to a multiple of 128, in the
+ * layer dtype.  0 for the identity expert. */
+MOEBLAZE_API size_t moeblaze_saved_bytes(const moeblaze_shape* s);
+MOEBLAZE_API size_t moeblaze_forward_workspace_bytes(const moeblaze_shape* s);
+MOEBLAZE_API size_t moeblaze_backward_workspace_bytes(const moeblaze_shape* s);
+
+/*
+ * Atomic-free three-step dispatch build (MoEBlaze, awesome-system-papers
+ * page, section "Atomic-free 三步 dispatch 构建"):
+ *   1. a dense token-expert bitmap (bit-packed, one 32-bit word per expert
+ *      per 32 tokens), each (token, expert) bit written once;
+ *   2. per-expert counts by population count and warp reduction, prefix
+ *      sums into expert_token_offsets;
+ *   3. a tile scan of the bitmap giving each (token, slot) its final
+ *      position, then parallel writes of the three (L,K)-sized maps.
+ * topk_ids: device int32 (L,K) row-major, the router's top-K expert ids.
+ * out: the five device buffers above.  ws: device scratch of
+ * moeblaze_dispatch_workspace_bytes(s) bytes (contents on entry ignored).
+ * validate != 0: synchronise `stream` once and return
+ * MOEBLAZE_ERR_BAD_ROUTING if any id is out of range or repeated within a
+ * token.  With validate == 0 such ids leave the outputs unspecified (but all
+ * writes stay inside the buffers) and the device error word records them
+ * (see moeblaze_device_error).
+ */
+MOEBLAZE_API moeblaze_status moeblaze_dispatch_build(const moeblaze_shape* s, const int32_t* topk_ids,
+                                        const moeblaze_dispatch* out, void* ws, size_t ws_bytes,
+                                        int validate, moeblaze_stream stream);
+
+/*
+ * Forward pass (MoEBlaze, awesome-system-papers page, sections
+ * "免物化 token dispatch" (Forward) and "SwiGLU kernel 融合 + activation
+ * checkpoint"): for every expert, its rows of x are gathered on the fly
+ * through expert_token_indices, W1 and W2 are applied from one load of x,
+ * SiLU(a)*b is formed in the GEMM epilogue, and the down-projection output
+ * is gate-weighted and reduced into y through the index maps.
+ *   x      device (L,d) dtype          gates device (L,K) fp32
+ *   disp   as written by moeblaze_dispatch_build for the same ids
+ *   W1, W2 device (E,d,h) dtype        W3 device (E,h,d) dtype
+ *          (W2 NULL for SiLU; W1, W2, W3 NULL for identity)
+ *   y      device (L,d) dtype, overwritten
+ *   saved  device moeblaze_saved_bytes(s) bytes: A (and B), overwritten;
+ *          needed by moeblaze_backward (NULL allowed when the size is 0)
+ *   ws     device moeblaze_forward_workspace_bytes(s) bytes of scratch
+ * The fp32 reduction into y sums the K contributions of a token in an
+ * unspecified order (bitwise reproducible for K <= 2).
+ */
+MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const float* gates,
+                                 const moeblaze_dispatch* disp, const void* W1, const void* W2,
+                                 const void* W3, void* y, void* saved, void* ws, size_t ws_bytes,
+                                 moeblaze_stream stream);
+
+/*
+ * Backward pass of the loss <y, dY> with ids and gates held constant
+ * (MoEBlaze, awesome-system-papers page, sections "免物化 token dispatch"
+ * (Backward) and "SwiGLU kernel 融合 + activation checkpoint"): dY is
+ * gathered to the expert rows through the same indices (no (L*K, d)
+ * expansion), SiLU(A) is recomputed from the saved A and B, the two
+ * branches' input gradients are accumulated in one accumulator, and dX is
+ * reduced back into (L, d).
+ *   dY      device (L,d) dtype                 x, gates, disp, W*: as forward
+ *   saved   as written by moeblaze_forward
+ *   dX      device (L,d) dtype, overwritten
+ *   dW1,dW2 device (E,d,h) dtype, overwritten  dW3 device (E,h,d) dtype, overwritten
+ *           (dW2 NULL for SiLU; all three NULL for identity)
+ *   ws      device moeblaze_backward_workspace_bytes(s) bytes of scratch
+ */
+MOEBLAZE_API moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x,
+                                  const float* gates, const moeblaze_dispatch* disp,
+                                  const void* W1, const void* W2, const void* W3,
+                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3,
+                                  void* ws, size_t ws_bytes, moeblaze_stream stream);
+
+/* Synchronise `stream` and read the device error word of `disp->meta`:
+ * *code = 0 when every kernel since the last dispatch_build on this meta
+ * finished normally; otherwise a bitwise OR of 1 (bad routing) and 2 (a
+ * bounded device-side wait ran out).  Returns MOEBLAZE_ERR_BAD_ROUTING or
+ * MOEBLAZE_ERR_TIMEOUT accordingly, MOEBLAZE_OK when *code == 0. */
+MOEBLAZE_API moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp,
+                                      int32_t* code, moeblaze_stream stream);
+
+/* Diagnostics.
+ *
+ * moeblaze_set_stage_events: when `events` is non-NULL, later
+ * moeblaze_forward / moeblaze_backward calls made from the calling thread
+ * record events[i] (each a cudaEvent_t created by the caller) on the call's
+ * stream at the stage boundaries of the bf16/fp32 expert paths:
+ *   forward : [0] before the up-projection, [1] after it, [2] after the
+ *             down-projection + combine, [3] after the final conversion;
+ *   backward: [0] before the dH GEMM, [1] after it, [2] after the dX GEMM,
+ *             [3] after the dW1/dW2 GEMM, [4] after the dW3 GEMM,
+ *             [5] after the final conversion.
+ * Only the first `n` events are recorded.  NULL switches recording off.
+ *
+ * moeblaze_kernel_launches: number of CUDA kernels this library has launched
+ * in the process so far (memsets and copies not counted). */
+MOEBLAZE_API void moeblaze_set_stage_events(void** events, int32_t n);
+MOEBLAZE_API int64_t moeblaze_kernel_launches(void);
+
+/* Static description of a status code. */
+MOEBLAZE_API const char* moeblaze_status_string(moeblaze_status st);
+
+/* Library version, major*10000 + minor*100 + patch. */
+MOEBLAZE_API int32_t moeblaze_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEBLAZE_H */

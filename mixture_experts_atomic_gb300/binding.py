@@ -1,0 +1,293 @@
+"""ctypes binding of libmoeblaze.so: the C entry points under the same names
+(argument marshalling only), plus small torch helpers that allocate the
+caller-owned buffers and pass their device pointers and the current stream.
+
+Every compute step runs in the library's CUDA kernels; there is no Python or
+CPU fallback.  Loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoeblaze.so")
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BAD_ROUTING, ERR_WORKSPACE, ERR_TIMEOUT, ERR_CUDA = range(7)
+F32, BF16 = 0, 1
+SWIGLU, SILU, IDENTITY = 0, 1, 2
+ACT = {"swiglu": SWIGLU, "silu": SILU, "identity": IDENTITY}
+DTYPE = {torch.float32: F32, torch.bfloat16: BF16}
+
+# names exported by include/moeblaze.h
+EXPORTS = [
+    "moeblaze_dispatch_meta_bytes", "moeblaze_dispatch_workspace_bytes", "moeblaze_saved_bytes",
+    "moeblaze_forward_workspace_bytes", "moeblaze_backward_workspace_bytes", "moeblaze_dispatch_build",
+    "moeblaze_forward", "moeblaze_backward", "moeblaze_device_error", "moeblaze_status_string",
+    "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
+]
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32)]
+
+
+class Dispatch(ctypes.Structure):
+    _fields_ = [("expert_token_indices", ctypes.c_void_p), ("expert_token_offsets", ctypes.c_void_p),
+                ("token_expert_indices", ctypes.c_void_p), ("token_index_map", ctypes.c_void_p),
+                ("meta", ctypes.c_void_p)]
+
+
+class MoEBlazeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib():
+    """The loaded library; raises if it is missing (build it first)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmoeblaze.so not built ({_LIB_PATH}); run "
+                               "`python -m mixture_experts_atomic_gb300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        sz = ctypes.c_size_t
+        P = ctypes.c_void_p
+        SP = ctypes.POINTER(Shape)
+        DP = ctypes.POINTER(Dispatch)
+        for n in ["moeblaze_dispatch_meta_bytes", "moeblaze_dispatch_workspace_bytes", "moeblaze_saved_bytes",
+                  "moeblaze_forward_workspace_bytes", "moeblaze_backward_workspace_bytes"]:
+            getattr(L, n).argtypes = [SP]
+            getattr(L, n).restype = sz
+        L.moeblaze_dispatch_build.argtypes = [SP, P, DP, P, sz, ctypes.c_int, P]
+        L.moeblaze_dispatch_build.restype = ctypes.c_int
+        L.moeblaze_forward.argtypes = [SP, P, P, DP, P, P, P, P, P, P, sz, P]
+        L.moeblaze_forward.restype = ctypes.c_int
+        L.moeblaze_backward.argtypes = [SP, P, P, P, DP, P, P, P, P, P, P, P, P, P, sz, P]
+        L.moeblaze_backward.restype = ctypes.c_int
+        L.moeblaze_device_error.argtypes = [SP, DP, ctypes.POINTER(ctypes.c_int32), P]
+        L.moeblaze_device_error.restype = ctypes.c_int
+        L.moeblaze_status_string.argtypes = [ctypes.c_int]
+        L.moeblaze_status_string.restype = ctypes.c_char_p
+        L.moeblaze_version.argtypes = []
+        L.moeblaze_version.restype = ctypes.c_int32
+        L.moeblaze_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
+        L.moeblaze_set_stage_events.restype = None
+        L.moeblaze_kernel_launches.argtypes = []
+        L.moeblaze_kernel_launches.restype = ctypes.c_int64
+        _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().moeblaze_status_string(st).decode()
+
+
+# ---------------------------------------------------------------- C names
+
+def moeblaze_dispatch_meta_bytes(shape: Shape) -> int:
+    return lib().moeblaze_dispatch_meta_bytes(ctypes.byref(shape))
+
+
+def moeblaze_dispatch_workspace_bytes(shape: Shape) -> int:
+    return lib().moeblaze_dispatch_workspace_bytes(ctypes.byref(shape))
+
+
+def moeblaze_saved_bytes(shape: Shape) -> int:
+    return lib().moeblaze_saved_bytes(ctypes.byref(shape))
+
+
+def moeblaze_forward_workspace_bytes(shape: Shape) -> int:
+    return lib().moeblaze_forward_workspace_bytes(ctypes.byref(shape))
+
+
+def moeblaze_backward_workspace_bytes(shape: Shape) -> int:
+    return lib().moeblaze_backward_workspace_bytes(ctypes.byref(shape))
+
+
+def moeblaze_dispatch_build(shape, topk_ids, disp, ws, ws_bytes, validate, stream) -> int:
+    return lib().moeblaze_dispatch_build(ctypes.byref(shape), topk_ids, ctypes.byref(disp), ws, ws_bytes,
+                                         int(validate), stream)
+
+
+def moeblaze_forward(shape, x, gates, disp, W1, W2, W3, y, saved, ws, ws_bytes, stream) -> int:
+    return lib().moeblaze_forward(ctypes.byref(shape), x, gates, ctypes.byref(disp), W1, W2, W3, y, saved, ws,
+                                  ws_bytes, stream)
+
+
+def moeblaze_backward(shape, dY, x, gates, disp, W1, W2, W3, saved, dX, dW1, dW2, dW3, ws, ws_bytes, stream) -> int:
+    return lib().moeblaze_backward(ctypes.byref(shape), dY, x, gates, ctypes.byref(disp), W1, W2, W3, saved, dX,
+                                   dW1, dW2, dW3, ws, ws_bytes, stream)
+
+
+def moeblaze_device_error(shape, disp, stream):
+    code = ctypes.c_int32(0)
+    st = lib().moeblaze_device_error(ctypes.byref(shape), ctypes.byref(disp), ctypes.byref(code), stream)
+    return st, code.value
+
+
+def moeblaze_set_stage_events(events, n: int) -> None:
+    lib().moeblaze_set_stage_events(events, int(n))
+
+
+def moeblaze_kernel_launches() -> int:
+    return int(lib().moeblaze_kernel_launches())
+
+
+# ---------------------------------------------------------------- torch helpers
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_shape(L, d, h, E, K, dtype, act) -> Shape:
+    dt = DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    a = ACT[act] if isinstance(act, str) else int(act)
+    return Shape(int(L), int(d), int(h), int(E), int(K), dt, a)
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise MoEBlazeError(st, where)
+
+
+@dataclass
+class DispatchBuffers:
+    shape: Shape
+    expert_token_indices: torch.Tensor
+    expert_token_offsets: torch.Tensor
+    token_expert_indices: torch.Tensor
+    token_index_map: torch.Tensor
+    meta: torch.Tensor
+    ws: torch.Tensor
+
+    def struct(self) -> Dispatch:
+        return Dispatch(self.expert_token_indices.data_ptr(), self.expert_token_offsets.data_ptr(),
+                        self.token_expert_indices.data_ptr(), self.token_index_map.data_ptr(), self.meta.data_ptr())
+
+
+def _bytes(n: int, device) -> torch.Tensor:
+    # 256-byte aligned device buffer of at least n bytes (torch allocations are)
+    return torch.empty(max(int(n), 16), dtype=torch.uint8, device=device)
+
+
+def alloc_dispatch(shape: Shape, device="cuda") -> DispatchBuffers:
+    LK = shape.L * shape.K
+    i32 = dict(dtype=torch.int32, device=device)
+    return DispatchBuffers(
+        shape,
+        torch.empty(max(LK, 4), **i32),
+        torch.empty(shape.E + 1 + 3, **i32),
+        torch.empty(max(LK, 4), **i32),
+        torch.empty(max(LK, 4), **i32),
+        _bytes(moeblaze_dispatch_meta_bytes(shape), device),
+        _bytes(moeblaze_dispatch_workspace_bytes(shape), device),
+    )
+
+
+def dispatch_build(shape: Shape, topk_ids: torch.Tensor, bufs: Optional[DispatchBuffers] = None,
+                   validate: bool = False, stream=None) -> DispatchBuffers:
+    """Run the three-step dispatch build; returns the buffers holding the
+    index structures (views: [:L*K], [:E+1])."""
+    assert topk_ids.is_cuda and topk_ids.dtype == torch.int32 and topk_ids.is_contiguous()
+    if bufs is None:
+        bufs = alloc_dispatch(shape, topk_ids.device)
+    d = bufs.struct()
+    st = moeblaze_dispatch_build(shape, _ptr(topk_ids), d, _ptr(bufs.ws), bufs.ws.numel(), validate, _stream(stream))
+    _check(st, "moeblaze_dispatch_build")
+    return bufs
+
+
+def index_views(shape: Shape, bufs: DispatchBuffers):
+    LK = shape.L * shape.K
+    return (bufs.expert_token_indices[:LK], bufs.expert_token_offsets[:shape.E + 1],
+            bufs.token_expert_indices[:LK].view(shape.L, shape.K), bufs.token_index_map[:LK].view(shape.L, shape.K))
+
+
+@dataclass
+class LayerBuffers:
+    saved: torch.Tensor
+    fwd_ws: torch.Tensor
+    bwd_ws: torch.Tensor
+
+
+def alloc_layer(shape: Shape, device="cuda") -> LayerBuffers:
+    return LayerBuffers(_bytes(moeblaze_saved_bytes(shape), device),
+                        _bytes(moeblaze_forward_workspace_bytes(shape), device),
+                        _bytes(moeblaze_backward_workspace_bytes(shape), device))
+
+
+def forward(shape: Shape, x, gates, disp: DispatchBuffers, W1, W2, W3, y, layer: LayerBuffers, stream=None):
+    st = moeblaze_forward(shape, _ptr(x), _ptr(gates), disp.struct(), _ptr(W1), _ptr(W2), _ptr(W3), _ptr(y),
+                          _ptr(layer.saved), _ptr(layer.fwd_ws), layer.fwd_ws.numel(), _stream(stream))
+    _check(st, "moeblaze_forward")
+    return y
+
+
+def backward(shape: Shape, dY, x, gates, disp: DispatchBuffers, W1, W2, W3, layer: LayerBuffers, dX, dW1, dW2, dW3,
+             stream=None):
+    st = moeblaze_backward(shape, _ptr(dY), _ptr(x), _ptr(gates), disp.struct(), _ptr(W1), _ptr(W2), _ptr(W3),
+                           _ptr(layer.saved), _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dW3), _ptr(layer.bwd_ws),
+                           layer.bwd_ws.numel(), _stream(stream))
+    _check(st, "moeblaze_backward")
+
+
+class StageEvents:
+    """CUDA events the library records at its stage boundaries (see
+    moeblaze_set_stage_events); use as a context manager around one call."""
+
+    def __init__(self, n: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in self.events:  # torch creates the CUDA event on its first record
+            e.record()
+        torch.cuda.current_stream().synchronize()
+        self._arr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
+
+    def __enter__(self):
+        moeblaze_set_stage_events(self._arr, len(self.events))
+        return self
+
+    def __exit__(self, *exc):
+        moeblaze_set_stage_events(None, 0)
+        return False
+
+    def elapsed_ms(self):
+        return [self.events[i].elapsed_time(self.events[i + 1]) for i in range(len(self.events) - 1)]
+
+
+def device_error(shape: Shape, disp: DispatchBuffers, stream=None) -> int:
+    st, code = moeblaze_device_error(shape, disp.struct(), _stream(stream))
+    if st not in (OK, ERR_BAD_ROUTING, ERR_TIMEOUT):
+        raise MoEBlazeError(st, "moeblaze_device_error")
+    return code
+
+
+def saved_views(shape: Shape, layer: LayerBuffers, dtype):
+    """(A, B) views of the saved checkpoint: (padded_rows, h) each (B None for SiLU)."""
+    es = 4 if dtype == torch.float32 else 2
+    h = shape.h
+    nb = 2 if shape.act == SWIGLU else 1
+    rows = moeblaze_saved_bytes(shape) // (nb * h * es)
+    t = layer.saved[: rows * nb * h * es].view(dtype).view(nb, rows, h)
+    return t[0], (t[1] if nb == 2 else None)
+
+
+def meta_arrays(shape: Shape, disp: DispatchBuffers):
+    """Host copies of (num_m_tiles, n_e, pad_off, order) from the meta buffer."""
+    m = disp.meta.view(torch.int32).cpu()
+    E = shape.E
+    n_e = m[8:8 + E]
+    pad = m[8 + E:8 + 2 * E + 1]
+    order = m[8 + 2 * E + 1:8 + 3 * E + 1]
+    return int(m[1]), n_e, pad, order

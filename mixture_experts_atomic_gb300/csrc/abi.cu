@@ -1,0 +1,252 @@
+// extern "C" entry points of the moeblaze library (declared in
+// include/moeblaze.h): argument validation, scratch carving and the order of
+// the stages; every stage runs in the kernels of dispatch.cu, identity.cu,
+// simt.cu and gemm_tc.cu.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moeblaze {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+std::atomic<int64_t> g_launches{0};
+thread_local void** g_events = nullptr;
+thread_local int32_t g_nevents = 0;
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void stage_event(int i, cudaStream_t st) {
+  if (g_events && i < g_nevents && g_events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_events[i]), st);
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// shape checks shared by every entry point
+moeblaze_status check_shape(const moeblaze_shape* s) {
+  if (!s) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L < 0 || s->E < 1 || s->K < 1 || s->d < 1) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->K > s->E) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->dtype != MOEBLAZE_F32 && s->dtype != MOEBLAZE_BF16) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->act != MOEBLAZE_SWIGLU && s->act != MOEBLAZE_SILU && s->act != MOEBLAZE_IDENTITY)
+    return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->act != MOEBLAZE_IDENTITY && s->h < 1) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->E > kMaxE || s->K > kMaxK) return MOEBLAZE_ERR_UNSUPPORTED;
+  if (s->L * (int64_t)s->K + (int64_t)s->E * kRowPad >= (int64_t(1) << 31)) return MOEBLAZE_ERR_UNSUPPORTED;
+  if (s->act == MOEBLAZE_IDENTITY) {
+    if (s->d % (s->dtype == MOEBLAZE_BF16 ? 8 : 4) != 0) return MOEBLAZE_ERR_UNSUPPORTED;
+  } else if (s->dtype == MOEBLAZE_BF16) {
+    if (s->d % 128 != 0 || s->h % 128 != 0) return MOEBLAZE_ERR_UNSUPPORTED;
+  } else {
+    if (s->d % 4 != 0 || s->h % 4 != 0) return MOEBLAZE_ERR_UNSUPPORTED;
+  }
+  return MOEBLAZE_OK;
+}
+
+moeblaze_status check_dispatch(const moeblaze_dispatch* d) {
+  if (!d) return MOEBLAZE_ERR_INVALID_ARG;
+  const void* ps[5] = {d->expert_token_indices, d->expert_token_offsets, d->token_expert_indices, d->token_index_map,
+                       d->meta};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return MOEBLAZE_ERR_INVALID_ARG;
+  return MOEBLAZE_OK;
+}
+
+bool ok_ptr(const void* p) { return p && aligned16(p); }
+
+size_t elem(const moeblaze_shape* s) { return s->dtype == MOEBLAZE_BF16 ? 2 : 4; }
+int nbranch(const moeblaze_shape* s) { return s->act == MOEBLAZE_SWIGLU ? 2 : 1; }
+
+// forward scratch: H (rows x h) | y32 (L x d fp32, bf16 only)
+// backward scratch: dAB (rows x nb*h) | Hg (rows x h) | dX32 (L x d fp32, bf16 only)
+size_t fwd_ws(const moeblaze_shape* s) {
+  if (s->act == MOEBLAZE_IDENTITY) return 0;
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  size_t b = align_up((size_t)rows * s->h * elem(s), 256);
+  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256);
+  return b;
+}
+size_t bwd_ws(const moeblaze_shape* s) {
+  if (s->act == MOEBLAZE_IDENTITY) return 0;
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  size_t b = align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256);
+  b += align_up((size_t)rows * s->h * elem(s), 256);
+  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256);
+  return b;
+}
+
+moeblaze_status zero_weight_grads(const moeblaze_shape* s, void* dW1, void* dW2, void* dW3, cudaStream_t st) {
+  const size_t n = (size_t)s->E * s->d * s->h * elem(s);
+  MB_CUDA(cudaMemsetAsync(dW1, 0, n, st));
+  if (dW2) MB_CUDA(cudaMemsetAsync(dW2, 0, n, st));
+  MB_CUDA(cudaMemsetAsync(dW3, 0, n, st));
+  return MOEBLAZE_OK;
+}
+
+}  // namespace
+}  // namespace moeblaze
+
+using namespace moeblaze;
+
+extern "C" {
+
+int32_t moeblaze_version(void) { return 10000; }
+
+void moeblaze_set_stage_events(void** events, int32_t n) {
+  g_events = events;
+  g_nevents = events ? n : 0;
+}
+
+int64_t moeblaze_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moeblaze_status_string(moeblaze_status st) {
+  switch (st) {
+    case MOEBLAZE_OK: return "ok";
+    case MOEBLAZE_ERR_INVALID_ARG: return "invalid argument";
+    case MOEBLAZE_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case MOEBLAZE_ERR_BAD_ROUTING: return "bad routing: expert id out of range or repeated within a token";
+    case MOEBLAZE_ERR_WORKSPACE: return "workspace too small";
+    case MOEBLAZE_ERR_TIMEOUT: return "a device-side wait timed out";
+    case MOEBLAZE_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t moeblaze_dispatch_meta_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK) return 0;
+  return meta_bytes(s->L * s->K, s->E);
+}
+
+size_t moeblaze_dispatch_workspace_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK) return 0;
+  return dispatch_ws_bytes(*s);
+}
+
+size_t moeblaze_saved_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK || s->act == MOEBLAZE_IDENTITY) return 0;
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  return (size_t)rows * nbranch(s) * s->h * elem(s);
+}
+
+size_t moeblaze_forward_workspace_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK) return 0;
+  return fwd_ws(s);
+}
+
+size_t moeblaze_backward_workspace_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK) return 0;
+  return bwd_ws(s);
+}
+
+moeblaze_status moeblaze_dispatch_build(const moeblaze_shape* s, const int32_t* topk_ids,
+                                        const moeblaze_dispatch* out, void* ws, size_t ws_bytes, int validate,
+                                        moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if ((r = check_dispatch(out)) != MOEBLAZE_OK) return r;
+  if (s->L > 0 && !ok_ptr(topk_ids)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (ws_bytes < dispatch_ws_bytes(*s)) return MOEBLAZE_ERR_WORKSPACE;
+  if (!ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  r = launch_dispatch(*s, topk_ids, *out, ws, st);
+  if (r != MOEBLAZE_OK || !validate) return r;
+  int32_t code = 0;
+  MB_CUDA(cudaMemcpyAsync(&code, out->meta, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MB_CUDA(cudaStreamSynchronize(st));
+  return (code & kErrBadRouting) ? MOEBLAZE_ERR_BAD_ROUTING : MOEBLAZE_OK;
+}
+
+moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const float* gates,
+                                 const moeblaze_dispatch* disp, const void* W1, const void* W2, const void* W3,
+                                 void* y, void* saved, void* ws, size_t ws_bytes, moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if ((r = check_dispatch(disp)) != MOEBLAZE_OK) return r;
+  // token-sized buffers may be empty (NULL) when L == 0
+  const bool tok_ok = s->L == 0 || (ok_ptr(x) && ok_ptr(gates) && ok_ptr(y));
+  if (!tok_ok) return MOEBLAZE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (s->act == MOEBLAZE_IDENTITY) return launch_identity_combine(*s, x, *disp, gates, y, st);
+  const bool sw = s->act == MOEBLAZE_SWIGLU;
+  if (!ok_ptr(W1) || !ok_ptr(W3) || (sw && !ok_ptr(W2)) || !ok_ptr(saved)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (ws_bytes < fwd_ws(s)) return MOEBLAZE_ERR_WORKSPACE;
+  if (!ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L == 0) return MOEBLAZE_OK;
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  char* w = reinterpret_cast<char*>(ws);
+  if (s->dtype == MOEBLAZE_F32) {
+    return simt_forward(*s, (const float*)x, gates, *disp, (const float*)W1, sw ? (const float*)W2 : nullptr,
+                        (const float*)W3, (float*)y, (float*)saved, (float*)w, st);
+  }
+  __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(w);
+  float* y32 = reinterpret_cast<float*>(w + align_up((size_t)rows * s->h * 2, 256));
+  return tc_forward(*s, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
+                    sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (__nv_bfloat16*)y,
+                    (__nv_bfloat16*)saved, H, y32, st);
+}
+
+moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x, const float* gates,
+                                  const moeblaze_dispatch* disp, const void* W1, const void* W2, const void* W3,
+                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3, void* ws,
+                                  size_t ws_bytes, moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if ((r = check_dispatch(disp)) != MOEBLAZE_OK) return r;
+  const bool tok_ok = s->L == 0 || (ok_ptr(dY) && ok_ptr(gates) && ok_ptr(dX) && ok_ptr(x));
+  if (!tok_ok) return MOEBLAZE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (s->act == MOEBLAZE_IDENTITY) return launch_identity_combine(*s, dY, *disp, gates, dX, st);
+  const bool sw = s->act == MOEBLAZE_SWIGLU;
+  if (!ok_ptr(W1) || !ok_ptr(W3) || (sw && !ok_ptr(W2)) || !ok_ptr(saved)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (!ok_ptr(dW1) || !ok_ptr(dW3) || (sw && !ok_ptr(dW2))) return MOEBLAZE_ERR_INVALID_ARG;
+  if (ws_bytes < bwd_ws(s)) return MOEBLAZE_ERR_WORKSPACE;
+  if (!ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L == 0) return zero_weight_grads(s, dW1, sw ? dW2 : nullptr, dW3, st);
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  char* w = reinterpret_cast<char*>(ws);
+  const size_t es = elem(s);
+  char* dAB = w;
+  char* Hg = w + align_up((size_t)rows * nbranch(s) * s->h * es, 256);
+  char* dX32 = Hg + align_up((size_t)rows * s->h * es, 256);
+  if (s->dtype == MOEBLAZE_F32) {
+    return simt_backward(*s, (const float*)dY, (const float*)x, gates, *disp, (const float*)W1,
+                         sw ? (const float*)W2 : nullptr, (const float*)W3, (const float*)saved, (float*)dX,
+                         (float*)dW1, sw ? (float*)dW2 : nullptr, (float*)dW3, (float*)dAB, (float*)Hg, st);
+  }
+  return tc_backward(*s, (const __nv_bfloat16*)dY, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
+                     sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (const __nv_bfloat16*)saved,
+                     (__nv_bfloat16*)dX, (__nv_bfloat16*)dW1, sw ? (__nv_bfloat16*)dW2 : nullptr, (__nv_bfloat16*)dW3,
+                     (__nv_bfloat16*)dAB, (__nv_bfloat16*)Hg, (float*)dX32, st);
+}
+
+moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp, int32_t* code,
+                                      moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if (!disp || !ok_ptr(disp->meta) || !code) return MOEBLAZE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t c = 0;
+  MB_CUDA(cudaMemcpyAsync(&c, disp->meta, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MB_CUDA(cudaStreamSynchronize(st));
+  *code = c;
+  if (c & kErrBadRouting) return MOEBLAZE_ERR_BAD_ROUTING;
+  if (c & kErrTimeout) return MOEBLAZE_ERR_TIMEOUT;
+  return MOEBLAZE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+// Internal declarations of the moeblaze library: shape-derived sizes, the
+// layout of the dispatch meta buffer, inline-PTX wrappers for mbarrier, TMA
+// and tcgen05 (sm_103a), and the launchers each .cu file provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moeblaze.h"
+
+namespace moeblaze {
+
+// ---------------------------------------------------------------- constants
+constexpr int kChunkTokens = 1024;       // tokens per dispatch chunk (32 bitmap words)
+constexpr int kChunkWords = kChunkTokens / 32;
+constexpr int kRowPad = 128;             // expert row segments are padded to this
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 8;
+
+// device error word bits
+constexpr int kErrBadRouting = 1;
+constexpr int kErrTimeout = 2;
+
+// ---------------------------------------------------------------- meta layout
+// The meta buffer written by the dispatch build and read by the GEMMs:
+//   int32 header[8]          err, num_m_tiles, padded_rows, reserved...
+//   int32 n_e[E]             tokens per expert
+//   int32 pad_off[E+1]       padded row offset of each expert (multiples of 128)
+//   int32 order[E]           experts by descending n_e (ties: lower id first)
+//   int32 tile_expert[MT]    expert of each 128-row tile, MT = max_m_tiles
+struct MetaView {
+  int32_t* err;
+  int32_t* num_m_tiles;
+  int32_t* padded_rows;
+  int32_t* n_e;
+  int32_t* pad_off;
+  int32_t* order;
+  int32_t* tile_expert;
+};
+
+inline int64_t max_padded_rows(int64_t LK, int E) {
+  int64_t r = LK + (int64_t)E * (kRowPad - 1);
+  return (r + kRowPad - 1) / kRowPad * kRowPad;
+}
+inline int64_t max_m_tiles(int64_t LK, int E) { return max_padded_rows(LK, E) / kRowPad; }
+inline int64_t num_chunks(int64_t L) { return (L + kChunkTokens - 1) / kChunkTokens; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline MetaView meta_view(void* meta, int E) {
+  int32_t* p = reinterpret_cast<int32_t*>(meta);
+  MetaView m;
+  m.err = p + 0;
+  m.num_m_tiles = p + 1;
+  m.padded_rows = p + 2;
+  int32_t* q = p + 8;
+  m.n_e = q; q += E;
+  m.pad_off = q; q += E + 1;
+  m.order = q; q += E;
+  m.tile_expert = q;
+  return m;
+}
+inline size_t meta_bytes(int64_t LK, int E) {
+  return align_up(sizeof(int32_t) * (8 + E + (E + 1) + E + (size_t)max_m_tiles(LK, E)), 256);
+}
+
+// ---------------------------------------------------------------- status helper
+#define MB_CUDA(call)                                           \
+  do {                                                          \
+    cudaError_t e_ = (call);                                    \
+    if (e_ != cudaSuccess) return MOEBLAZE_ERR_CUDA;            \
+  } while (0)
+
+// ---------------------------------------------------------------- launchers
+// dispatch.cu
+moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
+                                void* ws, cudaStream_t st);
+size_t dispatch_ws_bytes(const moeblaze_shape& s);
+
+// identity.cu
+moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,
+                                        const float* gates, void* dst, cudaStream_t st);
+
+// simt.cu (fp32 path)
+moeblaze_status simt_forward(const moeblaze_shape& s, const float* x, const float* gates,
+                             const moeblaze_dispatch& disp, const float* W1, const float* W2, const float* W3,
+                             float* y, float* saved, float* wsH, cudaStream_t st);
+moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const float* x, const float* gates,
+                              const moeblaze_dispatch& disp, const float* W1, const float* W2, const float* W3,
+                              const float* saved, float* dX, float* dW1, float* dW2, float* dW3,
+                              float* wsdAB, float* wsHg, cudaStream_t st);
+
+// gemm_tc.cu (bf16 tensor-core path)
+moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, const float* gates,
+                           const moeblaze_dispatch& disp, const __nv_bfloat16* W1, const __nv_bfloat16* W2,
+                           const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved,
+                           __nv_bfloat16* wsH, float* wsY32, cudaStream_t st);
+moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, const __nv_bfloat16* x,
+                            const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
+                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
+                            __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
+                            __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
+
+// shared helpers (abi.cu)
+int sm_count();
+void count_launch(int n = 1);
+// record stage-boundary event i on st if the caller asked for it
+void stage_event(int i, cudaStream_t st);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+
+// bf16x2 packing of two fp32 values, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(v);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace moeblaze

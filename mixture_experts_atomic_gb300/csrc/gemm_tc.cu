@@ -1,0 +1,815 @@
+// bf16 expert GEMMs of the layer on the sm_103a tensor cores (tcgen05 + TMEM,
+// operands staged by TMA), with the index-driven row gather and the fused
+// epilogues of MoEBlaze (awesome-system-papers page, sections
+// "免物化 token dispatch" and "SwiGLU kernel 融合 + activation checkpoint").
+//
+// One persistent, warp-specialised kernel template serves all six GEMMs:
+//   warp 0      producer: TMA loads of the A and B tiles into a 4-stage ring;
+//               routed rows of x / dY are fetched with tile::gather4 (four
+//               arbitrary rows per instruction) straight from the (L,d)
+//               tensor through expert_token_indices - no routed buffer.
+//   warp 1      TMEM allocator and MMA issuer: one thread issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N<=256, K=16),
+//               fp32 accumulators in TMEM, two accumulator buffers so the
+//               epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator rows and the fused
+//               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward,
+//               plain stores).
+//
+// Row space: an expert's routed rows form a segment of a padded row space,
+// [pad_off[e], pad_off[e+1]), 128-row aligned, so every 128-row M tile
+// belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
+// routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
+// gather a valid token and are zero where they feed a reduction.
+//
+// Stage                          A (M x K)                B (K x N)             epilogue
+//  UP_SWIGLU  a,b = X W1,X W2    x rows via D1 (gather4)  [W1_e | W2_e] tiles   A,B (saved), H=SiLU(a)b
+//  UP_SILU    a = X W1           x rows via D1            W1_e                  A (saved), H=SiLU(a)
+//  DOWN       Y = H W3           H rows                   W3_e                  y32[t] += g Y   (red.add)
+//  DH_*       dH = dY W3^T       dY rows via D1           W3_e (K-major)        dA, dB, Hg (SwiGLU bwd)
+//  DX         [dA|dB][W1|W2]^T   dAB rows                 W1_e^T then W2_e^T    dX32[t] += .    (red.add)
+//  DW12/DW1   X^T [dA|dB]        x rows via D1 along K    dAB rows (MN-major)   dW1, dW2
+//  DW3        Hg^T dY            Hg rows (MN-major)       dY rows via D1        dW3
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// kErrTimeout in the device error word, drains its own copies and MMAs with
+// bounded waits, frees TMEM and returns.
+#include "common.cuh"
+
+namespace moeblaze {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+
+enum Mode : int { UP_SWIGLU = 0, UP_SILU, DOWN, DH_SWIGLU, DH_SILU, DX, DW12, DW1, DW3 };
+
+__host__ __device__ constexpr bool is_wgrad(int m) { return m == DW12 || m == DW1 || m == DW3; }
+__host__ __device__ constexpr bool is_dual(int m) { return m == UP_SWIGLU || m == DW12; }
+__host__ __device__ constexpr bool a_mn_major(int m) { return is_wgrad(m); }
+__host__ __device__ constexpr bool b_k_major(int m) { return m == DH_SWIGLU || m == DH_SILU || m == DX; }
+// columns per n-tile (per branch for the dual stages)
+__host__ __device__ constexpr int tile_n(int m) { return is_dual(m) ? 128 : 256; }
+
+struct Params {
+  CUtensorMap tmA;
+  CUtensorMap tmB0;
+  CUtensorMap tmB1;
+  const int32_t* D1;
+  const int32_t* D2;
+  const int32_t* D3;
+  const float* gates;
+  MetaView meta;
+  int64_t L;
+  int d, h, E, K;
+  int N;            // output columns (per branch for dual stages)
+  int kblocks;      // row stages: reduction length / 64
+  int ksplit;       // DX: k-blocks taken from W1 before switching to W2
+  int n_tiles;
+  int m_tiles_w;    // weight-gradient stages: output rows / 128
+  int64_t total_w;  // weight-gradient stages: number of tiles
+  __nv_bfloat16* o0;
+  __nv_bfloat16* o1;
+  __nv_bfloat16* o2;
+  const __nv_bfloat16* i0;
+  const __nv_bfloat16* i1;
+  float* acc32;
+  int ld0;          // row stride (elements) of o0 for the stages that need it
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity` of `bar`; false on expiry or, when
+// `abort_s` is given, as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int32_t* err,
+                                             uint64_t limit_ns = kTimeoutNs) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort_s && *abort_s) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        if (abort_s) *abort_s = 1;
+        if (err) atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+      "[%7];" ::"r"(dst),
+      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;   // SWIZZLE_128B
+  return d;
+}
+// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, M = 128
+__device__ __forceinline__ uint32_t instr_desc(int n, bool a_mn, bool b_mn) {
+  uint32_t d = 0;
+  d |= 1u << 4;                       // D format fp32
+  d |= 1u << 7;                       // A format bf16
+  d |= 1u << 10;                      // B format bf16
+  d |= (a_mn ? 1u : 0u) << 15;        // A MN-major
+  d |= (b_mn ? 1u : 0u) << 16;        // B MN-major
+  d |= (uint32_t)(n >> 3) << 17;      // N / 8
+  d |= (uint32_t)(BM >> 4) << 24;     // M / 16
+  return d;
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define MB_TMEM_LD32(taddr, r)                                                                                       \
+  asm volatile(                                                                                                      \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19," \
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                                      \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),     \
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),          \
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),         \
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                      \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// store 32 consecutive fp32 values as bf16 (64 bytes, 16-byte aligned)
+__device__ __forceinline__ void store_row32(__nv_bfloat16* p, const float* v) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    q[i] = u;
+  }
+}
+__device__ __forceinline__ void store_zero32(__nv_bfloat16* p) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* p, float* v) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u = q[i];
+    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x; v[8 * i + 3] = b.y;
+    v[8 * i + 4] = c.x; v[8 * i + 5] = c.y; v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
+  }
+}
+
+// ------------------------------------------------------------------ tile decode
+struct Tile {
+  int e;        // expert
+  int row0;     // row stages: first padded row; weight stages: first output row (m0)
+  int n0;       // first output column (per branch)
+  int nw;       // columns in this tile (per branch)
+  int kblocks;  // k-blocks of 64
+  int pad0;     // pad_off[e]
+  int off;      // expert_token_offsets[e]
+  int n_e;      // tokens routed to e
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt) {
+  Tile t;
+  constexpr int TN = tile_n(MODE);
+  int nt;
+  if constexpr (is_wgrad(MODE)) {
+    const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
+    const int rank = (int)(tile / per_e);
+    const int r = (int)(tile % per_e);
+    const int mt = r % p.m_tiles_w;
+    nt = r / p.m_tiles_w;
+    t.e = p.meta.order[rank];
+    t.row0 = mt * BM;
+    t.pad0 = p.meta.pad_off[t.e];
+    t.kblocks = (p.meta.pad_off[t.e + 1] - t.pad0) / BK;
+  } else {
+    constexpr int GM = 16;
+    const int64_t per_g = (int64_t)GM * p.n_tiles;
+    const int g = (int)(tile / per_g);
+    const int r = (int)(tile % per_g);
+    const int gm = min(GM, num_mt - g * GM);
+    const int mt = g * GM + r % gm;
+    nt = r / gm;
+    t.e = p.meta.tile_expert[mt];
+    t.row0 = mt * BM;
+    t.pad0 = p.meta.pad_off[t.e];
+    t.kblocks = p.kblocks;
+  }
+  t.off = p.D2[t.e];
+  t.n_e = p.D2[t.e + 1] - t.off;
+  t.n0 = nt * TN;
+  t.nw = min(TN, p.N - t.n0);
+  return t;
+}
+
+// token of padded row q of the tile's expert (clamped to the last routed row)
+__device__ __forceinline__ int row_token(const Params& p, const Tile& t, int q) {
+  int i = q - t.pad0;
+  if (i >= t.n_e) i = t.n_e - 1;
+  if (i < 0) i = 0;
+  return p.D1[t.off + i];
+}
+
+__device__ __forceinline__ float gate_of(const Params& p, int tok, int e) {
+  const int64_t b = (int64_t)tok * p.K;
+  for (int k = 0; k < p.K; ++k)
+    if (p.D3[b + k] == e) return p.gates[b + k];
+  return 0.f;
+}
+
+// ------------------------------------------------------------------ kernel
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 17);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(s), 1);
+      mbar_init(bar(4 + s), 1);
+    }
+    mbar_init(bar(8), 1);
+    mbar_init(bar(9), 1);
+    mbar_init(bar(10), 128);
+    mbar_init(bar(11), 128);
+    mbar_init(bar(12), 1);
+    *abort_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
+  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
+  int32_t* err = p.meta.err;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t armed = 0, armed_par = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = decode<MODE>(p, tile, num_mt);
+      const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
+      const uint32_t tx_bytes = A_BYTES + nmma * BK * 2;
+      int tok[4] = {0, 0, 0, 0};
+      if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU || MODE == DH_SWIGLU || MODE == DH_SILU) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tok[j] = row_token(p, t, t.row0 + 4 * lane + j);
+      }
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t full = bar(s);
+        const uint32_t sA = smem_base + s * STAGE_BYTES;
+        const uint32_t sB = sA + A_BYTES;
+        if (lane == 0) mbar_expect_tx(full, tx_bytes);
+        __syncwarp();
+        armed |= 1u << s;
+        armed_par = (armed_par & ~(1u << s)) | (ph << s);
+        const int k0 = kb * BK;
+        // ---------------- A operand
+        if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU || MODE == DH_SWIGLU || MODE == DH_SILU) {
+          tma_gather4(sA + lane * 512, &p.tmA, k0, tok[0], tok[1], tok[2], tok[3], full);
+        } else if constexpr (MODE == DOWN || MODE == DX) {
+          if (lane == 0) tma_load_2d(sA, &p.tmA, k0, t.row0, full);
+        } else if constexpr (MODE == DW12 || MODE == DW1) {
+          const int j = lane >> 4, g = lane & 15;
+          const int qb = t.pad0 + k0 + 4 * g;
+          tma_gather4(sA + j * 8192 + g * 512, &p.tmA, t.row0 + 64 * j, row_token(p, t, qb), row_token(p, t, qb + 1),
+                      row_token(p, t, qb + 2), row_token(p, t, qb + 3), full);
+        } else {  // DW3: Hg^T, MN-major tiles
+          if (lane < 2) tma_load_2d(sA + lane * 8192, &p.tmA, t.row0 + 64 * lane, t.pad0 + k0, full);
+        }
+        // ---------------- B operand
+        if constexpr (MODE == UP_SWIGLU) {
+          if (lane < 4) {
+            const CUtensorMap* m = lane < 2 ? &p.tmB0 : &p.tmB1;
+            tma_load_2d(sB + lane * 8192, m, t.n0 + 64 * (lane & 1), t.e * p.d + k0, full);
+          }
+        } else if constexpr (MODE == UP_SILU) {
+          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.e * p.d + k0, full);
+        } else if constexpr (MODE == DOWN) {
+          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.e * p.h + k0, full);
+        } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
+          if (lane < t.nw / 128) tma_load_2d(sB + lane * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * lane, full);
+        } else if constexpr (MODE == DX) {
+          if (lane < t.nw / 128) {
+            const bool second = kb >= p.ksplit;
+            const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
+            const int kc = second ? k0 - p.ksplit * BK : k0;
+            tma_load_2d(sB + lane * 16384, m, kc, t.e * p.d + t.n0 + 128 * lane, full);
+          }
+        } else if constexpr (MODE == DW12) {
+          if (lane < 4) {
+            const int col = (lane < 2 ? 0 : p.h) + t.n0 + 64 * (lane & 1);
+            tma_load_2d(sB + lane * 8192, &p.tmB0, col, t.pad0 + k0, full);
+          }
+        } else if constexpr (MODE == DW1) {
+          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.pad0 + k0, full);
+        } else {  // DW3: dY rows via D1, MN-major, nw/64 atoms of 16 gather4 each
+          const int g = lane & 15;
+          const int qb = t.pad0 + k0 + 4 * g;
+          const int r0 = row_token(p, t, qb), r1 = row_token(p, t, qb + 1), r2 = row_token(p, t, qb + 2),
+                    r3 = row_token(p, t, qb + 3);
+          for (int j = lane >> 4; j < t.nw / 64; j += 2)
+            tma_gather4(sB + j * 8192 + g * 512, &p.tmB0, t.n0 + 64 * j, r0, r1, r2, r3, full);
+        }
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      // give the copies already issued a bounded chance to land
+      for (int i = 0; i < STAGES; ++i)
+        if (armed & (1u << i)) wait_bounded(bar(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int abuf = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode<MODE>(p, tile, num_mt);
+        const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
+        const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
+        ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + abuf * 256;
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          ok = wait_bounded(bar(s), ph, abort_s, err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sA = smem_base + s * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = a_mn_major(MODE) ? smem_desc(sA + kk * 2048, 8192, 1024) : smem_desc(sA + kk * 32, 16, 1024);
+            const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
+            mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+          }
+          mma_commit(bar(4 + s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(bar(8 + abuf));
+        if (++abuf == 2) { abuf = 0; aph ^= 1u; }
+      }
+      // all MMAs issued by this thread retire before TMEM is released
+      mma_commit(bar(12));
+      wait_bounded(bar(12), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter ...
+    const int r = quarter * 32 + lane;            // accumulator row of this thread
+    int abuf = 0;
+    uint32_t aph = 0;
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode<MODE>(p, tile, num_mt);
+      bool ok = true;
+      if (lane == 0) ok = wait_bounded(bar(8 + abuf), aph, abort_s, err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + abuf * 256;
+      uint32_t ra[32], rb[32];
+      float va[32], vb[32];
+
+      if constexpr (!is_wgrad(MODE)) {
+        const int q = t.row0 + r;
+        const bool valid = (q - t.pad0) < t.n_e;
+        if constexpr (MODE == UP_SWIGLU) {
+          const int64_t ro = (int64_t)q * p.h + t.n0;
+          for (int c = 0; c < t.nw / 32; ++c) {
+            MB_TMEM_LD32(tbase + 32 * c, ra);
+            MB_TMEM_LD32(tbase + 128 + 32 * c, rb);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                va[i] = __uint_as_float(ra[i]);
+                vb[i] = __uint_as_float(rb[i]);
+              }
+              store_row32(p.o0 + ro + 32 * c, va);
+              store_row32(p.o1 + ro + 32 * c, vb);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) va[i] = silu_f(va[i]) * vb[i];
+              store_row32(p.o2 + ro + 32 * c, va);
+            } else {
+              store_zero32(p.o0 + ro + 32 * c);
+              store_zero32(p.o1 + ro + 32 * c);
+              store_zero32(p.o2 + ro + 32 * c);
+            }
+          }
+        } else if constexpr (MODE == UP_SILU) {
+          const int64_t ro = (int64_t)q * p.h + t.n0;
+          for (int c = 0; c < t.nw / 32; ++c) {
+            MB_TMEM_LD32(tbase + 32 * c, ra);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+              store_row32(p.o0 + ro + 32 * c, va);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) va[i] = silu_f(va[i]);
+              store_row32(p.o2 + ro + 32 * c, va);
+            } else {
+              store_zero32(p.o0 + ro + 32 * c);
+              store_zero32(p.o2 + ro + 32 * c);
+            }
+          }
+        } else if constexpr (MODE == DOWN || MODE == DX) {
+          int tok = 0;
+          float g = 1.f;
+          if (valid) {
+            tok = p.D1[t.off + (q - t.pad0)];
+            if constexpr (MODE == DOWN) g = gate_of(p, tok, t.e);
+          }
+          float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
+          for (int c = 0; c < t.nw / 32; ++c) {
+            MB_TMEM_LD32(tbase + 32 * c, ra);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                red_add_v4(dst + 32 * c + i, g * __uint_as_float(ra[i]), g * __uint_as_float(ra[i + 1]),
+                           g * __uint_as_float(ra[i + 2]), g * __uint_as_float(ra[i + 3]));
+            }
+          }
+        } else {  // DH_SWIGLU / DH_SILU
+          constexpr bool SW = MODE == DH_SWIGLU;
+          float g = 0.f;
+          if (valid) g = gate_of(p, p.D1[t.off + (q - t.pad0)], t.e);
+          const int64_t ro = (int64_t)q * p.h + t.n0;              // A, B, Hg rows
+          const int64_t rab = (int64_t)q * p.ld0 + t.n0;           // dAB rows
+          for (int c = 0; c < t.nw / 32; ++c) {
+            MB_TMEM_LD32(tbase + 32 * c, ra);
+            tmem_wait_ld();
+            if (valid) {
+              float A[32], B[32], dA[32], dB[32], Hg[32];
+              load_row32(p.i0 + ro + 32 * c, A);
+              if constexpr (SW) load_row32(p.i1 + ro + 32 * c, B);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float dH = g * __uint_as_float(ra[i]);
+                const float a = A[i];
+                const float sg = 1.f / (1.f + __expf(-a));
+                const float sl = a * sg;
+                const float ds = sg * (1.f + a * (1.f - sg));
+                if constexpr (SW) {
+                  dA[i] = dH * B[i] * ds;
+                  dB[i] = dH * sl;
+                  Hg[i] = g * sl * B[i];
+                } else {
+                  dA[i] = dH * ds;
+                  Hg[i] = g * sl;
+                }
+              }
+              store_row32(p.o0 + rab + 32 * c, dA);
+              if constexpr (SW) store_row32(p.o0 + rab + p.h + 32 * c, dB);
+              store_row32(p.o1 + ro + 32 * c, Hg);
+            } else {
+              store_zero32(p.o0 + rab + 32 * c);
+              if constexpr (SW) store_zero32(p.o0 + rab + p.h + 32 * c);
+              store_zero32(p.o1 + ro + 32 * c);
+            }
+          }
+        }
+      } else {
+        // weight gradients: rows of dW_e, plain bf16 stores
+        const int64_t orow = (int64_t)(t.row0 + r);
+        if constexpr (MODE == DW12) {
+          const int64_t base = (int64_t)t.e * p.d * p.h + orow * p.h + t.n0;
+          for (int c = 0; c < 8; ++c) {
+            __nv_bfloat16* dst = (c < 4 ? p.o0 : p.o1) + base + 32 * (c & 3);
+            if (t.kblocks > 0) {
+              MB_TMEM_LD32(tbase + 32 * c, ra);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+              store_row32(dst, va);
+            } else {
+              store_zero32(dst);
+            }
+          }
+        } else {
+          const int ld = MODE == DW1 ? p.h : p.d;
+          const int64_t rows_e = MODE == DW1 ? p.d : p.h;
+          const int64_t base = (int64_t)t.e * rows_e * ld + orow * ld + t.n0;
+          for (int c = 0; c < t.nw / 32; ++c) {
+            if (t.kblocks > 0) {
+              MB_TMEM_LD32(tbase + 32 * c, ra);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+              store_row32(p.o0 + base + 32 * c, va);
+            } else {
+              store_zero32(p.o0 + base + 32 * c);
+            }
+          }
+        }
+      }
+      (void)rb; (void)vb;
+      tc_fence_before();
+      mbar_arrive(bar(10 + abuf));
+      if (++abuf == 2) { abuf = 0; aph ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major (rows x cols) matrix, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
+  if (tiles_bound <= 0) return MOEBLAZE_OK;
+  auto kern = moe_gemm_kernel<MODE>;
+  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+  const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
+  kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  return MOEBLAZE_OK;
+}
+
+Params base_params(const moeblaze_shape& s, const moeblaze_dispatch& disp, const float* gates) {
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.D1 = disp.expert_token_indices;
+  p.D2 = disp.expert_token_offsets;
+  p.D3 = disp.token_expert_indices;
+  p.gates = gates;
+  p.meta = meta_view(disp.meta, s.E);
+  p.L = s.L;
+  p.d = s.d; p.h = s.h; p.E = s.E; p.K = s.K;
+  return p;
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    float4 v = src[i];
+    dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+moeblaze_status convert(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t st) {
+  if (n == 0) return MOEBLAZE_OK;
+  const int64_t n4 = n / 4;  // n = L*d with d % 128 == 0
+  const int blocks = sm_count() * 8;
+  f32_to_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src), reinterpret_cast<uint2*>(dst), n4);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  return MOEBLAZE_OK;
+}
+
+}  // namespace tc
+
+using namespace tc;
+
+moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, const float* gates,
+                           const moeblaze_dispatch& disp, const __nv_bfloat16* W1, const __nv_bfloat16* W2,
+                           const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved, __nv_bfloat16* wsH,
+                           float* wsY32, cudaStream_t st) {
+  const bool sw = s.act == MOEBLAZE_SWIGLU;
+  const int64_t LK = s.L * s.K;
+  const int64_t rows = max_padded_rows(LK, s.E);
+  const int64_t mt_bound = rows / BM;
+  MB_CUDA(cudaMemsetAsync(wsY32, 0, sizeof(float) * s.L * s.d, st));
+  stage_event(0, st);
+  if (s.L > 0) {
+    __nv_bfloat16* A = saved;
+    __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;
+    {  // up projection
+      Params p = base_params(s, disp, gates);
+      if (!make_map(&p.tmA, x, s.d, s.L, 64, 1)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmB0, W1, s.h, (uint64_t)s.E * s.d, 64, 64)) return MOEBLAZE_ERR_CUDA;
+      if (sw && !make_map(&p.tmB1, W2, s.h, (uint64_t)s.E * s.d, 64, 64)) return MOEBLAZE_ERR_CUDA;
+      p.N = s.h;
+      p.kblocks = s.d / BK;
+      p.ksplit = p.kblocks;
+      p.n_tiles = (s.h + tile_n(sw ? UP_SWIGLU : UP_SILU) - 1) / tile_n(sw ? UP_SWIGLU : UP_SILU);
+      p.o0 = A; p.o1 = B; p.o2 = wsH;
+      moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
+      if (r != MOEBLAZE_OK) return r;
+    }
+    stage_event(1, st);
+    {  // down projection + gate-weighted combine into y32
+      Params p = base_params(s, disp, gates);
+      if (!make_map(&p.tmA, wsH, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 64)) return MOEBLAZE_ERR_CUDA;
+      p.N = s.d;
+      p.kblocks = s.h / BK;
+      p.ksplit = p.kblocks;
+      p.n_tiles = (s.d + 255) / 256;
+      p.acc32 = wsY32;
+      moeblaze_status r = launch<DOWN>(p, mt_bound * p.n_tiles, st);
+      if (r != MOEBLAZE_OK) return r;
+    }
+  }
+  stage_event(2, st);
+  moeblaze_status r = convert(wsY32, y, s.L * s.d, st);
+  stage_event(3, st);
+  return r;
+}
+
+moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, const __nv_bfloat16* x,
+                            const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
+                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
+                            __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
+                            __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st) {
+  const bool sw = s.act == MOEBLAZE_SWIGLU;
+  const int nb = sw ? 2 : 1;
+  const int64_t LK = s.L * s.K;
+  const int64_t rows = max_padded_rows(LK, s.E);
+  const int64_t mt_bound = rows / BM;
+  const __nv_bfloat16* A = saved;
+  const __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;
+  MB_CUDA(cudaMemsetAsync(wsdX32, 0, sizeof(float) * s.L * s.d, st));
+  stage_event(0, st);
+  if (s.L > 0) {
+    {  // dH = dY W3^T with the SwiGLU backward epilogue
+      Params p = base_params(s, disp, gates);
+      if (!make_map(&p.tmA, dY, s.d, s.L, 64, 1)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      p.N = s.h;
+      p.kblocks = s.d / BK;
+      p.ksplit = p.kblocks;
+      p.n_tiles = (s.h + 255) / 256;
+      p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
+      p.ld0 = nb * s.h;
+      moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
+      if (r != MOEBLAZE_OK) return r;
+    }
+    stage_event(1, st);
+    {  // dX = dA W1^T + dB W2^T, reduced into dX32
+      Params p = base_params(s, disp, gates);
+      if (!make_map(&p.tmA, wsdAB, (uint64_t)nb * s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmB0, W1, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      if (sw && !make_map(&p.tmB1, W2, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      p.N = s.d;
+      p.kblocks = nb * s.h / BK;
+      p.ksplit = s.h / BK;
+      p.n_tiles = (s.d + 255) / 256;
+      p.acc32 = wsdX32;
+      moeblaze_status r = launch<DX>(p, mt_bound * p.n_tiles, st);
+      if (r != MOEBLAZE_OK) return r;
+    }
+  }
+  stage_event(2, st);
+  {  // dW1 (and dW2) = X_e^T [dA | dB]
+    Params p = base_params(s, disp, gates);
+    if (!make_map(&p.tmA, x, s.d, s.L > 0 ? s.L : 1, 64, 1)) return MOEBLAZE_ERR_CUDA;
+    if (!make_map(&p.tmB0, wsdAB, (uint64_t)nb * s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    p.N = s.h;
+    p.m_tiles_w = s.d / BM;
+    p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
+    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
+    p.o0 = dW1; p.o1 = dW2;
+    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
+    if (r != MOEBLAZE_OK) return r;
+  }
+  stage_event(3, st);
+  {  // dW3 = Hg^T dY
+    Params p = base_params(s, disp, gates);
+    if (!make_map(&p.tmA, wsHg, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    if (!make_map(&p.tmB0, dY, s.d, s.L > 0 ? s.L : 1, 64, 1)) return MOEBLAZE_ERR_CUDA;
+    p.N = s.d;
+    p.m_tiles_w = s.h / BM;
+    p.n_tiles = (s.d + 255) / 256;
+    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
+    p.o0 = dW3;
+    moeblaze_status r = launch<DW3>(p, p.total_w, st);
+    if (r != MOEBLAZE_OK) return r;
+  }
+  stage_event(4, st);
+  moeblaze_status r = convert(wsdX32, dX, s.L * s.d, st);
+  stage_event(5, st);
+  return r;
+}
+
+}  // namespace moeblaze

@@ -1,0 +1,127 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol the header declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_atomic_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def _lib():
+    try:
+        return B.lib()
+    except RuntimeError as e:  # not built yet in this checkout
+        import __graft_entry__
+        __graft_entry__.build()
+        return B.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(HEADER_DIR, fn)).read()
+            names += re.findall(r"MOEBLAZE_API\s+[\w\s\*]+?\b(moeblaze_\w+)\s*\(", txt)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib()
+    declared = _declared_functions()
+    assert len(declared) >= 13
+    for n in declared:
+        assert hasattr(lib, n), n
+    assert sorted(declared) == sorted(B.EXPORTS)
+    assert lib.moeblaze_version() == 10000
+
+
+def test_status_strings():
+    _lib()
+    for st in range(7):
+        assert B.status_string(st)
+    assert "workspace" in B.status_string(B.ERR_WORKSPACE)
+
+
+FAKE = ctypes.c_void_p(0x100000)      # aligned, never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x100004)
+
+
+def _disp():
+    return B.Dispatch(0x100000, 0x100000, 0x100000, 0x100000, 0x100000)
+
+
+def test_sizes_and_shape_validation():
+    _lib()
+    s = B.make_shape(512, 64, 128, 8, 2, B.F32, "swiglu")
+    assert B.moeblaze_dispatch_meta_bytes(s) > 0
+    rows = (1024 + 8 * 127 + 127) // 128 * 128   # L*K plus 127 padding rows per expert
+    assert B.moeblaze_saved_bytes(s) == 2 * rows * 128 * 4
+    bad = [
+        B.make_shape(512, 64, 128, 2, 3, B.F32, "swiglu"),        # K > E
+        B.make_shape(-1, 64, 128, 8, 2, B.F32, "swiglu"),         # L < 0
+        B.make_shape(512, 64, 128, 8, 2, 7, "swiglu"),            # dtype
+        B.make_shape(512, 64, 128, 8, 2, B.F32, 9),               # act
+    ]
+    for sh in bad:
+        assert B.moeblaze_saved_bytes(sh) == 0
+        st = B.moeblaze_dispatch_build(sh, FAKE, _disp(), FAKE, 1 << 30, 0, None)
+        assert st == B.ERR_INVALID_ARG
+    unsup = [
+        B.make_shape(512, 96, 128, 8, 2, B.BF16, "swiglu"),       # bf16 needs d % 128 == 0
+        B.make_shape(512, 128, 200, 8, 2, B.BF16, "silu"),        # and h % 128 == 0
+        B.make_shape(512, 128, 128, 600, 2, B.BF16, "swiglu"),    # E > 512
+        B.make_shape(512, 128, 128, 16, 9, B.BF16, "swiglu"),     # K > 8
+        B.make_shape(1 << 30, 128, 128, 16, 4, B.BF16, "swiglu"), # L*K >= 2^31
+    ]
+    for sh in unsup:
+        st = B.moeblaze_forward(sh, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+        assert st == B.ERR_UNSUPPORTED
+
+
+def test_pointer_and_workspace_validation():
+    _lib()
+    s = B.make_shape(4096, 128, 256, 8, 2, B.BF16, "swiglu")
+    need = B.moeblaze_dispatch_workspace_bytes(s)
+    assert B.moeblaze_dispatch_build(s, None, _disp(), FAKE, need, 0, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_dispatch_build(s, MISALIGNED, _disp(), FAKE, need, 0, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_dispatch_build(s, FAKE, _disp(), FAKE, need - 1, 0, None) == B.ERR_WORKSPACE
+    d = _disp()
+    d.meta = None
+    assert B.moeblaze_dispatch_build(s, FAKE, d, FAKE, need, 0, None) == B.ERR_INVALID_ARG
+    fw = B.moeblaze_forward_workspace_bytes(s)
+    # missing W2 for SwiGLU
+    assert B.moeblaze_forward(s, FAKE, FAKE, _disp(), FAKE, None, FAKE, FAKE, FAKE, FAKE, fw, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_forward(s, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, fw - 1, None) == B.ERR_WORKSPACE
+    bw = B.moeblaze_backward_workspace_bytes(s)
+    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                               bw, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               bw - 1, None) == B.ERR_WORKSPACE
+    # SiLU takes no W2 / dW2
+    s2 = B.make_shape(4096, 128, 256, 8, 2, B.BF16, "silu")
+    assert B.moeblaze_saved_bytes(s2) * 2 == B.moeblaze_saved_bytes(s)
+    # identity needs no weights and no scratch
+    s3 = B.make_shape(4096, 128, 0, 8, 2, B.BF16, "identity")
+    assert B.moeblaze_saved_bytes(s3) == 0 and B.moeblaze_forward_workspace_bytes(s3) == 0
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        B.lib()
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "mixture_experts_atomic_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, fn

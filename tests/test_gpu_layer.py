@@ -1,0 +1,81 @@
+"""Forward + backward of the layer on the GPU (through the C ABI) vs the CPU
+oracle: whole-tensor parity at sizes the oracle finishes in seconds (several
+tiles, ragged tails, skew, empty experts, K = 1, K = E), and sampled parity
+at the full workload sizes in the launch configuration the bench times.
+Tolerance: max|gpu - ref| / max|ref| <= 1e-4 (fp32) and 2e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_atomic_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import ensure_built, full_compare, sampled_compare  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _routed_inputs(cfg, seed, one_expert=None):
+    inp = I.make_inputs(cfg, "cpu")
+    ids, gates = I.random_routing(cfg.L, cfg.E, cfg.K, seed, one_expert=one_expert)
+    inp["ids"], inp["gates"] = ids, gates
+    return inp
+
+
+def test_fp32_layer_full_size():
+    cfg = I.CONFIGS[0]
+    errs, _ = full_compare(cfg, I.make_inputs(cfg, "cpu"))
+    assert errs["y"] <= 1e-4
+
+
+@pytest.mark.parametrize("L,d,h,E,K,act,one", [
+    (1000, 256, 384, 5, 2, "swiglu", None),   # h % 256 == 128: half-width tail tiles
+    (1000, 256, 384, 5, 2, "silu", None),
+    (2500, 128, 256, 16, 6, "swiglu", 3),     # skewed: expert 3 takes every token
+    (700, 384, 128, 3, 3, "swiglu", None),    # K == E
+    (130, 128, 128, 8, 2, "silu", None),      # tiny, experts with few or no tokens
+    (4096, 512, 512, 4, 1, "swiglu", None),   # K = 1
+    (3000, 256, 640, 12, 2, "silu", 0),
+])
+def test_bf16_layer_small(L, d, h, E, K, act, one):
+    cfg = I.MoEConfig(f"t_{act}_{L}_{d}_{h}_{E}_{K}", L, d, h, E, K, act, "bf16", 11, "softmax")
+    full_compare(cfg, _routed_inputs(cfg, 5, one))
+
+
+def test_fp32_layer_other_shapes():
+    cfg = I.MoEConfig("t_f32_silu", 333, 32, 48, 5, 3, "silu", "f32", 12, "softmax")
+    full_compare(cfg, _routed_inputs(cfg, 6))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_identity_layer_small(dtype):
+    cfg = I.MoEConfig("t_identity", 1500, 1024 if dtype == "bf16" else 512, 0, 16, 4, "identity", dtype, 13, "zipf")
+    inp = I.make_inputs(cfg, "cpu")
+    full_compare(cfg, inp)
+
+
+def test_empty_layer_zero_grads():
+    from mixture_experts_atomic_gb300.layer import MoELayer
+    layer = MoELayer(0, 128, 128, 4, 2, torch.bfloat16, "swiglu", "cuda")
+    z = lambda *s: torch.randn(*s, device="cuda").to(torch.bfloat16)
+    W1, W2, W3 = z(4, 128, 128), z(4, 128, 128), z(4, 128, 128)
+    layer.dW1.fill_(1); layer.dW2.fill_(1); layer.dW3.fill_(1)
+    ids = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    g = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    layer.step({"ids": ids, "gates": g, "x": x, "dY": x, "W1": W1, "W2": W2, "W3": W3})
+    torch.cuda.synchronize()
+    assert float(layer.dW1.float().abs().sum()) == 0 and float(layer.dW3.float().abs().sum()) == 0
+
+
+@pytest.mark.parametrize("ci", [1, 2, 3])
+def test_workload_sampled(ci):
+    sampled_compare(I.CONFIGS[ci])
+
+
+def test_identity_workload_sampled():
+    sampled_compare(I.CONFIGS[4], n_tok=64)
