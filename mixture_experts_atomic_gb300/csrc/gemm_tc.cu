@@ -4,15 +4,16 @@
 // "免物化 token dispatch" and "SwiGLU kernel 融合 + activation checkpoint").
 //
 // One persistent, warp-specialised kernel template serves all six GEMMs:
-//   warp 0      producer: TMA loads of the A and B tiles into a 4-stage ring;
-//               routed rows of x / dY are fetched with tile::gather4 (four
-//               arbitrary rows per instruction) straight from the (L,d)
-//               tensor through expert_token_indices - no routed buffer.
-//   warp 1      TMEM allocator and MMA issuer: one thread issues
+//   warps 0-3   producer: tiled TMA loads (thread 0) of the weight and
+//               activation tiles into a 4-stage ring; the routed rows of x /
+//               dY are gathered straight from the (L,d) tensor through
+//               expert_token_indices by all 128 producer threads with 16-byte
+//               cp.async into the 128B-swizzled layout - no routed buffer.
+//   warp 4      TMEM allocator and MMA issuer: one thread issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N<=256, K=16),
 //               fp32 accumulators in TMEM, two accumulator buffers so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator rows and the fused
+//   warps 5-8   epilogue: tcgen05.ld of the accumulator rows and the fused
 //               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward,
 //               plain stores).
 //
@@ -23,7 +24,7 @@
 // gather a valid token and are zero where they feed a reduction.
 //
 // Stage                          A (M x K)                B (K x N)             epilogue
-//  UP_SWIGLU  a,b = X W1,X W2    x rows via D1 (gather4)  [W1_e | W2_e] tiles   A,B (saved), H=SiLU(a)b
+//  UP_SWIGLU  a,b = X W1,X W2    x rows via D1 (gather)   [W1_e | W2_e] tiles   A,B (saved), H=SiLU(a)b
 //  UP_SILU    a = X W1           x rows via D1            W1_e                  A (saved), H=SiLU(a)
 //  DOWN       Y = H W3           H rows                   W3_e                  y32[t] += g Y   (red.add)
 //  DH_*       dH = dY W3^T       dY rows via D1           W3_e (K-major)        dA, dB, Hg (SwiGLU bwd)
@@ -45,7 +46,11 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int PRODUCER_WARPS = 4;
+constexpr int PRODUCER_THREADS = PRODUCER_WARPS * 32;
+constexpr int MMA_WARP = PRODUCER_WARPS;
+constexpr int NUM_THREADS = (PRODUCER_WARPS + 1 + 4) * 32;  // producers, MMA, 4 epilogue warps
+constexpr int LAG = STAGES - 2;               // cp.async groups a producer thread keeps in flight
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
@@ -84,6 +89,8 @@ struct Params {
   const __nv_bfloat16* i1;
   float* acc32;
   int ld0;          // row stride (elements) of o0 for the stages that need it
+  const __nv_bfloat16* gsrc;  // gathered tensor (x or dY), rows of gld elements
+  int gld;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -99,6 +106,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// order this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core / TMA) accesses
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -132,14 +153,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
-      "[%7];" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -286,8 +299,16 @@ __device__ __forceinline__ float gate_of(const Params& p, int tok, int e) {
 }
 
 // ------------------------------------------------------------------ kernel
+// Operands fetched by the cp.async gather producer (rows picked through
+// expert_token_indices); every other operand tile comes by tiled TMA.
+__host__ __device__ constexpr bool cp_a(int m) {
+  return m == UP_SWIGLU || m == UP_SILU || m == DH_SWIGLU || m == DH_SILU || m == DW12 || m == DW1;
+}
+__host__ __device__ constexpr bool cp_b(int m) { return m == DW3; }
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
+  constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -301,7 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(s), 1);
+      mbar_init(bar(s), CP ? PRODUCER_THREADS : 1);
       mbar_init(bar(4 + s), 1);
     }
     mbar_init(bar(8), 1);
@@ -312,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
                  : "memory");
@@ -327,89 +348,145 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
   int32_t* err = p.meta.err;
 
-  if (warp == 0) {
+  if (warp < PRODUCER_WARPS) {
     // ================================================================ producer
-    int s = 0;
-    uint32_t ph = 0;
-    uint32_t armed = 0, armed_par = 0;
-    bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const Tile t = decode<MODE>(p, tile, num_mt);
-      const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
-      const uint32_t tx_bytes = A_BYTES + nmma * BK * 2;
-      int tok[4] = {0, 0, 0, 0};
-      if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU || MODE == DH_SWIGLU || MODE == DH_SILU) {
+    // Thread 0 issues the tiled TMA loads.  In the gather stages all 128
+    // producer threads also copy the gathered operand with 16-byte cp.async
+    // straight into the 128B-swizzled layout (8 consecutive threads cover one
+    // 128-byte row segment), keep LAG groups in flight, and arrive on the
+    // stage's full barrier once their copies of it have landed and been
+    // fenced for the tensor cores (async proxy).
+    const int pt = threadIdx.x;
+    if (CP || pt == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t armed = 0, armed_par = 0;
+      int inflight = 0;
+      bool ok = true;
+      const int c8 = pt & 7;   // 16-byte chunk of a 128-byte row this thread copies
+      const int r16 = pt >> 3; // row offset 0..15 within a group of 16 rows
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode<MODE>(p, tile, num_mt);
+        const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
+        int rtok[8];
+        int wtok[4];
+        if constexpr (CP && !is_wgrad(MODE)) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tok[j] = row_token(p, t, t.row0 + 4 * lane + j);
+          for (int it = 0; it < 8; ++it) rtok[it] = row_token(p, t, t.row0 + it * 16 + r16);
+        }
+        if constexpr (CP && is_wgrad(MODE)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) wtok[i] = row_token(p, t, t.pad0 + i * 16 + r16);
+        }
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const uint32_t full = bar(s);
+          const uint32_t sA = smem_base + s * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+          const int k0 = kb * BK;
+          int wnext[4];
+          if constexpr (CP && is_wgrad(MODE)) {
+            if (kb + 1 < t.kblocks) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) wnext[i] = row_token(p, t, t.pad0 + k0 + BK + i * 16 + r16);
+            }
+          }
+          if (pt == 0) {
+            // ---------------- tiled TMA part of the stage
+            const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
+            if (CP) mbar_expect_tx_only(full, tma_bytes);
+            else mbar_expect_tx(full, tma_bytes);
+            armed |= 1u << s;
+            armed_par = (armed_par & ~(1u << s)) | (ph << s);
+            if constexpr (MODE == DOWN || MODE == DX) {
+              tma_load_2d(sA, &p.tmA, k0, t.row0, full);
+            } else if constexpr (MODE == DW3) {
+              tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
+              tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
+            }
+            if constexpr (MODE == UP_SWIGLU) {
+              tma_load_2d(sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
+              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0, full);
+              tma_load_2d(sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0, full);
+              tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
+            } else if constexpr (MODE == UP_SILU) {
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
+            } else if constexpr (MODE == DOWN) {
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, full);
+            } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
+              for (int j = 0; j < t.nw / 128; ++j)
+                tma_load_2d(sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
+            } else if constexpr (MODE == DX) {
+              const bool second = kb >= p.ksplit;
+              const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
+              const int kc = second ? k0 - p.ksplit * BK : k0;
+              for (int j = 0; j < t.nw / 128; ++j) tma_load_2d(sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j, full);
+            } else if constexpr (MODE == DW12) {
+              tma_load_2d(sB, &p.tmB0, t.n0, t.pad0 + k0, full);
+              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0, full);
+              tma_load_2d(sB + 16384, &p.tmB0, p.h + t.n0, t.pad0 + k0, full);
+              tma_load_2d(sB + 24576, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0, full);
+            } else if constexpr (MODE == DW1) {
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.pad0 + k0, full);
+            }
+          }
+          if constexpr (CP) {
+            // ---------------- gathered part of the stage
+            if constexpr (!is_wgrad(MODE)) {
+              // K-major A: 128 routed rows x 64 columns of x (or dY)
+#pragma unroll
+              for (int it = 0; it < 8; ++it) {
+                const int r = it * 16 + r16;
+                const __nv_bfloat16* src = p.gsrc + (int64_t)rtok[it] * p.gld + k0 + c8 * 8;
+                cp_async16(sA + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+              }
+            } else {
+              // MN-major operand gathered along K: 64 routed rows x (atoms of 64 columns)
+              const int col0 = CPA ? t.row0 : t.n0;
+              const uint32_t dst0 = CPA ? sA : sB;
+              const int natoms = CPA ? 2 : t.nw / 64;
+              for (int j = 0; j < natoms; ++j) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int r = i * 16 + r16;
+                  const __nv_bfloat16* src = p.gsrc + (int64_t)wtok[i] * p.gld + col0 + 64 * j + c8 * 8;
+                  cp_async16(dst0 + j * 8192 + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+                }
+              }
+            }
+            cp_async_commit();
+            if (inflight == LAG) {
+              cp_async_wait<LAG>();
+              fence_proxy_async();
+              mbar_arrive(bar((s + STAGES - LAG) % STAGES));
+            } else {
+              ++inflight;
+            }
+          }
+          if constexpr (CP && is_wgrad(MODE)) {
+            if (kb + 1 < t.kblocks) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) wtok[i] = wnext[i];
+            }
+          }
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
       }
-      for (int kb = 0; kb < t.kblocks; ++kb) {
-        if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const uint32_t full = bar(s);
-        const uint32_t sA = smem_base + s * STAGE_BYTES;
-        const uint32_t sB = sA + A_BYTES;
-        if (lane == 0) mbar_expect_tx(full, tx_bytes);
-        __syncwarp();
-        armed |= 1u << s;
-        armed_par = (armed_par & ~(1u << s)) | (ph << s);
-        const int k0 = kb * BK;
-        // ---------------- A operand
-        if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU || MODE == DH_SWIGLU || MODE == DH_SILU) {
-          tma_gather4(sA + lane * 512, &p.tmA, k0, tok[0], tok[1], tok[2], tok[3], full);
-        } else if constexpr (MODE == DOWN || MODE == DX) {
-          if (lane == 0) tma_load_2d(sA, &p.tmA, k0, t.row0, full);
-        } else if constexpr (MODE == DW12 || MODE == DW1) {
-          const int j = lane >> 4, g = lane & 15;
-          const int qb = t.pad0 + k0 + 4 * g;
-          tma_gather4(sA + j * 8192 + g * 512, &p.tmA, t.row0 + 64 * j, row_token(p, t, qb), row_token(p, t, qb + 1),
-                      row_token(p, t, qb + 2), row_token(p, t, qb + 3), full);
-        } else {  // DW3: Hg^T, MN-major tiles
-          if (lane < 2) tma_load_2d(sA + lane * 8192, &p.tmA, t.row0 + 64 * lane, t.pad0 + k0, full);
-        }
-        // ---------------- B operand
-        if constexpr (MODE == UP_SWIGLU) {
-          if (lane < 4) {
-            const CUtensorMap* m = lane < 2 ? &p.tmB0 : &p.tmB1;
-            tma_load_2d(sB + lane * 8192, m, t.n0 + 64 * (lane & 1), t.e * p.d + k0, full);
-          }
-        } else if constexpr (MODE == UP_SILU) {
-          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.e * p.d + k0, full);
-        } else if constexpr (MODE == DOWN) {
-          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.e * p.h + k0, full);
-        } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
-          if (lane < t.nw / 128) tma_load_2d(sB + lane * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * lane, full);
-        } else if constexpr (MODE == DX) {
-          if (lane < t.nw / 128) {
-            const bool second = kb >= p.ksplit;
-            const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
-            const int kc = second ? k0 - p.ksplit * BK : k0;
-            tma_load_2d(sB + lane * 16384, m, kc, t.e * p.d + t.n0 + 128 * lane, full);
-          }
-        } else if constexpr (MODE == DW12) {
-          if (lane < 4) {
-            const int col = (lane < 2 ? 0 : p.h) + t.n0 + 64 * (lane & 1);
-            tma_load_2d(sB + lane * 8192, &p.tmB0, col, t.pad0 + k0, full);
-          }
-        } else if constexpr (MODE == DW1) {
-          if (lane < t.nw / 64) tma_load_2d(sB + lane * 8192, &p.tmB0, t.n0 + 64 * lane, t.pad0 + k0, full);
-        } else {  // DW3: dY rows via D1, MN-major, nw/64 atoms of 16 gather4 each
-          const int g = lane & 15;
-          const int qb = t.pad0 + k0 + 4 * g;
-          const int r0 = row_token(p, t, qb), r1 = row_token(p, t, qb + 1), r2 = row_token(p, t, qb + 2),
-                    r3 = row_token(p, t, qb + 3);
-          for (int j = lane >> 4; j < t.nw / 64; j += 2)
-            tma_gather4(sB + j * 8192 + g * 512, &p.tmB0, t.n0 + 64 * j, r0, r1, r2, r3, full);
-        }
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      if constexpr (CP) {
+        // the last `inflight` stages: wait for their copies and arrive
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + STAGES - i) % STAGES));
+      }
+      if (!ok && pt == 0) {
+        // give the TMA copies already issued a bounded chance to land
+        for (int i = 0; i < STAGES; ++i)
+          if (armed & (1u << i)) wait_bounded(bar(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
       }
     }
-    if (!ok && lane == 0) {
-      // give the copies already issued a bounded chance to land
-      for (int i = 0; i < STAGES; ++i)
-        if (armed & (1u << i)) wait_bounded(bar(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
-    }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       int s = 0;
@@ -610,7 +687,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
   }
 }
@@ -706,7 +783,8 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
     __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;
     {  // up projection
       Params p = base_params(s, disp, gates);
-      if (!make_map(&p.tmA, x, s.d, s.L, 64, 1)) return MOEBLAZE_ERR_CUDA;
+      p.gsrc = x;
+      p.gld = s.d;
       if (!make_map(&p.tmB0, W1, s.h, (uint64_t)s.E * s.d, 64, 64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmB1, W2, s.h, (uint64_t)s.E * s.d, 64, 64)) return MOEBLAZE_ERR_CUDA;
       p.N = s.h;
@@ -754,7 +832,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
   if (s.L > 0) {
     {  // dH = dY W3^T with the SwiGLU backward epilogue
       Params p = base_params(s, disp, gates);
-      if (!make_map(&p.tmA, dY, s.d, s.L, 64, 1)) return MOEBLAZE_ERR_CUDA;
+      p.gsrc = dY;
+      p.gld = s.d;
       if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 128)) return MOEBLAZE_ERR_CUDA;
       p.N = s.h;
       p.kblocks = s.d / BK;
@@ -783,7 +862,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
   stage_event(2, st);
   {  // dW1 (and dW2) = X_e^T [dA | dB]
     Params p = base_params(s, disp, gates);
-    if (!make_map(&p.tmA, x, s.d, s.L > 0 ? s.L : 1, 64, 1)) return MOEBLAZE_ERR_CUDA;
+    p.gsrc = x;
+    p.gld = s.d;
     if (!make_map(&p.tmB0, wsdAB, (uint64_t)nb * s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
     p.N = s.h;
     p.m_tiles_w = s.d / BM;
@@ -797,7 +877,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
   {  // dW3 = Hg^T dY
     Params p = base_params(s, disp, gates);
     if (!make_map(&p.tmA, wsHg, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
-    if (!make_map(&p.tmB0, dY, s.d, s.L > 0 ? s.L : 1, 64, 1)) return MOEBLAZE_ERR_CUDA;
+    p.gsrc = dY;
+    p.gld = s.d;
     p.N = s.d;
     p.m_tiles_w = s.h / BM;
     p.n_tiles = (s.d + 255) / 256;
