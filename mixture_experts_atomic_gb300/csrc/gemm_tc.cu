@@ -379,8 +379,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           for (int i = 0; i < 4; ++i) wtok[i] = row_token(p, t, t.pad0 + i * 16 + r16);
         }
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if constexpr (CP) {
+            // every lane of the four producer warps is here: lane 0 waits, the warp follows
+            if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          } else {
+            // thread 0 runs this loop alone: no warp-collective operations here
+            ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+          }
           if (!ok) break;
           const uint32_t full = bar(s);
           const uint32_t sA = smem_base + s * STAGE_BYTES;
