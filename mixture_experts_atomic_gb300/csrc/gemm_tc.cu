@@ -225,6 +225,15 @@ __device__ __forceinline__ void store_zero32(__nv_bfloat16* p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) q[i] = make_uint4(0u, 0u, 0u, 0u);
 }
+__device__ __forceinline__ void unpack_row32(const uint4* q, float* v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = q[i];
+    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x; v[8 * i + 3] = b.y;
+    v[8 * i + 4] = c.x; v[8 * i + 5] = c.y; v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
+  }
+}
 __device__ __forceinline__ void load_row32(const __nv_bfloat16* p, float* v) {
   const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll
@@ -365,19 +374,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       bool ok = true;
       const int c8 = pt & 7;   // 16-byte chunk of a 128-byte row this thread copies
       const int r16 = pt >> 3; // row offset 0..15 within a group of 16 rows
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode<MODE>(p, tile, num_mt);
-        const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
-        int rtok[8];
-        int wtok[4];
+      // The routed-row tokens of the next tile are loaded while this tile's
+      // k-blocks are issued, so a tile change costs no load latency.
+      int rtok[8], wtok[4], rnext[8], wfirst[4];
+      auto load_tile_tokens = [&](const Tile& tt, int* rr, int* ww) {
         if constexpr (CP && !is_wgrad(MODE)) {
 #pragma unroll
-          for (int it = 0; it < 8; ++it) rtok[it] = row_token(p, t, t.row0 + it * 16 + r16);
+          for (int it = 0; it < 8; ++it) rr[it] = row_token(p, tt, tt.row0 + it * 16 + r16);
         }
         if constexpr (CP && is_wgrad(MODE)) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) wtok[i] = row_token(p, t, t.pad0 + i * 16 + r16);
+          for (int i = 0; i < 4; ++i) ww[i] = row_token(p, tt, tt.pad0 + i * 16 + r16);
         }
+      };
+      Tile t;
+      if (blockIdx.x < total) {
+        t = decode<MODE>(p, blockIdx.x, num_mt);
+        load_tile_tokens(t, rtok, wtok);
+      }
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int64_t ntile = tile + gridDim.x;
+        Tile tn;
+        if (ntile < total) {
+          tn = decode<MODE>(p, ntile, num_mt);
+          load_tile_tokens(tn, rnext, wfirst);
+        }
+        const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if constexpr (CP) {
             // every lane of the four producer warps is here: lane 0 waits, the warp follows
@@ -479,6 +501,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
+        if (ntile < total) {
+          t = tn;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rtok[i] = rnext[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) wtok[i] = wfirst[i];
+        }
       }
       if constexpr (CP) {
         // the last `inflight` stages: wait for their copies and arrive
@@ -540,6 +569,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     uint32_t aph = 0;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode<MODE>(p, tile, num_mt);
+      // Per-row context that does not depend on the accumulator is fetched
+      // before waiting for it, so its latency overlaps the main loop.
+      constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
+      int q = 0, tok = 0;
+      bool valid = false;
+      float g = 1.f;
+      uint4 nA[4], nB[4];
+      if constexpr (!is_wgrad(MODE)) {
+        q = t.row0 + r;
+        valid = (q - t.pad0) < t.n_e;
+        if constexpr (MODE == DOWN || MODE == DX || DH) {
+          if (valid) {
+            tok = p.D1[t.off + (q - t.pad0)];
+            if constexpr (MODE != DX) g = gate_of(p, tok, t.e);
+          }
+        }
+        if constexpr (DH) {
+          if (valid) {
+            const uint4* pa = reinterpret_cast<const uint4*>(p.i0 + (int64_t)q * p.h + t.n0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) nA[i] = pa[i];
+            if constexpr (MODE == DH_SWIGLU) {
+              const uint4* pb = reinterpret_cast<const uint4*>(p.i1 + (int64_t)q * p.h + t.n0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) nB[i] = pb[i];
+            }
+          }
+        }
+      }
       bool ok = true;
       if (lane == 0) ok = wait_bounded(bar(8 + abuf), aph, abort_s, err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -550,8 +608,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       float va[32], vb[32];
 
       if constexpr (!is_wgrad(MODE)) {
-        const int q = t.row0 + r;
-        const bool valid = (q - t.pad0) < t.n_e;
         if constexpr (MODE == UP_SWIGLU) {
           const int64_t ro = (int64_t)q * p.h + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
@@ -593,12 +649,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             }
           }
         } else if constexpr (MODE == DOWN || MODE == DX) {
-          int tok = 0;
-          float g = 1.f;
-          if (valid) {
-            tok = p.D1[t.off + (q - t.pad0)];
-            if constexpr (MODE == DOWN) g = gate_of(p, tok, t.e);
-          }
           float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
@@ -612,17 +662,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
         } else {  // DH_SWIGLU / DH_SILU
           constexpr bool SW = MODE == DH_SWIGLU;
-          float g = 0.f;
-          if (valid) g = gate_of(p, p.D1[t.off + (q - t.pad0)], t.e);
           const int64_t ro = (int64_t)q * p.h + t.n0;              // A, B, Hg rows
           const int64_t rab = (int64_t)q * p.ld0 + t.n0;           // dAB rows
-          for (int c = 0; c < t.nw / 32; ++c) {
+          const int nch = t.nw / 32;
+          for (int c = 0; c < nch; ++c) {
+            // chunk c of A (B) was loaded one step ahead; start loading chunk c+1
+            uint4 cA[4], cB[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              cA[i] = nA[i];
+              if constexpr (SW) cB[i] = nB[i];
+            }
+            if (valid && c + 1 < nch) {
+              const uint4* pa = reinterpret_cast<const uint4*>(p.i0 + ro + 32 * (c + 1));
+#pragma unroll
+              for (int i = 0; i < 4; ++i) nA[i] = pa[i];
+              if constexpr (SW) {
+                const uint4* pb = reinterpret_cast<const uint4*>(p.i1 + ro + 32 * (c + 1));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) nB[i] = pb[i];
+              }
+            }
             MB_TMEM_LD32(tbase + 32 * c, ra);
             tmem_wait_ld();
             if (valid) {
               float A[32], B[32], dA[32], dB[32], Hg[32];
-              load_row32(p.i0 + ro + 32 * c, A);
-              if constexpr (SW) load_row32(p.i1 + ro + 32 * c, B);
+              unpack_row32(cA, A);
+              if constexpr (SW) unpack_row32(cB, B);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const float dH = g * __uint_as_float(ra[i]);
