@@ -110,7 +110,6 @@ void count_launch(int n = 1);
 void stage_event(int i, cudaStream_t st);
 
 // ---------------------------------------------------------------- device helpers
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 
 // bf16x2 packing of two fp32 values, round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -52,7 +52,12 @@ constexpr int MMA_WARP = PRODUCER_WARPS;
 constexpr int NUM_THREADS = (PRODUCER_WARPS + 1 + 4) * 32;  // producers, MMA, 4 epilogue warps
 constexpr int LAG = STAGES - 2;               // cp.async groups a producer thread keeps in flight
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+// epilogue staging for TMA stores: per epilogue warp a ring of EPI_RING
+// buffers of 32 rows x 32 bf16 (64-byte swizzle)
+constexpr int EPI_RING = 4;
+constexpr int EPI_BUF_BYTES = 32 * 64;
+constexpr int EPI_STAGE_BYTES = 4 * EPI_RING * EPI_BUF_BYTES;  // 32 KB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 256;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -69,6 +74,9 @@ struct Params {
   CUtensorMap tmA;
   CUtensorMap tmB0;
   CUtensorMap tmB1;
+  CUtensorMap tmO0;  // bf16 outputs written by TMA stores (up: A, B, H; dH: dA|dB, Hg)
+  CUtensorMap tmO1;
+  CUtensorMap tmO2;
   const int32_t* D1;
   const int32_t* D2;
   const int32_t* D3;
@@ -203,6 +211,59 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src), "r"(c0),
+               "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Writes this warp's 32 rows x 32 columns (lane = row, v = its 32 values;
+// zeros where !valid) to element (col, row0) of `map` through the warp's
+// staging ring: the lanes fill a 64-byte-swizzled 2 KB buffer, fence it for
+// the async proxy, and lane 0 issues one TMA store (one bulk group each).
+struct StoreRing {
+  uint32_t base;
+  int slot;
+};
+__device__ __forceinline__ void staged_store(StoreRing& ring, const CUtensorMap* map, int col, int row0, const float* v,
+                                             bool valid, int lane) {
+  const uint32_t buf = ring.base + ring.slot * EPI_BUF_BYTES;
+  if (lane == 0) bulk_wait_read<EPI_RING - 1>();  // this buffer's previous store has been read
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+      u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+      u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+      u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    }
+    st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), u);
+  }
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, col, row0);
+    bulk_commit();
+  }
+  ring.slot = (ring.slot + 1) % EPI_RING;
+}
+
+__device__ __forceinline__ float fast_sigmoid(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
@@ -320,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
   // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 17);
@@ -565,6 +626,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     // ================================================================ epilogue
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter ...
     const int r = quarter * 32 + lane;            // accumulator row of this thread
+    StoreRing ring{smem_base + STAGES * STAGE_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -604,49 +666,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + abuf * 256;
+      const int wrow0 = t.row0 + quarter * 32;    // first row of this warp in the output
       uint32_t ra[32], rb[32];
       float va[32], vb[32];
 
       if constexpr (!is_wgrad(MODE)) {
         if constexpr (MODE == UP_SWIGLU) {
-          const int64_t ro = (int64_t)q * p.h + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
             MB_TMEM_LD32(tbase + 128 + 32 * c, rb);
             tmem_wait_ld();
-            if (valid) {
+            float vh[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                va[i] = __uint_as_float(ra[i]);
-                vb[i] = __uint_as_float(rb[i]);
-              }
-              store_row32(p.o0 + ro + 32 * c, va);
-              store_row32(p.o1 + ro + 32 * c, vb);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) va[i] = silu_f(va[i]) * vb[i];
-              store_row32(p.o2 + ro + 32 * c, va);
-            } else {
-              store_zero32(p.o0 + ro + 32 * c);
-              store_zero32(p.o1 + ro + 32 * c);
-              store_zero32(p.o2 + ro + 32 * c);
+            for (int i = 0; i < 32; ++i) {
+              va[i] = __uint_as_float(ra[i]);
+              vb[i] = __uint_as_float(rb[i]);
+              vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
             }
+            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
+            staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, vb, valid, lane);
+            staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vh, valid, lane);
           }
         } else if constexpr (MODE == UP_SILU) {
-          const int64_t ro = (int64_t)q * p.h + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
             tmem_wait_ld();
-            if (valid) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
-              store_row32(p.o0 + ro + 32 * c, va);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) va[i] = silu_f(va[i]);
-              store_row32(p.o2 + ro + 32 * c, va);
-            } else {
-              store_zero32(p.o0 + ro + 32 * c);
-              store_zero32(p.o2 + ro + 32 * c);
+            for (int i = 0; i < 32; ++i) {
+              va[i] = __uint_as_float(ra[i]);
+              vb[i] = va[i] * fast_sigmoid(va[i]);
             }
+            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
+            staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vb, valid, lane);
           }
         } else if constexpr (MODE == DOWN || MODE == DX) {
           float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
@@ -662,8 +713,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
         } else {  // DH_SWIGLU / DH_SILU
           constexpr bool SW = MODE == DH_SWIGLU;
-          const int64_t ro = (int64_t)q * p.h + t.n0;              // A, B, Hg rows
-          const int64_t rab = (int64_t)q * p.ld0 + t.n0;           // dAB rows
+          const int64_t ro = (int64_t)q * p.h + t.n0;              // A, B rows
           const int nch = t.nw / 32;
           for (int c = 0; c < nch; ++c) {
             // chunk c of A (B) was loaded one step ahead; start loading chunk c+1
@@ -685,34 +735,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             }
             MB_TMEM_LD32(tbase + 32 * c, ra);
             tmem_wait_ld();
-            if (valid) {
-              float A[32], B[32], dA[32], dB[32], Hg[32];
-              unpack_row32(cA, A);
-              if constexpr (SW) unpack_row32(cB, B);
+            float A[32], B[32], dA[32], dB[32], Hg[32];
+            unpack_row32(cA, A);
+            if constexpr (SW) unpack_row32(cB, B);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float dH = g * __uint_as_float(ra[i]);
-                const float a = A[i];
-                const float sg = 1.f / (1.f + __expf(-a));
-                const float sl = a * sg;
-                const float ds = sg * (1.f + a * (1.f - sg));
-                if constexpr (SW) {
-                  dA[i] = dH * B[i] * ds;
-                  dB[i] = dH * sl;
-                  Hg[i] = g * sl * B[i];
-                } else {
-                  dA[i] = dH * ds;
-                  Hg[i] = g * sl;
-                }
+            for (int i = 0; i < 32; ++i) {
+              const float dH = g * __uint_as_float(ra[i]);
+              const float a = A[i];
+              const float sg = fast_sigmoid(a);
+              const float sl = a * sg;
+              const float ds = sg * (1.f + a * (1.f - sg));
+              if constexpr (SW) {
+                dA[i] = dH * B[i] * ds;
+                dB[i] = dH * sl;
+                Hg[i] = g * sl * B[i];
+              } else {
+                dA[i] = dH * ds;
+                Hg[i] = g * sl;
               }
-              store_row32(p.o0 + rab + 32 * c, dA);
-              if constexpr (SW) store_row32(p.o0 + rab + p.h + 32 * c, dB);
-              store_row32(p.o1 + ro + 32 * c, Hg);
-            } else {
-              store_zero32(p.o0 + rab + 32 * c);
-              if constexpr (SW) store_zero32(p.o0 + rab + p.h + 32 * c);
-              store_zero32(p.o1 + ro + 32 * c);
             }
+            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
+            if constexpr (SW) staged_store(ring, &p.tmO0, p.h + t.n0 + 32 * c, wrow0, dB, valid, lane);
+            staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
           }
         }
       } else {
@@ -754,6 +798,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       mbar_arrive(bar(10 + abuf));
       if (++abuf == 2) { abuf = 0; aph ^= 1u; }
     }
+    // the TMA stores issued by lane 0 complete before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -782,7 +829,8 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 tensor map over a row-major (rows x cols) matrix, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -790,7 +838,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -864,6 +912,10 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.h + tile_n(sw ? UP_SWIGLU : UP_SILU) - 1) / tile_n(sw ? UP_SWIGLU : UP_SILU);
       p.o0 = A; p.o1 = B; p.o2 = wsH;
+      const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
+      if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+      if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
@@ -912,6 +964,9 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = p.kblocks;
       p.n_tiles = (s.h + 255) / 256;
       p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
+      const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
+      if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       p.ld0 = nb * s.h;
       moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
