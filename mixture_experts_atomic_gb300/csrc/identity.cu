@@ -4,14 +4,15 @@
 // awesome-system-papers page, section "免物化 token dispatch", Forward and
 // Backward; the backward is the same kernel on dY -> dX).
 //
-// Schedule: one CTA per (window of 8 tokens, 1024 columns).  The window's
+// Schedule: one CTA per window of 8 tokens, all columns.  The window's
 // 8*K (token, slot) positions are read from token_index_map and ranked
 // ascending, which is expert-major order restricted to the window (the order
 // the grouped expert GEMM walks its rows).  The CTA then walks them in that
 // order, reading each routed row through expert_token_indices (the gather)
-// and adding g * row into a shared-memory fp32 accumulator; every thread owns
-// the same 8 (bf16) or 4 (fp32) columns of all 8 rows, so the accumulation
-// needs no atomics.  Each output row is written once, each input row is read
+// and adding g * row into a shared-memory fp32 accumulator, one chunk of
+// 1024 (bf16) or 512 (fp32) columns at a time with eight 16-byte row loads in
+// flight per thread; every thread owns the same columns of all 8 rows, so the
+// accumulation needs no atomics and the sorted list is built once per window.  Each output row is written once, each input row is read
 // from HBM once (its K reads fall inside one CTA), the routed (L*K, d)
 // buffer never exists.
 #include <climits>
@@ -69,8 +70,6 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
   const int tid = threadIdx.x;
   const int64_t t0 = (int64_t)blockIdx.x * kWin;
   const int n = kWin * K;
-  const int col = blockIdx.y * (kThreads * V) + tid * V;
-  const bool active = col < d;
 
   if (tid < n) {
     const int64_t t = t0 + tid / K;
@@ -83,8 +82,6 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
     pos_in[tid] = p;
     g_in[tid] = g;
   }
-#pragma unroll
-  for (int j = 0; j < kWin * V4; ++j) acc[j * kThreads + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   if (tid < n) {  // rank = place in ascending position order (expert-major)
     const int32_t p = pos_in[tid];
@@ -94,19 +91,27 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
     g_s[r] = g_in[tid];
   }
   __syncthreads();
-  if (tid < n) tok_s[tid] = (pos_s[tid] != INT_MAX) ? D1[pos_s[tid]] : -1;  // the gather index
+  if (tid < n) {  // the gather index; entries outside the window are dropped
+    const int32_t tok = (pos_s[tid] != INT_MAX) ? D1[pos_s[tid]] : -1;
+    tok_s[tid] = (tok >= 0 && tok - t0 >= 0 && tok - t0 < kWin) ? (int32_t)(tok - t0) : -1;
+  }
   __syncthreads();
 
-  if (active) {
-    constexpr int U = 4;
+  // The same sorted list serves every column chunk of the window's rows.
+  for (int cb = 0; cb < d; cb += kThreads * V) {
+    const int col = cb + tid * V;
+    if (col >= d) break;
+#pragma unroll
+    for (int j = 0; j < kWin * V4; ++j) acc[j * kThreads + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int U = 8;
     for (int i0 = 0; i0 < n; i0 += U) {
       float v[U][V];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u;
-        const int32_t tok = (i < n) ? tok_s[i] : -1;
-        if (tok >= 0 && tok - t0 >= 0 && tok - t0 < kWin) {
-          Vec<T>::load(src + (int64_t)tok * d + col, v[u]);
+        const int j = (i < n) ? tok_s[i] : -1;
+        if (j >= 0) {
+          Vec<T>::load(src + (t0 + j) * d + col, v[u]);
         } else {
 #pragma unroll
           for (int c = 0; c < V; ++c) v[u][c] = 0.f;
@@ -115,9 +120,8 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u;
-        const int32_t tok = (i < n) ? tok_s[i] : -1;
-        if (tok >= 0 && tok - t0 >= 0 && tok - t0 < kWin) {
-          const int j = (int)(tok - t0);
+        const int j = (i < n) ? tok_s[i] : -1;
+        if (j >= 0) {
           const float g = g_s[i];
 #pragma unroll
           for (int q = 0; q < V4; ++q) {
@@ -153,12 +157,10 @@ moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src
   const int64_t LK = s.L * s.K;
   dim3 grid((unsigned)((s.L + kWin - 1) / kWin), 1);
   if (s.dtype == MOEBLAZE_BF16) {
-    grid.y = (s.d + kThreads * 8 - 1) / (kThreads * 8);
     identity_combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         reinterpret_cast<const __nv_bfloat16*>(src), disp.expert_token_indices, disp.token_index_map, gates,
         reinterpret_cast<__nv_bfloat16*>(dst), s.L, s.d, s.K, LK);
   } else {
-    grid.y = (s.d + kThreads * 4 - 1) / (kThreads * 4);
     identity_combine_kernel<float><<<grid, kThreads, 0, st>>>(
         reinterpret_cast<const float*>(src), disp.expert_token_indices, disp.token_index_map, gates,
         reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK);
