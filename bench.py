@@ -362,6 +362,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=1, help="workload index (0..4); default: the SiLU bf16 layer")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload with this many tokens instead (smaller profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -371,6 +373,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = I.CONFIGS[args.config]
+    if args.tokens:
+        cfg = cfg.scaled(L=args.tokens, name=f"{cfg.name}_tokens{args.tokens}")
+        I.CONFIGS[args.config] = cfg
 
     if args.impl == "reference":
         if rank != 0:

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict
   extern __shared__ int32_t sm[];
   uint32_t* words = reinterpret_cast<uint32_t*>(sm);  // [E][32]
   int32_t* wpre = sm + E * kChunkWords;               // [E][32]
-  int32_t* off = wpre + E * kChunkWords;              // [E+1]
+  int32_t* off = wpre + E * kChunkWords;              // [E+1], then the chunk bases [E]
   __shared__ int32_t wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int64_t chunk = blockIdx.x;
@@ -169,13 +169,16 @@ __global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict
     const int e = i / kChunkWords, w = i % kChunkWords;
     words[i] = bitmap[(int64_t)e * words_per_expert + chunk * kChunkWords + w];
   }
+  // the chunk's per-expert bases, staged with the words (one coalesced read)
+  int32_t* cbase = off + E + 1;
+  if (tid < E) cbase[tid] = base[chunk * E + tid];
   __syncthreads();
 
   // first position of every (expert, word): warp per expert
   for (int e = warp; e < E; e += nw) {
     const int c = __popc(words[e * kChunkWords + lane]);
     const int in = warp_incl_scan(c, lane);
-    wpre[e * kChunkWords + lane] = off[e] + base[chunk * E + e] + in - c;
+    wpre[e * kChunkWords + lane] = off[e] + cbase[e] + in - c;
   }
   __syncthreads();
 
@@ -274,7 +277,7 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(w.base, C, E, meta.n_e);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  size_t sm3 = (size_t)E * kChunkWords * 8 + (E + 1) * sizeof(int32_t);
+  size_t sm3 = (size_t)E * kChunkWords * 8 + (2 * E + 1) * sizeof(int32_t);
   if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
   scatter_kernel<<<(unsigned)C, 1024, sm3, st>>>(ids, L, E, K, w.bitmap, wpe, w.base, meta.n_e,
                                                   out.expert_token_indices, out.expert_token_offsets,

@@ -10,8 +10,8 @@
 // the grouped expert GEMM walks its rows).  The CTA then walks them in that
 // order, reading each routed row through expert_token_indices (the gather)
 // and adding g * row into a shared-memory fp32 accumulator, one chunk of
-// 1024 (bf16) or 512 (fp32) columns at a time with eight 16-byte row loads in
-// flight per thread; every thread owns the same columns of all 8 rows, so the
+// 1024 (bf16) or 512 (fp32) columns at a time with sixteen 16-byte row loads
+// in flight per thread; every thread owns the same columns of all 8 rows, so the
 // accumulation needs no atomics and the sorted list is built once per window.  Each output row is written once, each input row is read
 // from HBM once (its K reads fall inside one CTA), the routed (L*K, d)
 // buffer never exists.
@@ -30,8 +30,7 @@ struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16* p, float* f) {
-    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  __device__ static void unpack(uint4 u, float* f) {
     float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
   }
@@ -45,9 +44,8 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
   static constexpr int N = 4;
-  __device__ static void load(const float* p, float* f) {
-    float4 v = __ldg(reinterpret_cast<const float4*>(p));
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  __device__ static void unpack(uint4 u, float* f) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
   }
   __device__ static void store(float* p, const float* f) {
     *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
@@ -103,19 +101,15 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
     if (col >= d) break;
 #pragma unroll
     for (int j = 0; j < kWin * V4; ++j) acc[j * kThreads + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int U = 8;
+    // 16 routed-row loads in flight per thread, kept packed until used
+    constexpr int U = 16;
     for (int i0 = 0; i0 < n; i0 += U) {
-      float v[U][V];
+      uint4 raw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u;
         const int j = (i < n) ? tok_s[i] : -1;
-        if (j >= 0) {
-          Vec<T>::load(src + (t0 + j) * d + col, v[u]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < V; ++c) v[u][c] = 0.f;
-        }
+        raw[u] = (j >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + (t0 + j) * d + col)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -123,13 +117,15 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
         const int j = (i < n) ? tok_s[i] : -1;
         if (j >= 0) {
           const float g = g_s[i];
+          float v[V];
+          Vec<T>::unpack(raw[u], v);
 #pragma unroll
           for (int q = 0; q < V4; ++q) {
             float4 a = acc[(j * V4 + q) * kThreads + tid];
-            a.x += g * v[u][4 * q + 0];
-            a.y += g * v[u][4 * q + 1];
-            a.z += g * v[u][4 * q + 2];
-            a.w += g * v[u][4 * q + 3];
+            a.x += g * v[4 * q + 0];
+            a.y += g * v[4 * q + 1];
+            a.z += g * v[4 * q + 2];
+            a.w += g * v[4 * q + 3];
             acc[(j * V4 + q) * kThreads + tid] = a;
           }
         }
