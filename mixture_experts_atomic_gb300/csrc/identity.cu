@@ -9,9 +9,9 @@
 // ascending, which is expert-major order restricted to the window (the order
 // the grouped expert GEMM walks its rows).  The CTA then walks them in that
 // order, reading each routed row through expert_token_indices (the gather)
-// and adding g * row into a shared-memory fp32 accumulator, one chunk of
-// 1024 (bf16) or 512 (fp32) columns at a time with sixteen 16-byte row loads
-// in flight per thread; every thread owns the same columns of all 8 rows, so the
+// and adding g * row into fp32 register accumulators, one chunk of 1024
+// (bf16) or 512 (fp32) columns at a time with eight 16-byte row loads in
+// flight per thread; every thread owns the same columns of all 8 rows, so the
 // accumulation needs no atomics and the sorted list is built once per window.  Each output row is written once, each input row is read
 // from HBM once (its K reads fall inside one CTA), the routed (L*K, d)
 // buffer never exists.
@@ -22,7 +22,7 @@
 namespace moeblaze {
 namespace {
 
-constexpr int kWin = 8;        // tokens per CTA
+constexpr int kWin = 8;        // tokens per CTA (the accumulator switch below has 8 rows)
 constexpr int kThreads = 128;  // 16 bytes per thread per row
 
 template <typename T>
@@ -60,8 +60,6 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
                                                                     T* __restrict__ dst, int64_t L, int d, int K,
                                                                     int64_t LK) {
   constexpr int V = Vec<T>::N;
-  constexpr int V4 = V / 4;
-  __shared__ float4 acc[kWin * V4 * kThreads];
   __shared__ int32_t pos_in[kWin * kMaxK], pos_s[kWin * kMaxK], tok_s[kWin * kMaxK];
   __shared__ float g_in[kWin * kMaxK], g_s[kWin * kMaxK];
 
@@ -96,13 +94,18 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
   __syncthreads();
 
   // The same sorted list serves every column chunk of the window's rows.
+  // Each thread keeps its columns of all 8 rows in registers; the row of an
+  // entry is the same for every thread, so the switch below selects a
+  // register accumulator without divergence.
   for (int cb = 0; cb < d; cb += kThreads * V) {
     const int col = cb + tid * V;
     if (col >= d) break;
+    float acc[kWin][V];
 #pragma unroll
-    for (int j = 0; j < kWin * V4; ++j) acc[j * kThreads + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // 16 routed-row loads in flight per thread, kept packed until used
-    constexpr int U = 16;
+    for (int j = 0; j < kWin; ++j)
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[j][c] = 0.f;
+    constexpr int U = 8;
     for (int i0 = 0; i0 < n; i0 += U) {
       uint4 raw[U];
 #pragma unroll
@@ -115,32 +118,25 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u;
         const int j = (i < n) ? tok_s[i] : -1;
-        if (j >= 0) {
-          const float g = g_s[i];
-          float v[V];
-          Vec<T>::unpack(raw[u], v);
-#pragma unroll
-          for (int q = 0; q < V4; ++q) {
-            float4 a = acc[(j * V4 + q) * kThreads + tid];
-            a.x += g * v[4 * q + 0];
-            a.y += g * v[4 * q + 1];
-            a.z += g * v[4 * q + 2];
-            a.w += g * v[4 * q + 3];
-            acc[(j * V4 + q) * kThreads + tid] = a;
-          }
+        const float g = (i < n) ? g_s[i] : 0.f;
+        float v[V];
+        Vec<T>::unpack(raw[u], v);
+        switch (j) {
+#define MB_ACC_ROW(J)                                    \
+  case J:                                                \
+    _Pragma("unroll") for (int c = 0; c < V; ++c) acc[J][c] += g * v[c]; \
+    break;
+          MB_ACC_ROW(0) MB_ACC_ROW(1) MB_ACC_ROW(2) MB_ACC_ROW(3)
+          MB_ACC_ROW(4) MB_ACC_ROW(5) MB_ACC_ROW(6) MB_ACC_ROW(7)
+#undef MB_ACC_ROW
+          default:
+            break;
         }
       }
     }
 #pragma unroll
     for (int j = 0; j < kWin; ++j) {
-      if (t0 + j >= L) break;
-      float f[V];
-#pragma unroll
-      for (int q = 0; q < V4; ++q) {
-        float4 a = acc[(j * V4 + q) * kThreads + tid];
-        f[4 * q + 0] = a.x; f[4 * q + 1] = a.y; f[4 * q + 2] = a.z; f[4 * q + 3] = a.w;
-      }
-      Vec<T>::store(dst + (t0 + j) * d + col, f);
+      if (t0 + j < L) Vec<T>::store(dst + (t0 + j) * d + col, acc[j]);
     }
   }
 }
