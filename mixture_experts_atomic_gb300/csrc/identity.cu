@@ -7,12 +7,13 @@
 // Schedule: one CTA per window of 8 tokens, all columns.  The window's
 // 8*K (token, slot) positions are read from token_index_map and ranked
 // ascending, which is expert-major order restricted to the window (the order
-// the grouped expert GEMM walks its rows).  The CTA then walks them in that
-// order, reading each routed row through expert_token_indices (the gather)
-// and adding g * row into fp32 register accumulators, one chunk of 1024
-// (bf16) or 512 (fp32) columns at a time with eight 16-byte row loads in
-// flight per thread; every thread owns the same columns of all 8 rows, so the
-// accumulation needs no atomics and the sorted list is built once per window.  Each output row is written once, each input row is read
+// the grouped expert GEMM walks its rows).  Like the GEMM path's producer,
+// the CTA then gathers those routed rows, through expert_token_indices and in
+// that order, into a shared-memory tile with 16-byte cp.async (one 1 KB
+// column chunk of every routed row per stage, two stages in flight); like its
+// epilogue, it then combines: every output piece sums the staged slots of its
+// row times their gates in registers and is written once.  No atomics; each
+// source row is read from HBM once (its K slots fall in one CTA).  Each output row is written once, each input row is read
 // from HBM once (its K reads fall inside one CTA), the routed (L*K, d)
 // buffer never exists.
 #include <climits>
@@ -22,8 +23,10 @@
 namespace moeblaze {
 namespace {
 
-constexpr int kWin = 8;        // tokens per CTA (the accumulator switch below has 8 rows)
-constexpr int kThreads = 128;  // 16 bytes per thread per row
+constexpr int kWin = 8;           // tokens per CTA
+constexpr int kThreads = 256;
+constexpr int kChunkBytes = 1024;  // bytes of one routed row per column chunk
+constexpr int kPieces = kChunkBytes / 16;
 
 template <typename T>
 struct Vec;
@@ -52,6 +55,10 @@ struct Vec<float> {
   }
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __restrict__ src,
                                                                     const int32_t* __restrict__ D1,
@@ -59,9 +66,14 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
                                                                     const float* __restrict__ gates,
                                                                     T* __restrict__ dst, int64_t L, int d, int K,
                                                                     int64_t LK) {
-  constexpr int V = Vec<T>::N;
+  constexpr int V = Vec<T>::N;                 // elements per 16-byte piece
+  constexpr int CH = kChunkBytes / sizeof(T);  // columns per chunk
+  extern __shared__ __align__(16) uint8_t stage[];  // [2][n][kChunkBytes]
   __shared__ int32_t pos_in[kWin * kMaxK], pos_s[kWin * kMaxK], tok_s[kWin * kMaxK];
   __shared__ float g_in[kWin * kMaxK], g_s[kWin * kMaxK];
+  __shared__ int32_t slot_of[kWin][kMaxK];
+  __shared__ float gate_of[kWin][kMaxK];
+  __shared__ int32_t nslot[kWin];
 
   const int tid = threadIdx.x;
   const int64_t t0 = (int64_t)blockIdx.x * kWin;
@@ -92,52 +104,60 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
     tok_s[tid] = (tok >= 0 && tok - t0 >= 0 && tok - t0 < kWin) ? (int32_t)(tok - t0) : -1;
   }
   __syncthreads();
+  if (tid < kWin) {  // the staged slots (expert-major) that belong to window row tid
+    int m = 0;
+    for (int i = 0; i < n; ++i)
+      if (tok_s[i] == tid && m < kMaxK) { slot_of[tid][m] = i; gate_of[tid][m] = g_s[i]; ++m; }
+    nslot[tid] = m;
+  }
+  __syncthreads();
 
-  // The same sorted list serves every column chunk of the window's rows.
-  // Each thread keeps its columns of all 8 rows in registers; the row of an
-  // entry is the same for every thread, so the switch below selects a
-  // register accumulator without divergence.
-  for (int cb = 0; cb < d; cb += kThreads * V) {
-    const int col = cb + tid * V;
-    if (col >= d) break;
-    float acc[kWin][V];
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+  const int nchunks = (d + CH - 1) / CH;
+  // gather: the n routed rows of chunk c, in expert-major order, into buffer c & 1
+  auto gather = [&](int c) {
+    const int col0 = c * CH;
+    const uint32_t buf = sbase + (c & 1) * n * kChunkBytes;
+    for (int pc = tid; pc < n * kPieces; pc += kThreads) {
+      const int i = pc / kPieces, off = pc % kPieces;
+      const int j = tok_s[i];
+      const int col = col0 + off * V;
+      if (j >= 0 && col < d) cp_async16(buf + i * kChunkBytes + off * 16, src + (t0 + j) * d + col);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // combine: each output piece sums its row's staged slots with their gates
+  auto combine = [&](int c) {
+    const int col0 = c * CH;
+    const uint8_t* buf = stage + (c & 1) * n * kChunkBytes;
+    for (int pc = tid; pc < kWin * kPieces; pc += kThreads) {
+      const int j = pc / kPieces, off = pc % kPieces;
+      const int col = col0 + off * V;
+      if (t0 + j >= L || col >= d) continue;
+      float acc[V];
 #pragma unroll
-    for (int j = 0; j < kWin; ++j)
-#pragma unroll
-      for (int c = 0; c < V; ++c) acc[j][c] = 0.f;
-    constexpr int U = 8;
-    for (int i0 = 0; i0 < n; i0 += U) {
-      uint4 raw[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u;
-        const int j = (i < n) ? tok_s[i] : -1;
-        raw[u] = (j >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + (t0 + j) * d + col)) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u;
-        const int j = (i < n) ? tok_s[i] : -1;
-        const float g = (i < n) ? g_s[i] : 0.f;
+      for (int e = 0; e < V; ++e) acc[e] = 0.f;
+      for (int m = 0; m < nslot[j]; ++m) {
         float v[V];
-        Vec<T>::unpack(raw[u], v);
-        switch (j) {
-#define MB_ACC_ROW(J)                                    \
-  case J:                                                \
-    _Pragma("unroll") for (int c = 0; c < V; ++c) acc[J][c] += g * v[c]; \
-    break;
-          MB_ACC_ROW(0) MB_ACC_ROW(1) MB_ACC_ROW(2) MB_ACC_ROW(3)
-          MB_ACC_ROW(4) MB_ACC_ROW(5) MB_ACC_ROW(6) MB_ACC_ROW(7)
-#undef MB_ACC_ROW
-          default:
-            break;
-        }
-      }
-    }
+        Vec<T>::unpack(*reinterpret_cast<const uint4*>(buf + slot_of[j][m] * kChunkBytes + off * 16), v);
+        const float g = gate_of[j][m];
 #pragma unroll
-    for (int j = 0; j < kWin; ++j) {
-      if (t0 + j < L) Vec<T>::store(dst + (t0 + j) * d + col, acc[j]);
+        for (int e = 0; e < V; ++e) acc[e] += g * v[e];
+      }
+      Vec<T>::store(dst + (t0 + j) * d + col, acc);
     }
+  };
+  gather(0);
+  for (int c = 0; c < nchunks; ++c) {
+    if (c + 1 < nchunks) {
+      gather(c + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    combine(c);
+    __syncthreads();  // buffer c & 1 is refilled by gather(c + 2)
   }
 }
 
@@ -147,15 +167,19 @@ moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src
                                         const float* gates, void* dst, cudaStream_t st) {
   if (s.L == 0) return MOEBLAZE_OK;
   const int64_t LK = s.L * s.K;
-  dim3 grid((unsigned)((s.L + kWin - 1) / kWin), 1);
+  const dim3 grid((unsigned)((s.L + kWin - 1) / kWin));
+  const size_t smem = 2 * (size_t)kWin * s.K * kChunkBytes;
   if (s.dtype == MOEBLAZE_BF16) {
-    identity_combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(src), disp.expert_token_indices, disp.token_index_map, gates,
-        reinterpret_cast<__nv_bfloat16*>(dst), s.L, s.d, s.K, LK);
+    auto k = identity_combine_kernel<__nv_bfloat16>;
+    if (smem > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), disp.expert_token_indices,
+                                    disp.token_index_map, gates, reinterpret_cast<__nv_bfloat16*>(dst), s.L, s.d,
+                                    s.K, LK);
   } else {
-    identity_combine_kernel<float><<<grid, kThreads, 0, st>>>(
-        reinterpret_cast<const float*>(src), disp.expert_token_indices, disp.token_index_map, gates,
-        reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK);
+    auto k = identity_combine_kernel<float>;
+    if (smem > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const float*>(src), disp.expert_token_indices,
+                                    disp.token_index_map, gates, reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK);
   }
   MB_CUDA(cudaGetLastError());
   count_launch();
