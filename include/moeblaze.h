@@ -126,6 +126,37 @@ MOEBLAZE_API moeblaze_status moeblaze_dispatch_build(const moeblaze_shape* s, co
                                         int validate, moeblaze_stream stream);
 
 /*
+ * Dispatch build for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that are handed their input and output buffers and have no way to obtain
+ * a scratch buffer: for example a runtime whose device memory is one
+ * fixed, fully claimed pool, or code on a path where a new device
+ * allocation is not allowed.  It runs the same three-step build as
+ * moeblaze_dispatch_build and writes the same outputs into `out`, but keeps
+ * its scratch (the bitmap and the per-chunk counts) in a fixed array that
+ * lives inside the library: MOEBLAZE_STATIC_SCRATCH_BYTES bytes on every GPU
+ * that loads the library, held until the process exits.
+ *   - A shape whose scratch would exceed MOEBLAZE_STATIC_SCRATCH_BYTES
+ *     (moeblaze_dispatch_workspace_bytes(s) > the limit; roughly
+ *     E * ceil(L / 1024) * 132 bytes) is rejected with
+ *     MOEBLAZE_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (a one-time set-up per device); make that first call
+ *     before any stream capture.
+ *   - Nothing is allocated or freed: no cudaMalloc, no cudaFree.
+ *   - Every call, on any stream, shares the one array and it keeps the last
+ *     call's contents (the build rewrites every scratch word it reads, so
+ *     nothing has to start at zero).  Calls whose GPU work overlaps in time
+ *     race on the array: serialise them (one stream, or events).
+ * Arguments, outputs, validate and errors are as for moeblaze_dispatch_build.
+ */
+#define MOEBLAZE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+MOEBLAZE_API moeblaze_status moeblaze_dispatch_build_static(const moeblaze_shape* s, const int32_t* topk_ids,
+                                                         const moeblaze_dispatch* out, int validate,
+                                                         moeblaze_stream stream);
+
+/*
  * Forward pass (MoEBlaze, awesome-system-papers page, sections
  * "免物化 token dispatch" (Forward) and "SwiGLU kernel 融合 + activation
  * checkpoint"): for every expert, its rows of x are gathered on the fly

@@ -29,7 +29,11 @@ EXPORTS = [
     "moeblaze_forward_workspace_bytes", "moeblaze_backward_workspace_bytes", "moeblaze_dispatch_build",
     "moeblaze_forward", "moeblaze_backward", "moeblaze_device_error", "moeblaze_status_string",
     "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
+    "moeblaze_dispatch_build_static",
 ]
+
+# fixed scratch of moeblaze_dispatch_build_static (MOEBLAZE_STATIC_SCRATCH_BYTES)
+STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class Shape(ctypes.Structure):
@@ -67,6 +71,8 @@ def lib():
             getattr(L, n).restype = sz
         L.moeblaze_dispatch_build.argtypes = [SP, P, DP, P, sz, ctypes.c_int, P]
         L.moeblaze_dispatch_build.restype = ctypes.c_int
+        L.moeblaze_dispatch_build_static.argtypes = [SP, P, DP, ctypes.c_int, P]
+        L.moeblaze_dispatch_build_static.restype = ctypes.c_int
         L.moeblaze_forward.argtypes = [SP, P, P, DP, P, P, P, P, P, P, sz, P]
         L.moeblaze_forward.restype = ctypes.c_int
         L.moeblaze_backward.argtypes = [SP, P, P, P, DP, P, P, P, P, P, P, P, P, P, sz, P]
@@ -114,6 +120,11 @@ def moeblaze_backward_workspace_bytes(shape: Shape) -> int:
 def moeblaze_dispatch_build(shape, topk_ids, disp, ws, ws_bytes, validate, stream) -> int:
     return lib().moeblaze_dispatch_build(ctypes.byref(shape), topk_ids, ctypes.byref(disp), ws, ws_bytes,
                                          int(validate), stream)
+
+
+def moeblaze_dispatch_build_static(shape, topk_ids, disp, validate, stream) -> int:
+    return lib().moeblaze_dispatch_build_static(ctypes.byref(shape), topk_ids, ctypes.byref(disp), int(validate),
+                                                stream)
 
 
 def moeblaze_forward(shape, x, gates, disp, W1, W2, W3, y, saved, ws, ws_bytes, stream) -> int:

@@ -171,6 +171,22 @@ moeblaze_status moeblaze_dispatch_build(const moeblaze_shape* s, const int32_t* 
   return (code & kErrBadRouting) ? MOEBLAZE_ERR_BAD_ROUTING : MOEBLAZE_OK;
 }
 
+moeblaze_status moeblaze_dispatch_build_static(const moeblaze_shape* s, const int32_t* topk_ids,
+                                               const moeblaze_dispatch* out, int validate, moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if ((r = check_dispatch(out)) != MOEBLAZE_OK) return r;
+  if (s->L > 0 && !ok_ptr(topk_ids)) return MOEBLAZE_ERR_INVALID_ARG;
+  if (dispatch_ws_bytes(*s) > MOEBLAZE_STATIC_SCRATCH_BYTES) return MOEBLAZE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  r = launch_dispatch_static(*s, topk_ids, *out, st);
+  if (r != MOEBLAZE_OK || !validate) return r;
+  int32_t code = 0;
+  MB_CUDA(cudaMemcpyAsync(&code, out->meta, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MB_CUDA(cudaStreamSynchronize(st));
+  return (code & kErrBadRouting) ? MOEBLAZE_ERR_BAD_ROUTING : MOEBLAZE_OK;
+}
+
 moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const float* gates,
                                  const moeblaze_dispatch* disp, const void* W1, const void* W2, const void* W3,
                                  void* y, void* saved, void* ws, size_t ws_bytes, moeblaze_stream stream) {

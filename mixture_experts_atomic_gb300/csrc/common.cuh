@@ -78,6 +78,9 @@ inline size_t meta_bytes(int64_t LK, int E) {
 moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
                                 void* ws, cudaStream_t st);
 size_t dispatch_ws_bytes(const moeblaze_shape& s);
+// the dispatch build on the library's fixed scratch array (see dispatch.cu)
+moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
+                                       cudaStream_t st);
 
 // identity.cu
 moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,

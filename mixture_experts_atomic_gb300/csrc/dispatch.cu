@@ -22,11 +22,18 @@
 //
 // No global atomics on the data path (the device error word is the only
 // atomic, and only for invalid routing).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moeblaze {
 
 namespace {
+
+// Fixed scratch for callers that cannot allocate (moeblaze_dispatch_build_static).
+// In host code this name is only a host-side stand-in: the device address is
+// looked up per device with cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_static_scratch[MOEBLAZE_STATIC_SCRATCH_BYTES];
 
 // dispatch workspace: bitmap [E][C*32] u32 | cnt/base [C][E] i32
 struct DispatchWs {
@@ -243,6 +250,28 @@ __global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict
 }
 
 }  // namespace
+
+moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
+                                       cudaStream_t st) {
+  constexpr int kMaxDev = 64;
+  static void* addr[kMaxDev] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  MB_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDev) return MOEBLAZE_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      // one-time set-up on this device (the current one): the array's device address
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOEBLAZE_ERR_CUDA;
+      addr[dev] = p;
+    }
+    ws = addr[dev];
+  }
+  return launch_dispatch(s, ids, out, ws, st);
+}
 
 size_t dispatch_ws_bytes(const moeblaze_shape& s) {
   int64_t C = num_chunks(s.L);
