@@ -15,7 +15,8 @@ namespace moeblaze {
 // ---------------------------------------------------------------- constants
 constexpr int kChunkTokens = 1024;       // tokens per dispatch chunk (32 bitmap words)
 constexpr int kChunkWords = kChunkTokens / 32;
-constexpr int kRowPad = 128;             // expert row segments are padded to this
+constexpr int kRowPad = 256;             // expert row segments are padded to this (a pair of GEMM tiles)
+constexpr int kTileM = 128;              // rows of one GEMM tile
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 8;
 
@@ -27,9 +28,9 @@ constexpr int kErrTimeout = 2;
 // The meta buffer written by the dispatch build and read by the GEMMs:
 //   int32 header[8]          err, num_m_tiles, padded_rows, reserved...
 //   int32 n_e[E]             tokens per expert
-//   int32 pad_off[E+1]       padded row offset of each expert (multiples of 128)
+//   int32 pad_off[E+1]       padded row offset of each expert (multiples of 256)
 //   int32 order[E]           experts by descending n_e (ties: lower id first)
-//   int32 tile_expert[MT]    expert of each 128-row tile, MT = max_m_tiles
+//   int32 tile_expert[MT]    expert of each 128-row tile, MT = max_m_tiles (an even count per expert)
 struct MetaView {
   int32_t* err;
   int32_t* num_m_tiles;
@@ -44,7 +45,7 @@ inline int64_t max_padded_rows(int64_t LK, int E) {
   int64_t r = LK + (int64_t)E * (kRowPad - 1);
   return (r + kRowPad - 1) / kRowPad * kRowPad;
 }
-inline int64_t max_m_tiles(int64_t LK, int E) { return max_padded_rows(LK, E) / kRowPad; }
+inline int64_t max_m_tiles(int64_t LK, int E) { return max_padded_rows(LK, E) / kTileM; }
 inline int64_t num_chunks(int64_t L) { return (L + kChunkTokens - 1) / kChunkTokens; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -219,16 +219,16 @@ __global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict
       }
       poff[E] = run;
       meta.pad_off[E] = run;
-      *meta.num_m_tiles = run / kRowPad;
+      *meta.num_m_tiles = run / kTileM;
       *meta.padded_rows = run;
     }
     __syncthreads();
-    const int32_t ntiles = poff[E] / kRowPad;
+    const int32_t ntiles = poff[E] / kTileM;
     for (int64_t m = tid; m < max_tiles; m += blockDim.x) {
       int32_t ex = -1;
       if (m < ntiles) {  // binary search: last e with poff[e] <= m*128
         int lo = 0, hi = E - 1;
-        const int32_t r = (int32_t)m * kRowPad;
+        const int32_t r = (int32_t)m * kTileM;
         while (lo < hi) {
           int mid = (lo + hi + 1) >> 1;
           if (poff[mid] <= r) lo = mid; else hi = mid - 1;

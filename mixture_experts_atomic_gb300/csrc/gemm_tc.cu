@@ -18,8 +18,8 @@
 //               plain stores).
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
-// [pad_off[e], pad_off[e+1]), 128-row aligned, so every 128-row M tile
-// belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
+// [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile (and
+// every pair of them that a cluster shares) belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
 // routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
 // gather a valid token and are zero where they feed a reduction.
 //
@@ -163,6 +163,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// multicast form: the box lands at `dst` and completes `bar` in every CTA of `mask`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -195,6 +212,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// arrive on `bar` at the same offset in every CTA of `mask` once this thread's MMAs retire
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -318,28 +342,37 @@ struct Tile {
   int n_e;      // tokens routed to e
 };
 
-template <int MODE>
-__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt) {
+// Tile `tile` of the launch.  With PAIR the two CTAs of a cluster walk the
+// same sequence of pair tiles and take the half given by their rank: two
+// 128-row tiles of one expert (the rows of a 256-row padded segment pair, or
+// two 128-row slices of d for dW1/dW2) sharing the weight-side operand, or
+// for dW3 two 256-column slices of d sharing the Hg tile.
+template <int MODE, bool PAIR>
+__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt, int rank) {
   Tile t;
   constexpr int TN = tile_n(MODE);
+  constexpr int PM = (PAIR && MODE != DW3) ? 2 : 1;  // tiles paired along M
+  constexpr int PN = (PAIR && MODE == DW3) ? 2 : 1;  // tiles paired along N
   int nt;
   if constexpr (is_wgrad(MODE)) {
-    const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
-    const int rank = (int)(tile / per_e);
+    const int mtp = p.m_tiles_w / PM, ntp = p.n_tiles / PN;
+    const int64_t per_e = (int64_t)mtp * ntp;
+    const int rk = (int)(tile / per_e);
     const int r = (int)(tile % per_e);
-    const int mt = r % p.m_tiles_w;
-    nt = r / p.m_tiles_w;
-    t.e = p.meta.order[rank];
+    const int mt = (r % mtp) * PM + (PM == 2 ? rank : 0);
+    nt = (r / mtp) * PN + (PN == 2 ? rank : 0);
+    t.e = p.meta.order[rk];
     t.row0 = mt * BM;
     t.pad0 = p.meta.pad_off[t.e];
     t.kblocks = (p.meta.pad_off[t.e + 1] - t.pad0) / BK;
   } else {
-    constexpr int GM = 16;
+    constexpr int GM = 8;  // groups of GM m-tile pairs (or 2*GM m-tiles) share weight tiles in L2
+    const int nmu = num_mt / PM;
     const int64_t per_g = (int64_t)GM * p.n_tiles;
     const int g = (int)(tile / per_g);
     const int r = (int)(tile % per_g);
-    const int gm = min(GM, num_mt - g * GM);
-    const int mt = g * GM + r % gm;
+    const int gm = min(GM, nmu - g * GM);
+    const int mt = (g * GM + r % gm) * PM + (PM == 2 ? rank : 0);
     nt = r / gm;
     t.e = p.meta.tile_expert[mt];
     t.row0 = mt * BM;
@@ -376,9 +409,15 @@ __host__ __device__ constexpr bool cp_a(int m) {
 }
 __host__ __device__ constexpr bool cp_b(int m) { return m == DW3; }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
+  // With PAIR the kernel runs as clusters of two CTAs: each CTA loads half of
+  // the shared operand's boxes and multicasts them to both, and a stage is
+  // free again only when both CTAs' MMAs have consumed it.
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  const int64_t cta0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t ncta = PAIR ? gridDim.x / 2 : gridDim.x;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
@@ -393,7 +432,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(s), CP ? PRODUCER_THREADS : 1);
-      mbar_init(bar(4 + s), 1);
+      mbar_init(bar(4 + s), PAIR ? 2 : 1);
     }
     mbar_init(bar(8), 1);
     mbar_init(bar(9), 1);
@@ -411,11 +450,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
-  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
+  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)(num_mt / (PAIR ? 2 : 1)) * p.n_tiles;
   int32_t* err = p.meta.err;
 
   if (warp < PRODUCER_WARPS) {
@@ -449,15 +489,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         }
       };
       Tile t;
-      if (blockIdx.x < total) {
-        t = decode<MODE>(p, blockIdx.x, num_mt);
+      if (cta0 < total) {
+        t = decode<MODE, PAIR>(p, cta0, num_mt, rank);
         load_tile_tokens(t, rtok, wtok);
       }
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const int64_t ntile = tile + gridDim.x;
+      for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
+        const int64_t ntile = tile + ncta;
         Tile tn;
         if (ntile < total) {
-          tn = decode<MODE>(p, ntile, num_mt);
+          tn = decode<MODE, PAIR>(p, ntile, num_mt, rank);
           load_tile_tokens(tn, rnext, wfirst);
         }
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
@@ -489,36 +529,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             else mbar_expect_tx(full, tma_bytes);
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
+            // Box j of the operand both CTAs of a pair share: with PAIR the
+            // CTA of rank j % 2 loads it for both (multicast), else this CTA.
+            auto shared_box = [&](int j, uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+              if constexpr (PAIR) {
+                if ((j & 1) == rank) tma_load_2d_mc(dst, m, c0, c1, full, (uint16_t)0x3);
+              } else {
+                tma_load_2d(dst, m, c0, c1, full);
+              }
+            };
             if constexpr (MODE == DOWN || MODE == DX) {
               tma_load_2d(sA, &p.tmA, k0, t.row0, full);
             } else if constexpr (MODE == DW3) {
-              tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
-              tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
+              shared_box(0, sA, &p.tmA, t.row0, t.pad0 + k0);
+              shared_box(1, sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0);
             }
             if constexpr (MODE == UP_SWIGLU) {
-              tma_load_2d(sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
-              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0, full);
-              tma_load_2d(sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0, full);
-              tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
+              shared_box(0, sB, &p.tmB0, t.n0, t.e * p.d + k0);
+              shared_box(1, sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0);
+              shared_box(2, sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0);
+              shared_box(3, sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0);
             } else if constexpr (MODE == UP_SILU) {
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
+              for (int j = 0; j < t.nw / 64; ++j) shared_box(j, sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0);
             } else if constexpr (MODE == DOWN) {
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, full);
+              for (int j = 0; j < t.nw / 64; ++j) shared_box(j, sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0);
             } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
               for (int j = 0; j < t.nw / 128; ++j)
-                tma_load_2d(sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
+                shared_box(j, sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j);
             } else if constexpr (MODE == DX) {
               const bool second = kb >= p.ksplit;
               const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
               const int kc = second ? k0 - p.ksplit * BK : k0;
-              for (int j = 0; j < t.nw / 128; ++j) tma_load_2d(sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j, full);
+              for (int j = 0; j < t.nw / 128; ++j) shared_box(j, sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j);
             } else if constexpr (MODE == DW12) {
-              tma_load_2d(sB, &p.tmB0, t.n0, t.pad0 + k0, full);
-              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0, full);
-              tma_load_2d(sB + 16384, &p.tmB0, p.h + t.n0, t.pad0 + k0, full);
-              tma_load_2d(sB + 24576, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0, full);
+              shared_box(0, sB, &p.tmB0, t.n0, t.pad0 + k0);
+              shared_box(1, sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0);
+              shared_box(2, sB + 16384, &p.tmB0, p.h + t.n0, t.pad0 + k0);
+              shared_box(3, sB + 24576, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0);
             } else if constexpr (MODE == DW1) {
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.pad0 + k0, full);
+              for (int j = 0; j < t.nw / 64; ++j) shared_box(j, sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.pad0 + k0);
             }
           }
           if constexpr (CP) {
@@ -590,8 +639,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       int abuf = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode<MODE>(p, tile, num_mt);
+      for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
+        const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
         ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err);
@@ -610,7 +659,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
             mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
-          mma_commit(bar(4 + s));
+          if constexpr (PAIR) mma_commit_mc(bar(4 + s), (uint16_t)0x3);  // frees the stage in both CTAs
+          else mma_commit(bar(4 + s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -629,8 +679,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     StoreRing ring{smem_base + STAGES * STAGE_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
-    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode<MODE>(p, tile, num_mt);
+    for (int64_t tile = cta0; tile < total; tile += ncta) {
+      const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
       constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
@@ -805,6 +855,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no remote arrive or multicast is still headed for this CTA
   tc_fence_after();
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
@@ -842,13 +893,37 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
-  if (tiles_bound <= 0) return MOEBLAZE_OK;
-  auto kern = moe_gemm_kernel<MODE>;
+// Launch one GEMM stage.  `units` bounds the number of (pair) tiles; the grid
+// is one CTA per SM (one cluster of two per SM pair with PAIR), never more
+// than there are units.
+template <int MODE, bool PAIR>
+moeblaze_status launch(Params& p, int64_t units, cudaStream_t st) {
+  if (units <= 0) return MOEBLAZE_OK;
+  auto kern = moe_gemm_kernel<MODE, PAIR>;
   MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-  const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
-  kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(2 * ((sm_count() / 2))));
+    int clusters = 0;
+    MB_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
+    if (clusters < 1) return MOEBLAZE_ERR_CUDA;
+    const int64_t g = units < clusters ? units : clusters;
+    cfg.gridDim = dim3((unsigned)(2 * g));
+    MB_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
+  } else {
+    const int64_t g = units < sm_count() ? units : sm_count();
+    kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  }
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
@@ -916,7 +991,8 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = sw ? launch<UP_SWIGLU, true>(p, mt_bound / 2 * p.n_tiles, st)
+                             : launch<UP_SILU, true>(p, mt_bound / 2 * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
@@ -929,7 +1005,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsY32;
-      moeblaze_status r = launch<DOWN>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = launch<DOWN, true>(p, mt_bound / 2 * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
   }
@@ -968,7 +1044,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       p.ld0 = nb * s.h;
-      moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = sw ? launch<DH_SWIGLU, true>(p, mt_bound / 2 * p.n_tiles, st)
+                             : launch<DH_SILU, true>(p, mt_bound / 2 * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
@@ -982,7 +1059,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = s.h / BK;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsdX32;
-      moeblaze_status r = launch<DX>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = launch<DX, true>(p, mt_bound / 2 * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
   }
@@ -995,9 +1072,12 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.N = s.h;
     p.m_tiles_w = s.d / BM;
     p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
-    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
+    const bool pair = p.m_tiles_w % 2 == 0;  // pairs of 128-row slices of d share the dA|dB tile
+    p.total_w = (int64_t)s.E * (p.m_tiles_w / (pair ? 2 : 1)) * p.n_tiles;
     p.o0 = dW1; p.o1 = dW2;
-    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
+    moeblaze_status r;
+    if (sw) r = pair ? launch<DW12, true>(p, p.total_w, st) : launch<DW12, false>(p, p.total_w, st);
+    else r = pair ? launch<DW1, true>(p, p.total_w, st) : launch<DW1, false>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(3, st);
@@ -1009,9 +1089,10 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.N = s.d;
     p.m_tiles_w = s.h / BM;
     p.n_tiles = (s.d + 255) / 256;
-    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
+    const bool pair = p.n_tiles % 2 == 0;  // pairs of 256-column slices of d share the Hg tile
+    p.total_w = (int64_t)s.E * p.m_tiles_w * (p.n_tiles / (pair ? 2 : 1));
     p.o0 = dW3;
-    moeblaze_status r = launch<DW3>(p, p.total_w, st);
+    moeblaze_status r = pair ? launch<DW3, true>(p, p.total_w, st) : launch<DW3, false>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(4, st);
