@@ -137,25 +137,38 @@ __device__ __forceinline__ void cp_async_wait() {
 // order this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core / TMA) accesses
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// CL: acquire at cluster scope, for barriers that receive arrivals from the peer CTA
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CL) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // Bounded wait for the phase of `parity` of `bar`; false on expiry or, when
 // `abort_s` is given, as soon as another role of the CTA has given up.
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int32_t* err,
                                              uint64_t limit_ns = kTimeoutNs) {
-  if (mbar_try(bar, parity)) return true;
+  if (mbar_try<CL>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_try<CL>(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (abort_s && *abort_s) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -468,17 +481,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   const uint32_t smem_base = smem_u32(smem);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   // the barrier the MMA issuer waits on: this CTA's, or rank 0's with CG = 2
-  auto lbar = [&](int i) { return CG == 2 ? leader_addr(bar(i)) : bar(i); };
+  // waits on barriers that the peer CTA also arrives on acquire at cluster scope
+  auto wait = [&](uint32_t b, uint32_t par, volatile int* ab, int32_t* er, uint64_t lim = kTimeoutNs) {
+    return wait_bounded<CG == 2>(b, par, ab, er, lim);
+  };
 
   if (threadIdx.x == 0) {
+    // Every copy completes on its own CTA's stage barrier; with CG = 2 rank 1
+    // relays one arrival per stage to rank 0's (one more expected there), and
+    // rank 1's four epilogue warps release an accumulator with one arrival each.
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_FULL + s), CP ? PRODUCER_THREADS * CG : CG);
+      mbar_init(bar(B_FULL + s), (CP ? PRODUCER_THREADS : 1) + (CG == 2 && rank == 0 ? 1 : 0));
       mbar_init(bar(B_EMPTY + s), 1);
     }
     mbar_init(bar(B_TFULL), 1);
     mbar_init(bar(B_TFULL + 1), 1);
-    mbar_init(bar(B_TEMPTY), 128 * CG);
-    mbar_init(bar(B_TEMPTY + 1), 128 * CG);
+    mbar_init(bar(B_TEMPTY), 128 + 4 * (CG - 1));
+    mbar_init(bar(B_TEMPTY + 1), 128 + 4 * (CG - 1));
     mbar_init(bar(B_DRAIN), 1);
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -554,14 +573,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if constexpr (CP) {
             // every lane of the four producer warps is here: lane 0 waits, the warp follows
-            if (lane == 0) ok = wait_bounded(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
+            if (lane == 0) ok = wait(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           } else {
             // thread 0 runs this loop alone: no warp-collective operations here
-            ok = wait_bounded(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
+            ok = wait(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
           }
           if (!ok) break;
-          const uint32_t full = lbar(B_FULL + s);
+          const uint32_t full = bar(B_FULL + s);
           const uint32_t sA = smem_base + s * STAGE_BYTES;
           const uint32_t sB = sA + A_BYTES;
           const int k0 = kb * BK;
@@ -575,19 +594,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           if (pt == 0) {
             // ---------------- tiled TMA part of the stage
             const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nb_cta * BK * 2));
-            if constexpr (CG == 2) {
-              if (CP) mbar_expect_tx_cl(full, tma_bytes);
-              else mbar_arrive_expect_tx_cl(full, tma_bytes);
-            } else {
-              if (CP) mbar_expect_tx_only(full, tma_bytes);
-              else mbar_expect_tx(full, tma_bytes);
-            }
+            if (CP) mbar_expect_tx_only(full, tma_bytes);
+            else mbar_expect_tx(full, tma_bytes);
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
-            auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
-              if constexpr (CG == 2) tma_load_2d_cg2(dst, m, c0, c1, full);
-              else tma_load_2d(dst, m, c0, c1, full);
-            };
+            auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) { tma_load_2d(dst, m, c0, c1, full); };
             // B: with CG = 2 this CTA stages columns [128 * rank, 128 * rank + 128) of the
             // 256-wide tile (for the dual stages: rank 0 the first branch, rank 1 the second)
             const int nb0 = t.n0 + (CG == 2 ? 128 * rank : 0);
@@ -660,8 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             if (inflight == LAG) {
               cp_async_wait<LAG>();
               fence_proxy_async();
-              if constexpr (CG == 2) mbar_arrive_cl(lbar(B_FULL + (s + STAGES - LAG) % STAGES));
-              else mbar_arrive(bar(B_FULL + (s + STAGES - LAG) % STAGES));
+              mbar_arrive(bar(B_FULL + (s + STAGES - LAG) % STAGES));
             } else {
               ++inflight;
             }
@@ -686,15 +696,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         // the last `inflight` stages: wait for their copies and arrive
         cp_async_wait<0>();
         fence_proxy_async();
-        for (int i = inflight; i > 0; --i) {
-          if constexpr (CG == 2) mbar_arrive_cl(lbar(B_FULL + (s + STAGES - i) % STAGES));
-          else mbar_arrive(bar(B_FULL + (s + STAGES - i) % STAGES));
-        }
+        for (int i = inflight; i > 0; --i) mbar_arrive(bar(B_FULL + (s + STAGES - i) % STAGES));
       }
       if (!ok && pt == 0) {
         // give the TMA copies already issued a bounded chance to land
         for (int i = 0; i < STAGES; ++i)
-          if (armed & (1u << i)) wait_bounded(bar(B_FULL + i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
+          if (armed & (1u << i)) wait(bar(B_FULL + i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -712,12 +719,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         const Tile t = decode<MODE, CG>(p, tile, num_mt, rank);
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE), CG);
-        ok = wait_bounded(bar(B_TEMPTY + abuf), aph ^ 1u, abort_s, err);
+        ok = wait(bar(B_TEMPTY + abuf), aph ^ 1u, abort_s, err);
         if (!ok) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + abuf * 256;
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          ok = wait_bounded(bar(B_FULL + s), ph, abort_s, err);
+          ok = wait(bar(B_FULL + s), ph, abort_s, err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sA = smem_base + s * STAGE_BYTES;
@@ -741,7 +748,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       // all MMAs issued by this thread retire before TMEM is released
       if constexpr (CG == 2) mma_commit_cg2(bar(B_DRAIN));
       else mma_commit(bar(B_DRAIN));
-      wait_bounded(bar(B_DRAIN), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
+      wait(bar(B_DRAIN), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
+    }
+    if constexpr (CG == 2) {
+      // rank 1: relay each stage's completion (its loads and gathers have
+      // landed) to rank 0's stage barrier with one cluster-scope arrive
+      if (lane == 0 && rank == 1) {
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
+          const Tile t = decode<MODE, CG>(p, tile, num_mt, rank);
+          for (int kb = 0; kb < t.kblocks; ++kb) {
+            ok = wait(bar(B_FULL + s), ph, abort_s, err);
+            if (!ok) break;
+            mbar_arrive_cl(leader_addr(bar(B_FULL + s)));
+            if (++s == STAGES) { s = 0; ph ^= 1u; }
+          }
+        }
+      }
     }
     __syncwarp();
   } else {
@@ -783,7 +808,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         }
       }
       bool ok = true;
-      if (lane == 0) ok = wait_bounded(bar(B_TFULL + abuf), aph, abort_s, err);
+      if (lane == 0) ok = wait(bar(B_TFULL + abuf), aph, abort_s, err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
@@ -917,8 +942,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       }
       (void)rb; (void)vb;
       tc_fence_before();
-      if constexpr (CG == 2) mbar_arrive_cl(lbar(B_TEMPTY + abuf));  // rank 0 reuses the accumulator
-      else mbar_arrive(bar(B_TEMPTY + abuf));
+      if (CG == 1 || rank == 0) {
+        mbar_arrive(bar(B_TEMPTY + abuf));
+      } else {
+        __syncwarp();  // the warp's TMEM reads are done: one arrival on rank 0's barrier
+        if (lane == 0) mbar_arrive_cl(leader_addr(bar(B_TEMPTY + abuf)));
+      }
       if (++abuf == 2) { abuf = 0; aph ^= 1u; }
     }
     // the TMA stores issued by lane 0 complete before the CTA exits
