@@ -18,8 +18,8 @@
 //               plain stores).
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
-// [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile (and
-// every pair of them that a cluster shares) belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
+// [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile
+// belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
 // routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
 // gather a valid token and are zero where they feed a reduction.
 //
@@ -42,31 +42,22 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-// Per-CTA stage ring.  CG = 1: A 128x64 + B up to 256x64 per stage, 4 stages.
-// CG = 2 (a CTA pair issues M = 256 MMAs): each CTA stages its A slice and
-// half of B, 32 KB per stage, 6 stages.  Both rings are 192 KB.
-template <int CG>
-struct Ring {
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
-  static constexpr int B_BYTES = CG == 2 ? 128 * BK * 2 : 256 * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int LAG = STAGES - 2;      // cp.async groups a producer thread keeps in flight
-};
-constexpr int RING_BYTES = 4 * (A_BYTES + 256 * BK * 2);
-static_assert(Ring<1>::STAGES * Ring<1>::STAGE_BYTES == RING_BYTES, "ring size");
-static_assert(Ring<2>::STAGES * Ring<2>::STAGE_BYTES == RING_BYTES, "ring size");
+constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
 constexpr int PRODUCER_WARPS = 4;
 constexpr int PRODUCER_THREADS = PRODUCER_WARPS * 32;
 constexpr int MMA_WARP = PRODUCER_WARPS;
 constexpr int NUM_THREADS = (PRODUCER_WARPS + 1 + 4) * 32;  // producers, MMA, 4 epilogue warps
+constexpr int LAG = STAGES - 2;               // cp.async groups a producer thread keeps in flight
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
 // epilogue staging for TMA stores: per epilogue warp a ring of EPI_RING
 // buffers of 32 rows x 32 bf16 (64-byte swizzle)
 constexpr int EPI_RING = 4;
 constexpr int EPI_BUF_BYTES = 32 * 64;
 constexpr int EPI_STAGE_BYTES = 4 * EPI_RING * EPI_BUF_BYTES;  // 32 KB
-constexpr int SMEM_BYTES = RING_BYTES + EPI_STAGE_BYTES + 1024 + 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 256;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -137,38 +128,25 @@ __device__ __forceinline__ void cp_async_wait() {
 // order this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core / TMA) accesses
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// CL: acquire at cluster scope, for barriers that receive arrivals from the peer CTA
-template <bool CL = false>
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  if constexpr (CL) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  }
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
   return ok != 0;
 }
 // Bounded wait for the phase of `parity` of `bar`; false on expiry or, when
 // `abort_s` is given, as soon as another role of the CTA has given up.
-template <bool CL = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int32_t* err,
                                              uint64_t limit_ns = kTimeoutNs) {
-  if (mbar_try<CL>(bar, parity)) return true;
+  if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try<CL>(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (abort_s && *abort_s) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -185,38 +163,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
-// 2-SM forms: the copy lands in this CTA's shared memory and completes `bar`,
-// which may be the peer CTA's barrier (a shared::cluster address)
-__device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t leader_addr(uint32_t local) {  // same offset in the CTA of rank 0
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(0));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx_cl(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -227,8 +173,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   d |= (uint64_t)2 << 61;   // SWIZZLE_128B
   return d;
 }
-// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, M = 128 * cg
-__device__ __forceinline__ uint32_t instr_desc(int n, bool a_mn, bool b_mn, int cg) {
+// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, M = 128
+__device__ __forceinline__ uint32_t instr_desc(int n, bool a_mn, bool b_mn) {
   uint32_t d = 0;
   d |= 1u << 4;                       // D format fp32
   d |= 1u << 7;                       // A format bf16
@@ -236,27 +182,8 @@ __device__ __forceinline__ uint32_t instr_desc(int n, bool a_mn, bool b_mn, int 
   d |= (a_mn ? 1u : 0u) << 15;        // A MN-major
   d |= (b_mn ? 1u : 0u) << 16;        // B MN-major
   d |= (uint32_t)(n >> 3) << 17;      // N / 8
-  d |= (uint32_t)((BM * cg) >> 4) << 24;  // M / 16
+  d |= (uint32_t)(BM >> 4) << 24;     // M / 16
   return d;
-}
-__device__ __forceinline__ void mma_bf16_cg2(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit_cg2(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// arrive on `bar` at the same offset in both CTAs of the pair
-__device__ __forceinline__ void mma_commit_cg2_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)0x3)
-      : "memory");
 }
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
   asm volatile(
@@ -391,34 +318,28 @@ struct Tile {
   int n_e;      // tokens routed to e
 };
 
-// Tile `tile` of the launch.  With CG = 2 the two CTAs of a cluster walk
-// the same sequence of pair tiles (M = 256: two 128-row tiles of one expert,
-// or two 128-row slices of the weight gradient) and take the half given by
-// their rank.
-template <int MODE, int CG>
-__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt, int rank) {
+template <int MODE>
+__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt) {
   Tile t;
   constexpr int TN = tile_n(MODE);
   int nt;
   if constexpr (is_wgrad(MODE)) {
-    const int mtp = p.m_tiles_w / CG;
-    const int64_t per_e = (int64_t)mtp * p.n_tiles;
-    const int rk = (int)(tile / per_e);
+    const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
+    const int rank = (int)(tile / per_e);
     const int r = (int)(tile % per_e);
-    const int mt = (r % mtp) * CG + rank;
-    nt = r / mtp;
-    t.e = p.meta.order[rk];
+    const int mt = r % p.m_tiles_w;
+    nt = r / p.m_tiles_w;
+    t.e = p.meta.order[rank];
     t.row0 = mt * BM;
     t.pad0 = p.meta.pad_off[t.e];
     t.kblocks = (p.meta.pad_off[t.e + 1] - t.pad0) / BK;
   } else {
-    constexpr int GM = 16 / CG;  // groups of 16 m-tiles share weight tiles in L2
-    const int nmu = num_mt / CG;
+    constexpr int GM = 16;
     const int64_t per_g = (int64_t)GM * p.n_tiles;
     const int g = (int)(tile / per_g);
     const int r = (int)(tile % per_g);
-    const int gm = min(GM, nmu - g * GM);
-    const int mt = (g * GM + r % gm) * CG + rank;
+    const int gm = min(GM, num_mt - g * GM);
+    const int mt = g * GM + r % gm;
     nt = r / gm;
     t.e = p.meta.tile_expert[mt];
     t.row0 = mt * BM;
@@ -455,75 +376,46 @@ __host__ __device__ constexpr bool cp_a(int m) {
 }
 __host__ __device__ constexpr bool cp_b(int m) { return m == DW3; }
 
-template <int MODE, int CG>
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
-  constexpr int STAGES = Ring<CG>::STAGES, STAGE_BYTES = Ring<CG>::STAGE_BYTES, LAG = Ring<CG>::LAG;
-  // With CG = 2 the kernel runs as clusters of two CTAs on two SMs.  The CTA
-  // of rank 0 issues tcgen05.mma.cta_group::2 (M = 256): each CTA stages its
-  // own 128-row A slice and one half of the 256-wide B tile, every load of
-  // both CTAs completes on rank 0's stage barrier, rank 0's commits free the
-  // stage and hand the accumulator to both CTAs, and each CTA's epilogue
-  // drains its own TMEM half and reports back to rank 0.
-  const int rank = CG == 2 ? (int)cluster_rank() : 0;
-  const int64_t cta0 = CG == 2 ? blockIdx.x / 2 : blockIdx.x;
-  const int64_t ncta = CG == 2 ? gridDim.x / 2 : gridDim.x;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_STAGE_BYTES);
-  // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  constexpr int B_FULL = 0, B_EMPTY = STAGES, B_TFULL = 2 * STAGES, B_TEMPTY = 2 * STAGES + 2,
-                B_DRAIN = 2 * STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 21);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
+  // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 17);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  // the barrier the MMA issuer waits on: this CTA's, or rank 0's with CG = 2
-  // waits on barriers that the peer CTA also arrives on acquire at cluster scope
-  auto wait = [&](uint32_t b, uint32_t par, volatile int* ab, int32_t* er, uint64_t lim = kTimeoutNs) {
-    return wait_bounded<CG == 2>(b, par, ab, er, lim);
-  };
 
   if (threadIdx.x == 0) {
-    // Every copy completes on its own CTA's stage barrier; with CG = 2 rank 1
-    // relays one arrival per stage to rank 0's (one more expected there), and
-    // rank 1's four epilogue warps release an accumulator with one arrival each.
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_FULL + s), (CP ? PRODUCER_THREADS : 1) + (CG == 2 && rank == 0 ? 1 : 0));
-      mbar_init(bar(B_EMPTY + s), 1);
+      mbar_init(bar(s), CP ? PRODUCER_THREADS : 1);
+      mbar_init(bar(4 + s), 1);
     }
-    mbar_init(bar(B_TFULL), 1);
-    mbar_init(bar(B_TFULL + 1), 1);
-    mbar_init(bar(B_TEMPTY), 128 + 4 * (CG - 1));
-    mbar_init(bar(B_TEMPTY + 1), 128 + 4 * (CG - 1));
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(8), 1);
+    mbar_init(bar(9), 1);
+    mbar_init(bar(10), 128);
+    mbar_init(bar(11), 128);
+    mbar_init(bar(12), 1);
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == MMA_WARP) {
-    // one warp in each CTA (of the pair) allocates; the pair gets the same columns
-    if constexpr (CG == 2) {
-      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                   "r"(TMEM_COLS)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                   "r"(TMEM_COLS)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
-  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)(num_mt / CG) * p.n_tiles;
+  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
   int32_t* err = p.meta.err;
 
   if (warp < PRODUCER_WARPS) {
@@ -557,30 +449,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         }
       };
       Tile t;
-      if (cta0 < total) {
-        t = decode<MODE, CG>(p, cta0, num_mt, rank);
+      if (blockIdx.x < total) {
+        t = decode<MODE>(p, blockIdx.x, num_mt);
         load_tile_tokens(t, rtok, wtok);
       }
-      for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
-        const int64_t ntile = tile + ncta;
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int64_t ntile = tile + gridDim.x;
         Tile tn;
         if (ntile < total) {
-          tn = decode<MODE, CG>(p, ntile, num_mt, rank);
+          tn = decode<MODE>(p, ntile, num_mt);
           load_tile_tokens(tn, rnext, wfirst);
         }
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
-        const int nb_cta = nmma / CG;  // B columns staged by this CTA
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if constexpr (CP) {
             // every lane of the four producer warps is here: lane 0 waits, the warp follows
-            if (lane == 0) ok = wait(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
+            if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           } else {
             // thread 0 runs this loop alone: no warp-collective operations here
-            ok = wait(bar(B_EMPTY + s), ph ^ 1u, abort_s, err);
+            ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
           }
           if (!ok) break;
-          const uint32_t full = bar(B_FULL + s);
+          const uint32_t full = bar(s);
           const uint32_t sA = smem_base + s * STAGE_BYTES;
           const uint32_t sB = sA + A_BYTES;
           const int k0 = kb * BK;
@@ -593,54 +484,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           if (pt == 0) {
             // ---------------- tiled TMA part of the stage
-            const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nb_cta * BK * 2));
+            const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
             if (CP) mbar_expect_tx_only(full, tma_bytes);
             else mbar_expect_tx(full, tma_bytes);
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
-            auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) { tma_load_2d(dst, m, c0, c1, full); };
-            // B: with CG = 2 this CTA stages columns [128 * rank, 128 * rank + 128) of the
-            // 256-wide tile (for the dual stages: rank 0 the first branch, rank 1 the second)
-            const int nb0 = t.n0 + (CG == 2 ? 128 * rank : 0);
             if constexpr (MODE == DOWN || MODE == DX) {
-              load(sA, &p.tmA, k0, t.row0);
+              tma_load_2d(sA, &p.tmA, k0, t.row0, full);
             } else if constexpr (MODE == DW3) {
-              load(sA, &p.tmA, t.row0, t.pad0 + k0);
-              load(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0);
+              tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
+              tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
             }
             if constexpr (MODE == UP_SWIGLU) {
-              if (CG == 1 || rank == 0) {
-                load(sB, &p.tmB0, t.n0, t.e * p.d + k0);
-                load(sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0);
-              }
-              if (CG == 1 || rank == 1) {
-                const uint32_t o = CG == 2 ? 0u : 16384u;
-                load(sB + o, &p.tmB1, t.n0, t.e * p.d + k0);
-                load(sB + o + 8192, &p.tmB1, t.n0 + 64, t.e * p.d + k0);
-              }
+              tma_load_2d(sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
+              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0, full);
+              tma_load_2d(sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0, full);
+              tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
             } else if constexpr (MODE == UP_SILU) {
-              for (int j = 0; j < nb_cta / 64; ++j) load(sB + j * 8192, &p.tmB0, nb0 + 64 * j, t.e * p.d + k0);
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
             } else if constexpr (MODE == DOWN) {
-              for (int j = 0; j < nb_cta / 64; ++j) load(sB + j * 8192, &p.tmB0, nb0 + 64 * j, t.e * p.h + k0);
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, full);
             } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
-              for (int j = 0; j < nb_cta / 128; ++j) load(sB + j * 16384, &p.tmB0, k0, t.e * p.h + nb0 + 128 * j);
+              for (int j = 0; j < t.nw / 128; ++j)
+                tma_load_2d(sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
             } else if constexpr (MODE == DX) {
               const bool second = kb >= p.ksplit;
               const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
               const int kc = second ? k0 - p.ksplit * BK : k0;
-              for (int j = 0; j < nb_cta / 128; ++j) load(sB + j * 16384, m, kc, t.e * p.d + nb0 + 128 * j);
+              for (int j = 0; j < t.nw / 128; ++j) tma_load_2d(sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j, full);
             } else if constexpr (MODE == DW12) {
-              if (CG == 1 || rank == 0) {
-                load(sB, &p.tmB0, t.n0, t.pad0 + k0);
-                load(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0);
-              }
-              if (CG == 1 || rank == 1) {
-                const uint32_t o = CG == 2 ? 0u : 16384u;
-                load(sB + o, &p.tmB0, p.h + t.n0, t.pad0 + k0);
-                load(sB + o + 8192, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0);
-              }
+              tma_load_2d(sB, &p.tmB0, t.n0, t.pad0 + k0, full);
+              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0, full);
+              tma_load_2d(sB + 16384, &p.tmB0, p.h + t.n0, t.pad0 + k0, full);
+              tma_load_2d(sB + 24576, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0, full);
             } else if constexpr (MODE == DW1) {
-              for (int j = 0; j < nb_cta / 64; ++j) load(sB + j * 8192, &p.tmB0, nb0 + 64 * j, t.pad0 + k0);
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.pad0 + k0, full);
             }
           }
           if constexpr (CP) {
@@ -655,9 +533,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
               }
             } else {
               // MN-major operand gathered along K: 64 routed rows x (atoms of 64 columns)
-              const int col0 = CPA ? t.row0 : t.n0 + (CG == 2 ? 128 * rank : 0);
+              const int col0 = CPA ? t.row0 : t.n0;
               const uint32_t dst0 = CPA ? sA : sB;
-              const int natoms = CPA ? 2 : nb_cta / 64;
+              const int natoms = CPA ? 2 : t.nw / 64;
               for (int j = 0; j < natoms; ++j) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -671,7 +549,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             if (inflight == LAG) {
               cp_async_wait<LAG>();
               fence_proxy_async();
-              mbar_arrive(bar(B_FULL + (s + STAGES - LAG) % STAGES));
+              mbar_arrive(bar((s + STAGES - LAG) % STAGES));
             } else {
               ++inflight;
             }
@@ -696,35 +574,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         // the last `inflight` stages: wait for their copies and arrive
         cp_async_wait<0>();
         fence_proxy_async();
-        for (int i = inflight; i > 0; --i) mbar_arrive(bar(B_FULL + (s + STAGES - i) % STAGES));
+        for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + STAGES - i) % STAGES));
       }
       if (!ok && pt == 0) {
         // give the TMA copies already issued a bounded chance to land
         for (int i = 0; i < STAGES; ++i)
-          if (armed & (1u << i)) wait(bar(B_FULL + i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
+          if (armed & (1u << i)) wait_bounded(bar(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
       }
     }
   } else if (warp == MMA_WARP) {
     // ================================================================ MMA issuer
-    // With CG = 2 only rank 0 issues; the descriptors name the same shared
-    // memory offsets in both CTAs and the accumulator rows land in each
-    // CTA's own TMEM.
-    if (lane == 0 && rank == 0) {
+    if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
       int abuf = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
-        const Tile t = decode<MODE, CG>(p, tile, num_mt, rank);
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode<MODE>(p, tile, num_mt);
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
-        const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE), CG);
-        ok = wait(bar(B_TEMPTY + abuf), aph ^ 1u, abort_s, err);
+        const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
+        ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err);
         if (!ok) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + abuf * 256;
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          ok = wait(bar(B_FULL + s), ph, abort_s, err);
+          ok = wait_bounded(bar(s), ph, abort_s, err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sA = smem_base + s * STAGE_BYTES;
@@ -733,51 +608,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = a_mn_major(MODE) ? smem_desc(sA + kk * 2048, 8192, 1024) : smem_desc(sA + kk * 32, 16, 1024);
             const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
-            if constexpr (CG == 2) mma_bf16_cg2(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
-            else mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
-          if constexpr (CG == 2) mma_commit_cg2_both(bar(B_EMPTY + s));  // frees the stage in both CTAs
-          else mma_commit(bar(B_EMPTY + s));
+          mma_commit(bar(4 + s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        if constexpr (CG == 2) mma_commit_cg2_both(bar(B_TFULL + abuf));
-        else mma_commit(bar(B_TFULL + abuf));
+        mma_commit(bar(8 + abuf));
         if (++abuf == 2) { abuf = 0; aph ^= 1u; }
       }
       // all MMAs issued by this thread retire before TMEM is released
-      if constexpr (CG == 2) mma_commit_cg2(bar(B_DRAIN));
-      else mma_commit(bar(B_DRAIN));
-      wait(bar(B_DRAIN), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
-    }
-    if constexpr (CG == 2) {
-      // rank 1: relay each stage's completion (its loads and gathers have
-      // landed) to rank 0's stage barrier with one cluster-scope arrive
-      if (lane == 0 && rank == 1) {
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int64_t tile = cta0; tile < total && ok; tile += ncta) {
-          const Tile t = decode<MODE, CG>(p, tile, num_mt, rank);
-          for (int kb = 0; kb < t.kblocks; ++kb) {
-            ok = wait(bar(B_FULL + s), ph, abort_s, err);
-            if (!ok) break;
-            mbar_arrive_cl(leader_addr(bar(B_FULL + s)));
-            if (++s == STAGES) { s = 0; ph ^= 1u; }
-          }
-        }
-      }
+      mma_commit(bar(12));
+      wait_bounded(bar(12), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
     }
     __syncwarp();
   } else {
     // ================================================================ epilogue
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter ...
     const int r = quarter * 32 + lane;            // accumulator row of this thread
-    StoreRing ring{smem_base + RING_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
+    StoreRing ring{smem_base + STAGES * STAGE_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
-    for (int64_t tile = cta0; tile < total; tile += ncta) {
-      const Tile t = decode<MODE, CG>(p, tile, num_mt, rank);
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode<MODE>(p, tile, num_mt);
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
       constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
@@ -808,7 +661,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         }
       }
       bool ok = true;
-      if (lane == 0) ok = wait(bar(B_TFULL + abuf), aph, abort_s, err);
+      if (lane == 0) ok = wait_bounded(bar(8 + abuf), aph, abort_s, err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
@@ -942,12 +795,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       }
       (void)rb; (void)vb;
       tc_fence_before();
-      if (CG == 1 || rank == 0) {
-        mbar_arrive(bar(B_TEMPTY + abuf));
-      } else {
-        __syncwarp();  // the warp's TMEM reads are done: one arrival on rank 0's barrier
-        if (lane == 0) mbar_arrive_cl(leader_addr(bar(B_TEMPTY + abuf)));
-      }
+      mbar_arrive(bar(10 + abuf));
       if (++abuf == 2) { abuf = 0; aph ^= 1u; }
     }
     // the TMA stores issued by lane 0 complete before the CTA exits
@@ -957,13 +805,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // no remote arrive or MMA still targets this CTA
   tc_fence_after();
   if (warp == MMA_WARP) {
-    if constexpr (CG == 2)
-      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
-    else
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
   }
 }
 
@@ -998,37 +842,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launch one GEMM stage.  `units` bounds the number of (pair) tiles; the grid
-// is one CTA per SM (one cluster of two per SM pair with CG = 2), never more
-// than there are units.
-template <int MODE, int CG>
-moeblaze_status launch(Params& p, int64_t units, cudaStream_t st) {
-  if (units <= 0) return MOEBLAZE_OK;
-  auto kern = moe_gemm_kernel<MODE, CG>;
+template <int MODE>
+moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
+  if (tiles_bound <= 0) return MOEBLAZE_OK;
+  auto kern = moe_gemm_kernel<MODE>;
   MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-  if constexpr (CG == 2) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)(2 * ((sm_count() / 2))));
-    int clusters = 0;
-    MB_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
-    if (clusters < 1) return MOEBLAZE_ERR_CUDA;
-    const int64_t g = units < clusters ? units : clusters;
-    cfg.gridDim = dim3((unsigned)(2 * g));
-    MB_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
-  } else {
-    const int64_t g = units < sm_count() ? units : sm_count();
-    kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
-  }
+  const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
+  kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
@@ -1096,10 +916,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      moeblaze_status r;
-      if (sw) r = launch<UP_SWIGLU, 2>(p, mt_bound / 2 * p.n_tiles, st);
-      else if (s.h % 256 == 0) r = launch<UP_SILU, 2>(p, mt_bound / 2 * p.n_tiles, st);
-      else r = launch<UP_SILU, 1>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
@@ -1112,8 +929,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsY32;
-      moeblaze_status r = s.d % 256 == 0 ? launch<DOWN, 2>(p, mt_bound / 2 * p.n_tiles, st)
-                                         : launch<DOWN, 1>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = launch<DOWN>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
   }
@@ -1152,10 +968,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       p.ld0 = nb * s.h;
-      const bool cg2 = s.h % 256 == 0;  // 256-wide tiles only
-      moeblaze_status r;
-      if (sw) r = cg2 ? launch<DH_SWIGLU, 2>(p, mt_bound / 2 * p.n_tiles, st) : launch<DH_SWIGLU, 1>(p, mt_bound * p.n_tiles, st);
-      else r = cg2 ? launch<DH_SILU, 2>(p, mt_bound / 2 * p.n_tiles, st) : launch<DH_SILU, 1>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
@@ -1169,8 +982,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = s.h / BK;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsdX32;
-      moeblaze_status r = s.d % 256 == 0 ? launch<DX, 2>(p, mt_bound / 2 * p.n_tiles, st)
-                                         : launch<DX, 1>(p, mt_bound * p.n_tiles, st);
+      moeblaze_status r = launch<DX>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
   }
@@ -1183,13 +995,9 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.N = s.h;
     p.m_tiles_w = s.d / BM;
     p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
-    // pairs of 128-row slices of d; 256-wide tiles only
-    const bool cg2 = p.m_tiles_w % 2 == 0 && (sw || s.h % 256 == 0);
-    p.total_w = (int64_t)s.E * (p.m_tiles_w / (cg2 ? 2 : 1)) * p.n_tiles;
+    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW1; p.o1 = dW2;
-    moeblaze_status r;
-    if (sw) r = cg2 ? launch<DW12, 2>(p, p.total_w, st) : launch<DW12, 1>(p, p.total_w, st);
-    else r = cg2 ? launch<DW1, 2>(p, p.total_w, st) : launch<DW1, 1>(p, p.total_w, st);
+    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(3, st);
@@ -1201,11 +1009,9 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.N = s.d;
     p.m_tiles_w = s.h / BM;
     p.n_tiles = (s.d + 255) / 256;
-    // pairs of 128-row slices of h; 256-wide tiles only
-    const bool cg2 = p.m_tiles_w % 2 == 0 && s.d % 256 == 0;
-    p.total_w = (int64_t)s.E * (p.m_tiles_w / (cg2 ? 2 : 1)) * p.n_tiles;
+    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW3;
-    moeblaze_status r = cg2 ? launch<DW3, 2>(p, p.total_w, st) : launch<DW3, 1>(p, p.total_w, st);
+    moeblaze_status r = launch<DW3>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(4, st);
