@@ -180,7 +180,7 @@ MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const voi
                                  moeblaze_stream stream);
 
 /*
- * Backward pass of the loss <y, dY> with ids and gates held constant
+ * Backward pass of the loss <y, dY> with the routing ids held constant
  * (MoEBlaze, awesome-system-papers page, sections "免物化 token dispatch"
  * (Backward) and "SwiGLU kernel 融合 + activation checkpoint"): dY is
  * gathered to the expert rows through the same indices (no (L*K, d)
@@ -192,13 +192,18 @@ MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const voi
  *   dX      device (L,d) dtype, overwritten
  *   dW1,dW2 device (E,d,h) dtype, overwritten  dW3 device (E,h,d) dtype, overwritten
  *           (dW2 NULL for SiLU; all three NULL for identity)
+ *   dgates  device (L,K) fp32, overwritten, or NULL: the gate gradients
+ *           dg[t,k] = <dY[t], expert_{ids[t,k]}(x[t])> (y is linear in the
+ *           gates), for a router's backward; not on the pages, whose backward
+ *           holds the router fixed.  Summed in fp32 over h in an unspecified
+ *           order.
  *   ws      device moeblaze_backward_workspace_bytes(s) bytes of scratch
  */
 MOEBLAZE_API moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x,
                                   const float* gates, const moeblaze_dispatch* disp,
                                   const void* W1, const void* W2, const void* W3,
                                   const void* saved, void* dX, void* dW1, void* dW2, void* dW3,
-                                  void* ws, size_t ws_bytes, moeblaze_stream stream);
+                                  float* dgates, void* ws, size_t ws_bytes, moeblaze_stream stream);
 
 /* Synchronise `stream` and read the device error word of `disp->meta`:
  * *code = 0 when every kernel since the last dispatch_build on this meta

@@ -75,7 +75,7 @@ def lib():
         L.moeblaze_dispatch_build_static.restype = ctypes.c_int
         L.moeblaze_forward.argtypes = [SP, P, P, DP, P, P, P, P, P, P, sz, P]
         L.moeblaze_forward.restype = ctypes.c_int
-        L.moeblaze_backward.argtypes = [SP, P, P, P, DP, P, P, P, P, P, P, P, P, P, sz, P]
+        L.moeblaze_backward.argtypes = [SP, P, P, P, DP, P, P, P, P, P, P, P, P, P, P, sz, P]
         L.moeblaze_backward.restype = ctypes.c_int
         L.moeblaze_device_error.argtypes = [SP, DP, ctypes.POINTER(ctypes.c_int32), P]
         L.moeblaze_device_error.restype = ctypes.c_int
@@ -132,9 +132,10 @@ def moeblaze_forward(shape, x, gates, disp, W1, W2, W3, y, saved, ws, ws_bytes, 
                                   ws_bytes, stream)
 
 
-def moeblaze_backward(shape, dY, x, gates, disp, W1, W2, W3, saved, dX, dW1, dW2, dW3, ws, ws_bytes, stream) -> int:
+def moeblaze_backward(shape, dY, x, gates, disp, W1, W2, W3, saved, dX, dW1, dW2, dW3, dgates, ws, ws_bytes,
+                      stream) -> int:
     return lib().moeblaze_backward(ctypes.byref(shape), dY, x, gates, ctypes.byref(disp), W1, W2, W3, saved, dX,
-                                   dW1, dW2, dW3, ws, ws_bytes, stream)
+                                   dW1, dW2, dW3, dgates, ws, ws_bytes, stream)
 
 
 def moeblaze_device_error(shape, disp, stream):
@@ -247,10 +248,10 @@ def forward(shape: Shape, x, gates, disp: DispatchBuffers, W1, W2, W3, y, layer:
 
 
 def backward(shape: Shape, dY, x, gates, disp: DispatchBuffers, W1, W2, W3, layer: LayerBuffers, dX, dW1, dW2, dW3,
-             stream=None):
+             dgates=None, stream=None):
     st = moeblaze_backward(shape, _ptr(dY), _ptr(x), _ptr(gates), disp.struct(), _ptr(W1), _ptr(W2), _ptr(W3),
-                           _ptr(layer.saved), _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dW3), _ptr(layer.bwd_ws),
-                           layer.bwd_ws.numel(), _stream(stream))
+                           _ptr(layer.saved), _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dW3), _ptr(dgates),
+                           _ptr(layer.bwd_ws), layer.bwd_ws.numel(), _stream(stream))
     _check(st, "moeblaze_backward")
 
 

@@ -218,21 +218,27 @@ moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const f
 
 moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x, const float* gates,
                                   const moeblaze_dispatch* disp, const void* W1, const void* W2, const void* W3,
-                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3, void* ws,
-                                  size_t ws_bytes, moeblaze_stream stream) {
+                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3, float* dgates,
+                                  void* ws, size_t ws_bytes, moeblaze_stream stream) {
   moeblaze_status r = check_shape(s);
   if (r != MOEBLAZE_OK) return r;
   if ((r = check_dispatch(disp)) != MOEBLAZE_OK) return r;
   const bool tok_ok = s->L == 0 || (ok_ptr(dY) && ok_ptr(gates) && ok_ptr(dX) && ok_ptr(x));
   if (!tok_ok) return MOEBLAZE_ERR_INVALID_ARG;
+  if (dgates && !aligned16(dgates)) return MOEBLAZE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (s->act == MOEBLAZE_IDENTITY) return launch_identity_combine(*s, dY, *disp, gates, dX, st);
+  if (s->act == MOEBLAZE_IDENTITY) {
+    r = launch_identity_combine(*s, dY, *disp, gates, dX, st);
+    if (r != MOEBLAZE_OK || !dgates) return r;
+    return launch_identity_dgates(*s, x, dY, dgates, st);
+  }
   const bool sw = s->act == MOEBLAZE_SWIGLU;
   if (!ok_ptr(W1) || !ok_ptr(W3) || (sw && !ok_ptr(W2)) || !ok_ptr(saved)) return MOEBLAZE_ERR_INVALID_ARG;
   if (!ok_ptr(dW1) || !ok_ptr(dW3) || (sw && !ok_ptr(dW2))) return MOEBLAZE_ERR_INVALID_ARG;
   if (ws_bytes < bwd_ws(s)) return MOEBLAZE_ERR_WORKSPACE;
   if (!ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
   if (s->L == 0) return zero_weight_grads(s, dW1, sw ? dW2 : nullptr, dW3, st);
+  if (dgates) MB_CUDA(cudaMemsetAsync(dgates, 0, sizeof(float) * s->L * s->K, st));
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
   char* w = reinterpret_cast<char*>(ws);
   const size_t es = elem(s);
@@ -242,12 +248,12 @@ moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const
   if (s->dtype == MOEBLAZE_F32) {
     return simt_backward(*s, (const float*)dY, (const float*)x, gates, *disp, (const float*)W1,
                          sw ? (const float*)W2 : nullptr, (const float*)W3, (const float*)saved, (float*)dX,
-                         (float*)dW1, sw ? (float*)dW2 : nullptr, (float*)dW3, (float*)dAB, (float*)Hg, st);
+                         (float*)dW1, sw ? (float*)dW2 : nullptr, (float*)dW3, dgates, (float*)dAB, (float*)Hg, st);
   }
   return tc_backward(*s, (const __nv_bfloat16*)dY, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
                      sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (const __nv_bfloat16*)saved,
                      (__nv_bfloat16*)dX, (__nv_bfloat16*)dW1, sw ? (__nv_bfloat16*)dW2 : nullptr, (__nv_bfloat16*)dW3,
-                     (__nv_bfloat16*)dAB, (__nv_bfloat16*)Hg, (float*)dX32, st);
+                     dgates, (__nv_bfloat16*)dAB, (__nv_bfloat16*)Hg, (float*)dX32, st);
 }
 
 moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp, int32_t* code,

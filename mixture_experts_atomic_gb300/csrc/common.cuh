@@ -86,6 +86,8 @@ moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* i
 // identity.cu
 moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,
                                         const float* gates, void* dst, cudaStream_t st);
+moeblaze_status launch_identity_dgates(const moeblaze_shape& s, const void* x, const void* dY, float* dgates,
+                                       cudaStream_t st);
 
 // simt.cu (fp32 path)
 moeblaze_status simt_forward(const moeblaze_shape& s, const float* x, const float* gates,
@@ -93,7 +95,7 @@ moeblaze_status simt_forward(const moeblaze_shape& s, const float* x, const floa
                              float* y, float* saved, float* wsH, cudaStream_t st);
 moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const float* x, const float* gates,
                               const moeblaze_dispatch& disp, const float* W1, const float* W2, const float* W3,
-                              const float* saved, float* dX, float* dW1, float* dW2, float* dW3,
+                              const float* saved, float* dX, float* dW1, float* dW2, float* dW3, float* dgates,
                               float* wsdAB, float* wsHg, cudaStream_t st);
 
 // gemm_tc.cu (bf16 tensor-core path)
@@ -105,7 +107,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
                             const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
+                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
 
 // shared helpers (abi.cu)
 int sm_count();

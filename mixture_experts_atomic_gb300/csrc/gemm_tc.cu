@@ -99,6 +99,7 @@ struct Params {
   int ld0;          // row stride (elements) of o0 for the stages that need it
   const __nv_bfloat16* gsrc;  // gathered tensor (x or dY), rows of gld elements
   int gld;
+  float* dg;                  // dH stage: gate gradients (L,K) fp32, or null
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -361,10 +362,15 @@ __device__ __forceinline__ int row_token(const Params& p, const Tile& t, int q) 
   return p.D1[t.off + i];
 }
 
-__device__ __forceinline__ float gate_of(const Params& p, int tok, int e) {
+// gate of (token, expert) and its slot k (token_expert_indices[tok, k] == e)
+__device__ __forceinline__ float gate_of(const Params& p, int tok, int e, int* slot = nullptr) {
   const int64_t b = (int64_t)tok * p.K;
   for (int k = 0; k < p.K; ++k)
-    if (p.D3[b + k] == e) return p.gates[b + k];
+    if (p.D3[b + k] == e) {
+      if (slot) *slot = k;
+      return p.gates[b + k];
+    }
+  if (slot) *slot = 0;
   return 0.f;
 }
 
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
       constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
-      int q = 0, tok = 0;
+      int q = 0, tok = 0, kslot = 0;
       bool valid = false;
       float g = 1.f;
       uint4 nA[4], nB[4];
@@ -644,7 +650,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         if constexpr (MODE == DOWN || MODE == DX || DH) {
           if (valid) {
             tok = p.D1[t.off + (q - t.pad0)];
-            if constexpr (MODE != DX) g = gate_of(p, tok, t.e);
+            if constexpr (MODE != DX) g = gate_of(p, tok, t.e, &kslot);
           }
         }
         if constexpr (DH) {
@@ -715,6 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           constexpr bool SW = MODE == DH_SWIGLU;
           const int64_t ro = (int64_t)q * p.h + t.n0;              // A, B rows
           const int nch = t.nw / 32;
+          float dgp = 0.f;  // this tile's part of <H_row, dY W3^T> = <dY, Y_row>
           for (int c = 0; c < nch; ++c) {
             // chunk c of A (B) was loaded one step ahead; start loading chunk c+1
             uint4 cA[4], cB[4];
@@ -749,15 +756,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
                 dA[i] = dH * B[i] * ds;
                 dB[i] = dH * sl;
                 Hg[i] = g * sl * B[i];
+                dgp += sl * B[i] * __uint_as_float(ra[i]);
               } else {
                 dA[i] = dH * ds;
                 Hg[i] = g * sl;
+                dgp += sl * __uint_as_float(ra[i]);
               }
             }
             staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
             if constexpr (SW) staged_store(ring, &p.tmO0, p.h + t.n0 + 32 * c, wrow0, dB, valid, lane);
             staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
           }
+          if (valid && p.dg) atomicAdd(p.dg + (int64_t)tok * p.K + kslot, dgp);
         }
       } else {
         // weight gradients: rows of dW_e, plain bf16 stores
@@ -943,7 +953,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
                             const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st) {
+                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st) {
   const bool sw = s.act == MOEBLAZE_SWIGLU;
   const int nb = sw ? 2 : 1;
   const int64_t LK = s.L * s.K;
@@ -964,6 +974,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = p.kblocks;
       p.n_tiles = (s.h + 255) / 256;
       p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
+      p.dg = dgates;
       const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;

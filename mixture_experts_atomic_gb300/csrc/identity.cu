@@ -161,7 +161,45 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
   }
 }
 
+// Gate gradients of the identity expert: dg[t,k] = <dY[t], x[t]> for every
+// slot k (the expert's output is the token itself).  One warp per token.
+template <typename T>
+__global__ void __launch_bounds__(256) identity_dgates_kernel(const T* __restrict__ x, const T* __restrict__ dY,
+                                                              float* __restrict__ dg, int64_t L, int d, int K) {
+  constexpr int V = Vec<T>::N;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= L) return;
+  float acc = 0.f;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    float a[V], b[V];
+    Vec<T>::unpack(__ldg(reinterpret_cast<const uint4*>(x + t * d + c)), a);
+    Vec<T>::unpack(__ldg(reinterpret_cast<const uint4*>(dY + t * d + c)), b);
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc += a[e] * b[e];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane < K) dg[t * K + lane] = acc;
+}
+
 }  // namespace
+
+moeblaze_status launch_identity_dgates(const moeblaze_shape& s, const void* x, const void* dY, float* dgates,
+                                       cudaStream_t st) {
+  if (s.L == 0) return MOEBLAZE_OK;
+  const unsigned grid = (unsigned)((s.L + 7) / 8);
+  if (s.dtype == MOEBLAZE_BF16)
+    identity_dgates_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                                                reinterpret_cast<const __nv_bfloat16*>(dY), dgates,
+                                                                s.L, s.d, s.K);
+  else
+    identity_dgates_kernel<float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(x),
+                                                        reinterpret_cast<const float*>(dY), dgates, s.L, s.d, s.K);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  return MOEBLAZE_OK;
+}
 
 moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,
                                         const float* gates, void* dst, cudaStream_t st) {

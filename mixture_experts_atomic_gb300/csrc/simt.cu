@@ -51,9 +51,13 @@ struct Common {
     return D1[c.off + i];
   }
   __device__ bool valid(const RowCtx& c, int q) const { return q - c.pad0 < c.n; }
-  __device__ float gate(int t, int e) const {
+  __device__ float gate(int t, int e, int* slot = nullptr) const {
     for (int k = 0; k < K; ++k)
-      if (D3[(int64_t)t * K + k] == e) return gates[(int64_t)t * K + k];
+      if (D3[(int64_t)t * K + k] == e) {
+        if (slot) *slot = k;
+        return gates[(int64_t)t * K + k];
+      }
+    if (slot) *slot = 0;
     return 0.f;
   }
 };
@@ -124,7 +128,7 @@ __global__ void down_kernel(Common c, const float* __restrict__ H, const float* 
 // dA = dH * B * SiLU'(A), dB = dH * SiLU(A), Hg = g * SiLU(A) * B
 __global__ void dh_kernel(Common c, const float* __restrict__ dY, const float* __restrict__ W3,
                           const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ dAB,
-                          float* __restrict__ Hg, bool swiglu) {
+                          float* __restrict__ Hg, float* __restrict__ dg, bool swiglu) {
   __shared__ float Gs[T][T + 1], Ws[T][T + 1];
   __shared__ int toks[T];
   RowCtx r;
@@ -156,7 +160,8 @@ __global__ void dh_kernel(Common c, const float* __restrict__ dY, const float* _
     return;
   }
   const int t = toks[ty];
-  const float g = c.gate(t, r.e);
+  int kslot = 0;
+  const float g = c.gate(t, r.e, &kslot);
   const float dH = g * acc;
   const float a = A[o];
   const float sg = 1.f / (1.f + expf(-a));
@@ -167,9 +172,11 @@ __global__ void dh_kernel(Common c, const float* __restrict__ dY, const float* _
     dAB[oab] = dH * b * dsilu;
     dAB[oab + c.h] = dH * s;
     Hg[o] = g * s * b;
+    if (dg) atomicAdd(&dg[(int64_t)t * c.K + kslot], s * b * acc);  // <H_row, dY W3^T>
   } else {
     dAB[oab] = dH * dsilu;
     Hg[o] = g * s;
+    if (dg) atomicAdd(&dg[(int64_t)t * c.K + kslot], s * acc);
   }
 }
 
@@ -316,7 +323,7 @@ moeblaze_status simt_forward(const moeblaze_shape& s, const float* x, const floa
 
 moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const float* x, const float* gates,
                               const moeblaze_dispatch& disp, const float* W1, const float* W2, const float* W3,
-                              const float* saved, float* dX, float* dW1, float* dW2, float* dW3,
+                              const float* saved, float* dX, float* dW1, float* dW2, float* dW3, float* dgates,
                               float* wsdAB, float* wsHg, cudaStream_t st) {
   const bool swiglu = s.act == MOEBLAZE_SWIGLU;
   const int64_t LK = s.L * s.K;
@@ -328,7 +335,7 @@ moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const fl
   dim3 blk(T, T);
   stage_event(0, st);
   if (s.L > 0) {
-    dh_kernel<<<dim3((unsigned)(rows / T), (s.h + T - 1) / T), blk, 0, st>>>(c, dY, W3, A, B, wsdAB, wsHg, swiglu);
+    dh_kernel<<<dim3((unsigned)(rows / T), (s.h + T - 1) / T), blk, 0, st>>>(c, dY, W3, A, B, wsdAB, wsHg, dgates, swiglu);
     MB_CUDA(cudaGetLastError());
     count_launch();
     stage_event(1, st);

@@ -20,6 +20,7 @@ class MoELayer:
         self.bufs = B.alloc_layer(self.shape, device)
         self.y = torch.empty((L, d), dtype=dtype, device=device)
         self.dX = torch.empty((L, d), dtype=dtype, device=device)
+        self.dgates = torch.empty((L, K), dtype=torch.float32, device=device)
         if act == "identity":
             self.dW1 = self.dW2 = self.dW3 = None
         else:
@@ -40,8 +41,9 @@ class MoELayer:
         return self.y
 
     def backward(self, dY, x, gates, W1=None, W2=None, W3=None):
-        B.backward(self.shape, dY, x, gates, self.disp, W1, W2, W3, self.bufs, self.dX, self.dW1, self.dW2, self.dW3)
-        return self.dX, self.dW1, self.dW2, self.dW3
+        B.backward(self.shape, dY, x, gates, self.disp, W1, W2, W3, self.bufs, self.dX, self.dW1, self.dW2, self.dW3,
+                   self.dgates)
+        return self.dX, self.dW1, self.dW2, self.dW3, self.dgates
 
     def step(self, inp: Dict[str, torch.Tensor]):
         """dispatch build + forward + backward on one batch of inputs."""

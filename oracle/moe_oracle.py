@@ -41,6 +41,7 @@ PINNED = {
     "dispatch": "brute-force per-slot loops, hand-worked golden case, invariants",
     "forward": "per-token brute force, identity closed form, dense-MLP special case",
     "backward": "central finite differences (fp64), torch.autograd of a dense formulation",
+    "backward dgates": "central finite differences in the gates, autograd, hand-worked golden case",
     "forward_rows / backward_rows / weight_grad_slices": "agree with forward/backward on every row and column at small sizes",
 }
 
@@ -198,8 +199,8 @@ def forward(topk_ids, gates, x, W1=None, W2=None, W3=None, act: str = "swiglu",
 
 def backward(topk_ids, gates, x, dY, W1=None, W2=None, W3=None, act: str = "swiglu",
              E: Optional[int] = None):
-    """Hand-derived backward of the loss <y, dY> with ids and gates held
-    constant.  Per expert e and its routed rows (token t, gate g):
+    """Hand-derived backward of the loss <y, dY> with the ids held constant.
+    Per expert e and its routed rows (token t, gate g):
 
         G      = g * dY[t]                       (the gradient scattered to the row)
         dW3_e += H^T G
@@ -209,8 +210,11 @@ def backward(topk_ids, gates, x, dY, W1=None, W2=None, W3=None, act: str = "swig
         dW1_e += X_e^T dA ;  dW2_e += X_e^T dB
         dx[t] += dA W1_e^T + dB W2_e^T
     Identity expert: dx[t] = sum_k g[t,k] dY[t].
+    Gate gradient (y is linear in the gates): dg[t,k] = <dY[t], Y_row>, the
+    expert's output for that routed row before gating.
 
-    Returns (dX (L,d), dW1, dW2, dW3) in fp64 (None where the weight is absent).
+    Returns (dX (L,d), dW1, dW2, dW3, dgates (L,K)) in fp64 (None where the
+    weight is absent).
     """
     ids = _i64(topk_ids)
     g = _f64(gates)
@@ -226,9 +230,11 @@ def backward(topk_ids, gates, x, dY, W1=None, W2=None, W3=None, act: str = "swig
     for k in range(K):
         gate_routed[D4[:, k]] = g[:, k]
     dX = np.zeros_like(X)
+    dg_routed = np.zeros(L * K, dtype=np.float64)     # <dY[t], Y_row> per routed row
     if act == "identity":
         np.add.at(dX, D1, gate_routed[:, None] * gy[D1])
-        return dX, None, None, None
+        dg_routed[:] = np.sum(gy[D1] * X[D1], axis=1)
+        return dX, None, None, None, dg_routed[D4]
     dW1 = np.zeros_like(w1)
     dW2 = np.zeros_like(w2) if act == "swiglu" else None
     dW3 = np.zeros_like(w3)
@@ -240,6 +246,7 @@ def backward(topk_ids, gates, x, dY, W1=None, W2=None, W3=None, act: str = "swig
         Xe = X[rows]
         out = expert_forward(Xe, w1[e], None if w2 is None else w2[e], w3[e], act)
         G = gate_routed[lo:hi, None] * gy[rows]  # expand dY to the routed rows
+        dg_routed[lo:hi] = np.sum(gy[rows] * out["Y"], axis=1)
         dW3[e] = out["H"].T @ G
         dH = G @ w3[e].T
         if act == "swiglu":
@@ -252,7 +259,7 @@ def backward(topk_ids, gates, x, dY, W1=None, W2=None, W3=None, act: str = "swig
             dXe = dA @ w1[e].T
         dW1[e] = Xe.T @ dA
         np.add.at(dX, rows, dXe)                 # reduce the routed rows
-    return dX, dW1, dW2, dW3
+    return dX, dW1, dW2, dW3, dg_routed[D4]
 
 
 # ---------------------------------------------------------------------------
@@ -282,8 +289,9 @@ def forward_rows(tokens: Sequence[int], topk_ids, gates, x_rows, W1=None, W2=Non
 
 
 def backward_rows(tokens: Sequence[int], topk_ids, gates, x_rows, dy_rows, W1=None,
-                  W2=None, W3=None, act: str = "swiglu") -> np.ndarray:
-    """dX for a subset of tokens (same formulas as ``backward``)."""
+                  W2=None, W3=None, act: str = "swiglu", with_dgates: bool = False):
+    """dX for a subset of tokens (same formulas as ``backward``); with
+    ``with_dgates`` also the (len(tokens), K) gate gradients."""
     ids = _i64(topk_ids)
     g = _f64(gates)
     Xr = _f64(x_rows)
@@ -291,10 +299,12 @@ def backward_rows(tokens: Sequence[int], topk_ids, gates, x_rows, dy_rows, W1=No
     tokens = np.asarray(tokens, dtype=np.int64)
     K = ids.shape[1]
     dX = np.zeros_like(Xr)
+    dg = np.zeros((len(tokens), K))
     for k in range(K):
         gk = g[tokens, k:k + 1]
         if act == "identity":
             dX += gk * Gy
+            dg[:, k] = np.sum(Gy * Xr, axis=1)
             continue
         ek = ids[tokens, k]
         for e in np.unique(ek):
@@ -302,6 +312,7 @@ def backward_rows(tokens: Sequence[int], topk_ids, gates, x_rows, dy_rows, W1=No
             w1 = _f64(W1[e]); w3 = _f64(W3[e])
             w2 = _f64(W2[e]) if act == "swiglu" else None
             out = expert_forward(Xr[sel], w1, w2, w3, act)
+            dg[sel, k] = np.sum(Gy[sel] * out["Y"], axis=1)
             dH = (gk[sel] * Gy[sel]) @ w3.T
             if act == "swiglu":
                 dA = dH * out["b"] * silu_grad(out["a"])
@@ -310,7 +321,7 @@ def backward_rows(tokens: Sequence[int], topk_ids, gates, x_rows, dy_rows, W1=No
             else:
                 dA = dH * silu_grad(out["a"])
                 dX[sel] += dA @ w1.T
-    return dX
+    return (dX, dg) if with_dgates else dX
 
 
 def weight_grad_slices(e: int, rows_tokens, row_gates, X_e, dY_e, W1, W2, W3,

@@ -56,8 +56,9 @@ def full_compare(cfg, inp_cpu, tol=None, check_saved=True):
     D1, D2, D3, D4 = check_dispatch(layer, inp_cpu["ids"], cfg.E)
     a = inp_cpu
     y, keep = O.forward(a["ids"], a["gates"], a["x"], a["W1"], a["W2"], a["W3"], cfg.act, E=cfg.E, keep=True)
-    dX, dW1, dW2, dW3 = O.backward(a["ids"], a["gates"], a["x"], a["dY"], a["W1"], a["W2"], a["W3"], cfg.act, E=cfg.E)
-    errs = {"y": O.rel_err(layer.y, y), "dX": O.rel_err(layer.dX, dX)}
+    dX, dW1, dW2, dW3, dg = O.backward(a["ids"], a["gates"], a["x"], a["dY"], a["W1"], a["W2"], a["W3"], cfg.act,
+                                       E=cfg.E)
+    errs = {"y": O.rel_err(layer.y, y), "dX": O.rel_err(layer.dX, dX), "dgates": O.rel_err(layer.dgates, dg)}
     if cfg.act != "identity":
         errs["dW1"] = O.rel_err(layer.dW1, dW1)
         errs["dW3"] = O.rel_err(layer.dW3, dW3)
@@ -98,8 +99,9 @@ def sampled_compare(cfg, n_tok=48, n_cols=3, seed=0, tol=None):
     xr = inp["x"][tt].cpu()
     dyr = inp["dY"][tt].cpu()
     y_ref = O.forward_rows(toks, ids, gates, xr, W["W1"], W["W2"], W["W3"], cfg.act)
-    dx_ref = O.backward_rows(toks, ids, gates, xr, dyr, W["W1"], W["W2"], W["W3"], cfg.act)
-    errs = {"y": O.rel_err(layer.y[tt], y_ref), "dX": O.rel_err(layer.dX[tt], dx_ref)}
+    dx_ref, dg_ref = O.backward_rows(toks, ids, gates, xr, dyr, W["W1"], W["W2"], W["W3"], cfg.act, with_dgates=True)
+    errs = {"y": O.rel_err(layer.y[tt], y_ref), "dX": O.rel_err(layer.dX[tt], dx_ref),
+            "dgates": O.rel_err(layer.dgates[tt], dg_ref)}
     if cfg.act != "identity":
         n_e = np.diff(D2)
         nz = np.nonzero(n_e)[0]

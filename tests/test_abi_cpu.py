@@ -99,10 +99,13 @@ def test_pointer_and_workspace_validation():
     assert B.moeblaze_forward(s, FAKE, FAKE, _disp(), FAKE, None, FAKE, FAKE, FAKE, FAKE, fw, None) == B.ERR_INVALID_ARG
     assert B.moeblaze_forward(s, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, fw - 1, None) == B.ERR_WORKSPACE
     bw = B.moeblaze_backward_workspace_bytes(s)
-    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
-                               bw, None) == B.ERR_INVALID_ARG
-    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
-                               bw - 1, None) == B.ERR_WORKSPACE
+    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
+                               FAKE, bw, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                               FAKE, bw - 1, None) == B.ERR_WORKSPACE
+    # a misaligned dgates pointer is rejected
+    assert B.moeblaze_backward(s, FAKE, FAKE, FAKE, _disp(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               MISALIGNED, FAKE, bw, None) == B.ERR_INVALID_ARG
     # SiLU takes no W2 / dW2
     s2 = B.make_shape(4096, 128, 256, 8, 2, B.BF16, "silu")
     assert B.moeblaze_saved_bytes(s2) * 2 == B.moeblaze_saved_bytes(s)

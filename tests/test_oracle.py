@@ -172,8 +172,8 @@ def test_swiglu_scalar_golden():
     W1 = f("W1").reshape(1, 1, 1); W2 = f("W2").reshape(1, 1, 1); W3 = f("W3").reshape(1, 1, 1)
     ids = np.zeros((1, 1), dtype=np.int64); g = f("g").reshape(1, 1); dY = f("dY").reshape(1, 1)
     y = O.forward(ids, g, x, W1, W2, W3, "swiglu", E=1)
-    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, "swiglu", E=1)
-    for name, v in [("y", y), ("dX", dX), ("dW1", dW1), ("dW2", dW2), ("dW3", dW3)]:
+    dX, dW1, dW2, dW3, dg = O.backward(ids, g, x, dY, W1, W2, W3, "swiglu", E=1)
+    for name, v in [("y", y), ("dX", dX), ("dW1", dW1), ("dW2", dW2), ("dW3", dW3), ("dgates", dg)]:
         assert float(v.reshape(-1)[0]) == pytest.approx(gd[name][0], rel=1e-14), name
 
 
@@ -185,10 +185,10 @@ def _loss(ids, g, x, W1, W2, W3, dY, act, E):
 
 def _fd_errors(ids, g, x, W1, W2, W3, dY, act, E, eps=1e-5, n_samples=None, seed=0):
     """max relative error of the oracle's backward vs central differences."""
-    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    dX, dW1, dW2, dW3, dg = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
     rng = np.random.default_rng(seed)
     errs = {}
-    for name, arr, grad in [("x", x, dX), ("W1", W1, dW1), ("W2", W2, dW2), ("W3", W3, dW3)]:
+    for name, arr, grad in [("x", x, dX), ("W1", W1, dW1), ("W2", W2, dW2), ("W3", W3, dW3), ("gates", g, dg)]:
         if arr is None:
             continue
         flat = arr.reshape(-1)
@@ -234,12 +234,13 @@ def test_backward_matches_autograd_dense(act):
     L, d, h, E, K = 11, 6, 5, 4, 2
     ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, act, 31)
     T = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
-    xt, w1, w3 = T(x), T(W1), T(W3)
+    xt, w1, w3, gt = T(x), T(W1), T(W3), T(g)
     w2 = T(W2) if act == "swiglu" else None
-    Gd = torch.zeros(L, E, dtype=torch.float64)
+    onehot = torch.zeros(L, K, E, dtype=torch.float64)
     for t in range(L):
         for k in range(K):
-            Gd[t, ids[t, k]] += g[t, k]
+            onehot[t, k, ids[t, k]] = 1.0
+    Gd = torch.einsum("lk,lke->le", gt, onehot)
     a = torch.einsum("ld,edh->leh", xt, w1)
     H = torch.nn.functional.silu(a)
     if act == "swiglu":
@@ -247,8 +248,9 @@ def test_backward_matches_autograd_dense(act):
     Y = torch.einsum("leh,ehd->led", H, w3)
     y = (Gd[:, :, None] * Y).sum(1)
     (y * torch.tensor(dY)).sum().backward()
-    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    dX, dW1, dW2, dW3, dg = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
     np.testing.assert_allclose(dX, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dg, gt.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dW1, w1.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dW3, w3.grad.numpy(), rtol=1e-10, atol=1e-12)
     if act == "swiglu":
@@ -264,11 +266,12 @@ def test_sampled_helpers_agree_with_full_oracle(act):
     L, d, h, E, K = 30, 8, 6, 5, 3
     ids, g, x, W1, W2, W3, dY = _rand_problem(L, d, h, E, K, act, 41)
     y = O.forward(ids, g, x, W1, W2, W3, act, E=E)
-    dX, dW1, dW2, dW3 = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
+    dX, dW1, dW2, dW3, dg = O.backward(ids, g, x, dY, W1, W2, W3, act, E=E)
     toks = [0, 3, 17, 29]
     np.testing.assert_allclose(O.forward_rows(toks, ids, g, x[toks], W1, W2, W3, act), y[toks], rtol=1e-12, atol=1e-13)
-    np.testing.assert_allclose(O.backward_rows(toks, ids, g, x[toks], dY[toks], W1, W2, W3, act), dX[toks],
-                               rtol=1e-12, atol=1e-13)
+    rdx, rdg = O.backward_rows(toks, ids, g, x[toks], dY[toks], W1, W2, W3, act, with_dgates=True)
+    np.testing.assert_allclose(rdx, dX[toks], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(rdg, dg[toks], rtol=1e-12, atol=1e-13)
     if act == "identity":
         return
     D1, D2, D3, D4 = O.dispatch(ids, E)
