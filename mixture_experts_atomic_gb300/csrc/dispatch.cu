@@ -7,12 +7,12 @@
 //                      same expert elected by match_any so no two lanes touch
 //                      one word), writes it transposed (expert-major, each
 //                      expert's 32 words = one 128-byte line) and the per
-//                      (chunk, expert) popcount.
-//   K2 scan_kernel     per expert, the exclusive scan of the chunk counts over
-//                      chunks (warp shuffles) -> chunk bases and n_e.
+//                      (expert, chunk) popcount.
+//   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
+//                      counts -> chunk bases and n_e.
 //   K3 scatter_kernel  one CTA per chunk.  Scans n_e over experts ->
-//                      expert_token_offsets; a per-expert warp scan of the
-//                      chunk's 32 popcounts gives every word its first
+//                      expert_token_offsets; a prefix walk over each
+//                      expert's 32 popcounts gives every word its first
 //                      position; each token then places its K slots:
 //                      pos = off[e] + base[c][e] + wordprefix + popc(bits below).
 //                      Writes token_index_map and token_expert_indices
@@ -35,7 +35,7 @@ namespace {
 // looked up per device with cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_scratch[MOEBLAZE_STATIC_SCRATCH_BYTES];
 
-// dispatch workspace: bitmap [E][C*32] u32 | cnt/base [C][E] i32
+// dispatch workspace: bitmap [E][C*32] u32 | cnt/base [E][C] i32
 struct DispatchWs {
   uint32_t* bitmap;
   int32_t* base;
@@ -50,91 +50,80 @@ DispatchWs carve(void* ws, const moeblaze_shape& s) {
   return w;
 }
 
-__global__ void __launch_bounds__(1024) bitmap_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
-                                                      uint32_t* __restrict__ bitmap, int32_t* __restrict__ cnt,
-                                                      int64_t words_per_expert, int32_t* err) {
+constexpr int kThreads = 256;                       // 8 warps; warp w owns words w, w+8, w+16, w+24
+constexpr int kPasses = kChunkTokens / kThreads;    // tokens per thread (4)
+constexpr int kRow = kChunkWords + 1;               // padded shared row: conflict-free column walks
+
+// K1: one CTA per chunk of 1024 tokens.  All ids are loaded up front; the
+// chunk's bitmap is built in shared memory (word [e][w] holds the tokens
+// 32w..32w+31 of the chunk routed to e), stored expert-major, and the
+// per-(expert, chunk) popcounts are written expert-major for the scan.
+__global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
+                                                          uint32_t* __restrict__ bitmap, int32_t* __restrict__ cnt,
+                                                          int64_t C, int32_t* err) {
   extern __shared__ uint32_t words[];  // [E][32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
-  for (int i = tid; i < E * kChunkWords; i += blockDim.x) words[i] = 0u;
-  __syncthreads();
+  const int64_t wpe = C * kChunkWords;
 
-  const int64_t t = chunk * kChunkTokens + tid;
-  int e_k[kMaxK];
+  int e_k[kPasses][kMaxK];
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
+  }
+  uint4* w4 = reinterpret_cast<uint4*>(words);
+  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) w4[i] = make_uint4(0u, 0u, 0u, 0u);
+
   bool bad = false;
 #pragma unroll
-  for (int k = 0; k < kMaxK; ++k) {
-    e_k[k] = -1;
-    if (k < K && t < L) {
-      int e = ids[t * K + k];
-      if (e < 0 || e >= E) { bad = true; e = -1; }
-      e_k[k] = e;
+  for (int j = 0; j < kPasses; ++j)
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      if (k >= K) continue;
+      const int e = e_k[j][k];
+      const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
+      if (t < L && (e < 0 || e >= E)) { bad = true; e_k[j][k] = -1; }
+#pragma unroll
+      for (int i = 0; i < kMaxK; ++i)
+        if (i < k && e_k[j][k] >= 0 && e_k[j][k] == e_k[j][i]) bad = true;
     }
-  }
-#pragma unroll
-  for (int k = 0; k < kMaxK; ++k)
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < k && k < K && e_k[k] >= 0 && e_k[k] == e_k[j]) bad = true;
   if (bad) atomicOr(err, kErrBadRouting);
+  __syncthreads();
 
-  // Word [e][warp] collects the lanes of this warp routed to e.  Within one
+  // Word [e][w] collects the lanes of this warp routed to e.  Within one
   // slot k the lanes sharing an expert are grouped by match_any and only the
   // group's lowest lane writes; distinct groups write distinct words.
-  for (int k = 0; k < K; ++k) {
-    const int e = e_k[k];
-    const unsigned grp = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(grp) - 1) words[e * kChunkWords + warp] |= grp;
-    __syncwarp();
-  }
-  __syncthreads();
-
-  // transposed store: expert e's 32 words of this chunk are one 128-byte line
-  for (int i = tid; i < E * kChunkWords; i += blockDim.x) {
-    const int e = i / kChunkWords, w = i % kChunkWords;
-    bitmap[(int64_t)e * words_per_expert + chunk * kChunkWords + w] = words[i];
-  }
-  // per-(chunk, expert) popcount: warp per expert, shuffle reduction
-  for (int e = warp; e < E; e += blockDim.x / 32) {
-    int v = __popc(words[e * kChunkWords + lane]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) cnt[chunk * E + e] = v;
+  for (int j = 0; j < kPasses; ++j) {
+    const int w = warp + 8 * j;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      if (k >= K) break;  // K is the same for every lane
+      const int e = e_k[j][k];
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(grp) - 1) words[e * kChunkWords + w] |= grp;
+      __syncwarp();
+    }
   }
-}
+  __syncthreads();
 
-// One CTA per 32 experts (lane = expert); the warps split the chunks, each
-// sums its range, the per-warp sums are scanned in shared memory and a second
-// pass writes the exclusive chunk bases in place of the counts.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ cnt, int64_t C, int E,
-                                                    int32_t* __restrict__ n_e) {
-  __shared__ int32_t part[32][33];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int e = blockIdx.x * 32 + lane;
-  const int64_t per = (C + nw - 1) / nw;
-  const int64_t c0 = warp * per, c1 = (c0 + per < C) ? c0 + per : C;
-  int32_t s = 0;
-  if (e < E)
-    for (int64_t c = c0; c < c1; ++c) s += cnt[c * E + e];
-  part[warp][lane] = s;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t run = 0;
-    for (int w = 0; w < nw; ++w) {
-      int32_t v = part[w][lane];
-      part[w][lane] = run;
-      run += v;
-    }
-    if (e < E) n_e[e] = run;
+  // expert-major store: expert e's 32 words of this chunk are one 128-byte line
+  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) {
+    const int e = i / (kChunkWords / 4), pc = i % (kChunkWords / 4);
+    reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] = w4[i];
   }
-  __syncthreads();
-  int32_t run = part[warp][lane];
-  if (e < E)
-    for (int64_t c = c0; c < c1; ++c) {
-      int32_t v = cnt[c * E + e];
-      cnt[c * E + e] = run;
-      run += v;
+  // per-(expert, chunk) population count, stored [E][C]
+  for (int e = tid; e < E; e += kThreads) {
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < kChunkWords / 4; ++q) {
+      const uint4 u = w4[e * (kChunkWords / 4) + q];
+      c += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
     }
+    cnt[(int64_t)e * C + chunk] = c;
+  }
 }
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -146,58 +135,131 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-__global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
-                                                       const uint32_t* __restrict__ bitmap, int64_t words_per_expert,
-                                                       const int32_t* __restrict__ base, const int32_t* __restrict__ n_e,
-                                                       int32_t* __restrict__ D1, int32_t* __restrict__ D2,
-                                                       int32_t* __restrict__ D3, int32_t* __restrict__ D4,
-                                                       MetaView meta, int64_t max_tiles) {
-  extern __shared__ int32_t sm[];
-  uint32_t* words = reinterpret_cast<uint32_t*>(sm);  // [E][32]
-  int32_t* wpre = sm + E * kChunkWords;               // [E][32]
-  int32_t* off = wpre + E * kChunkWords;              // [E+1], then the chunk bases [E]
-  __shared__ int32_t wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int64_t chunk = blockIdx.x;
-
-  // exclusive scan of n_e over experts (E <= 1024 = blockDim)
-  int v = (tid < E) ? n_e[tid] : 0;
-  int incl = warp_incl_scan(v, lane);
+// Exclusive scan of kThreads values (one per thread) across the block.
+__device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int incl = warp_incl_scan(v, lane);
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = (lane < nw) ? wsum[lane] : 0;
-    wsum[lane] = warp_incl_scan(w, lane) - w;
+    const int x = lane < kThreads / 32 ? wsum[lane] : 0;
+    const int xi = warp_incl_scan(x, lane);
+    if (lane < kThreads / 32) wsum[lane] = xi - x;
+    if (lane == kThreads / 32 - 1) *total = xi;
   }
   __syncthreads();
-  if (tid < E) off[tid] = incl - v + wsum[warp];
-  if (tid == E - 1) off[E] = incl + wsum[warp];
-  for (int i = tid; i < E * kChunkWords; i += blockDim.x) {
-    const int e = i / kChunkWords, w = i % kChunkWords;
-    words[i] = bitmap[(int64_t)e * words_per_expert + chunk * kChunkWords + w];
+  const int r = incl - v + wsum[warp];
+  __syncthreads();
+  return r;
+}
+
+// K2: one CTA per expert: exclusive scan of its chunk counts (in place) and
+// its total n_e.  Each thread sums a contiguous run of chunks.
+__global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cnt, int64_t C, int32_t* __restrict__ n_e) {
+  __shared__ int wsum[32];
+  __shared__ int total;
+  const int e = blockIdx.x;
+  int32_t* row = cnt + (int64_t)e * C;
+  const int64_t per = (C + kThreads - 1) / kThreads;
+  const int64_t c0 = threadIdx.x * per, c1 = (c0 + per < C) ? c0 + per : C;
+  int s = 0;
+  for (int64_t c = c0; c < c1; ++c) s += row[c];
+  int run = block_excl_scan(s, wsum, &total);
+  for (int64_t c = c0; c < c1; ++c) {
+    const int v = row[c];
+    row[c] = run;
+    run += v;
   }
-  // the chunk's per-expert bases, staged with the words (one coalesced read)
-  int32_t* cbase = off + E + 1;
-  if (tid < E) cbase[tid] = base[chunk * E + tid];
+  if (threadIdx.x == 0) n_e[e] = total;
+}
+
+// K3: one CTA per chunk.  Every global read (expert totals, chunk bases,
+// bitmap words, ids) is issued first; a block scan of n_e gives
+// expert_token_offsets; one thread per expert walks its 32 words to give
+// each word its first position; each token then places its K slots:
+// pos = off[e] + base[e][c] + wordprefix + popc(bits below).
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
+                                                           const uint32_t* __restrict__ bitmap, int64_t C,
+                                                           const int32_t* __restrict__ base,
+                                                           const int32_t* __restrict__ n_e, int32_t* __restrict__ D1,
+                                                           int32_t* __restrict__ D2, int32_t* __restrict__ D3,
+                                                           int32_t* __restrict__ D4, MetaView meta, int64_t max_tiles) {
+  extern __shared__ int32_t sm[];
+  uint32_t* words = reinterpret_cast<uint32_t*>(sm);  // [E][kRow]
+  int32_t* wpre = sm + E * kRow;                      // [E][kRow]
+  int32_t* off = wpre + E * kRow;                     // [E+1]
+  __shared__ int wsum[32];
+  __shared__ int total;
+  const int tid = threadIdx.x;
+  const int64_t chunk = blockIdx.x;
+  const int64_t wpe = C * kChunkWords;
+  constexpr int kEPT = kMaxE / kThreads;  // experts per thread
+
+  // ---- all global reads first
+  int nv[kEPT], cb[kEPT];
+#pragma unroll
+  for (int q = 0; q < kEPT; ++q) {
+    const int e = tid + q * kThreads;
+    nv[q] = e < E ? n_e[e] : 0;
+    cb[q] = e < E ? base[(int64_t)e * C + chunk] : 0;
+  }
+  int e_k[kPasses][kMaxK];
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
+  }
+  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) {
+    const int e = i / (kChunkWords / 4), pc = i % (kChunkWords / 4);
+    const uint4 u = reinterpret_cast<const uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc];
+    uint32_t* dst = words + e * kRow + pc * 4;
+    dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
+  }
+
+  // ---- expert offsets (exclusive scan of n_e over experts); thread tid
+  // owns experts tid and tid + 256, scanned as two ordered halves
+  int pre0 = block_excl_scan(nv[0], wsum, &total);
+  const int tot0 = total;
+  if (tid < E) off[tid] = pre0;
+  if constexpr (kEPT > 1) {
+    int pre1 = block_excl_scan(nv[1], wsum, &total);
+    if (tid + kThreads < E) off[tid + kThreads] = tot0 + pre1;
+    if (tid == 0) off[E] = tot0 + total;
+  } else {
+    if (tid == 0) off[E] = tot0;
+  }
   __syncthreads();
 
-  // first position of every (expert, word): warp per expert
-  for (int e = warp; e < E; e += nw) {
-    const int c = __popc(words[e * kChunkWords + lane]);
-    const int in = warp_incl_scan(c, lane);
-    wpre[e * kChunkWords + lane] = off[e] + cbase[e] + in - c;
+  // ---- first position of every (expert, word): one thread per expert
+#pragma unroll
+  for (int q = 0; q < kEPT; ++q) {
+    const int e = tid + q * kThreads;
+    if (e < E) {
+      int r = off[e] + cb[q];
+      for (int w = 0; w < kChunkWords; ++w) {
+        wpre[e * kRow + w] = r;
+        r += __popc(words[e * kRow + w]);
+      }
+    }
   }
   __syncthreads();
 
-  const int64_t t = chunk * kChunkTokens + tid;
-  if (t < L) {
-    const int w = tid >> 5, b = tid & 31;
+  // ---- place every (token, slot)
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int tl = tid + kThreads * j;
+    const int64_t t = chunk * kChunkTokens + tl;
+    if (t >= L) continue;
+    const int w = tl >> 5, b = tl & 31;
     const uint32_t below = (1u << b) - 1u;
-    for (int k = 0; k < K; ++k) {
-      const int e = ids[t * K + k];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      if (k >= K) continue;
+      const int e = e_k[j][k];
       int32_t pos = -1;
       if (e >= 0 && e < E) {
-        pos = wpre[e * kChunkWords + w] + __popc(words[e * kChunkWords + w] & below);
+        pos = wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
         D1[pos] = (int32_t)t;
       }
       D3[t * K + k] = e;
@@ -208,43 +270,39 @@ __global__ void __launch_bounds__(1024) scatter_kernel(const int32_t* __restrict
   if (chunk == 0) {
     // offsets, padded offsets, tile table, load order (CTA 0 only)
     __shared__ int32_t poff[kMaxE + 1];
-    for (int e = tid; e <= E; e += blockDim.x) D2[e] = off[e];
+    for (int e = tid; e <= E; e += kThreads) D2[e] = off[e];
     if (tid == 0) {
-      int32_t run = 0;
+      int32_t r = 0;
       for (int e = 0; e < E; ++e) {
-        poff[e] = run;
-        meta.pad_off[e] = run;
-        int32_t n = off[e + 1] - off[e];
-        run += (n + kRowPad - 1) / kRowPad * kRowPad;
+        poff[e] = r;
+        meta.pad_off[e] = r;
+        const int32_t n = off[e + 1] - off[e];
+        r += (n + kRowPad - 1) / kRowPad * kRowPad;
       }
-      poff[E] = run;
-      meta.pad_off[E] = run;
-      *meta.num_m_tiles = run / kTileM;
-      *meta.padded_rows = run;
+      poff[E] = r;
+      meta.pad_off[E] = r;
+      *meta.num_m_tiles = r / kTileM;
+      *meta.padded_rows = r;
     }
     __syncthreads();
     const int32_t ntiles = poff[E] / kTileM;
-    for (int64_t m = tid; m < max_tiles; m += blockDim.x) {
-      int32_t ex = -1;
-      if (m < ntiles) {  // binary search: last e with poff[e] <= m*128
-        int lo = 0, hi = E - 1;
-        const int32_t r = (int32_t)m * kTileM;
-        while (lo < hi) {
-          int mid = (lo + hi + 1) >> 1;
-          if (poff[mid] <= r) lo = mid; else hi = mid - 1;
+    // tile table: one warp per expert writes its range of 128-row tiles
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int e = warp; e < E; e += kThreads / 32)
+      for (int32_t m = poff[e] / kTileM + lane; m < poff[e + 1] / kTileM; m += 32) meta.tile_expert[m] = e;
+    for (int64_t m = ntiles + tid; m < max_tiles; m += kThreads) meta.tile_expert[m] = -1;
+#pragma unroll
+    for (int q = 0; q < kEPT; ++q) {
+      const int e = tid + q * kThreads;
+      if (e < E) {
+        const int32_t me = off[e + 1] - off[e];
+        int rank = 0;
+        for (int j = 0; j < E; ++j) {
+          const int32_t nj = off[j + 1] - off[j];
+          rank += (nj > me) || (nj == me && j < e);
         }
-        ex = lo;
+        meta.order[rank] = e;
       }
-      meta.tile_expert[m] = ex;
-    }
-    if (tid < E) {
-      const int32_t me = off[tid + 1] - off[tid];
-      int rank = 0;
-      for (int j = 0; j < E; ++j) {
-        const int32_t nj = off[j + 1] - off[j];
-        rank += (nj > me) || (nj == me && j < tid);
-      }
-      meta.order[rank] = tid;
     }
   }
 }
@@ -297,20 +355,19 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
     return MOEBLAZE_OK;
   }
   DispatchWs w = carve(ws, s);
-  const int64_t wpe = C * kChunkWords;
-  size_t sm1 = (size_t)E * kChunkWords * sizeof(uint32_t);
+  const size_t sm1 = (size_t)E * kChunkWords * sizeof(uint32_t);
   if (sm1 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
-  bitmap_kernel<<<(unsigned)C, 1024, sm1, st>>>(ids, L, E, K, w.bitmap, w.base, wpe, meta.err);
+  bitmap_kernel<<<(unsigned)C, kThreads, sm1, st>>>(ids, L, E, K, w.bitmap, w.base, C, meta.err);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(w.base, C, E, meta.n_e);
+  scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  size_t sm3 = (size_t)E * kChunkWords * 8 + (2 * E + 1) * sizeof(int32_t);
+  const size_t sm3 = (size_t)E * kRow * 8 + (E + 1) * sizeof(int32_t);
   if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<<<(unsigned)C, 1024, sm3, st>>>(ids, L, E, K, w.bitmap, wpe, w.base, meta.n_e,
-                                                  out.expert_token_indices, out.expert_token_offsets,
-                                                  out.token_expert_indices, out.token_index_map, meta, mt);
+  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, meta.n_e,
+                                                      out.expert_token_indices, out.expert_token_offsets,
+                                                      out.token_expert_indices, out.token_index_map, meta, mt);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
