@@ -176,7 +176,9 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     from mixture_experts_atomic_gb300.layer import MoELayer
     inp = I.make_inputs(cfg, dev)
-    layer = MoELayer.for_config(cfg, dev)
+    # the step is the layer's dispatch, forward and backward (dX, dW1..dW3);
+    # the optional gate gradients are not requested
+    layer = MoELayer.for_config(cfg, dev, with_dgates=False)
     flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     identity = cfg.act == "identity"
     nf, nbk = 4, 6

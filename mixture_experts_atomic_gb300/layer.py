@@ -12,7 +12,8 @@ from . import binding as B
 
 
 class MoELayer:
-    def __init__(self, L: int, d: int, h: int, E: int, K: int, dtype: torch.dtype, act: str, device="cuda"):
+    def __init__(self, L: int, d: int, h: int, E: int, K: int, dtype: torch.dtype, act: str, device="cuda",
+                 with_dgates: bool = True):
         self.shape = B.make_shape(L, d, h, E, K, dtype, act)
         self.L, self.d, self.h, self.E, self.K = L, d, h, E, K
         self.dtype, self.act, self.device = dtype, act, device
@@ -20,7 +21,8 @@ class MoELayer:
         self.bufs = B.alloc_layer(self.shape, device)
         self.y = torch.empty((L, d), dtype=dtype, device=device)
         self.dX = torch.empty((L, d), dtype=dtype, device=device)
-        self.dgates = torch.empty((L, K), dtype=torch.float32, device=device)
+        # gate gradients (for a router's backward): optional extra output
+        self.dgates = torch.empty((L, K), dtype=torch.float32, device=device) if with_dgates else None
         if act == "identity":
             self.dW1 = self.dW2 = self.dW3 = None
         else:
@@ -29,8 +31,8 @@ class MoELayer:
             self.dW3 = torch.empty((E, h, d), dtype=dtype, device=device)
 
     @classmethod
-    def for_config(cls, cfg, device="cuda"):
-        return cls(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act, device)
+    def for_config(cls, cfg, device="cuda", with_dgates: bool = True):
+        return cls(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act, device, with_dgates)
 
     def dispatch(self, ids: torch.Tensor, validate: bool = False):
         B.dispatch_build(self.shape, ids, self.disp, validate=validate)
