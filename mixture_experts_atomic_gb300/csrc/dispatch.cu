@@ -61,7 +61,7 @@ constexpr int kRow = kChunkWords + 1;               // padded shared row: confli
 __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
                                                           uint32_t* __restrict__ bitmap, int32_t* __restrict__ cnt,
                                                           int64_t C, int32_t* err) {
-  extern __shared__ uint32_t words[];  // [E][32]
+  extern __shared__ uint32_t words[];  // [E][kRow]: a padded row keeps [e][w] and [e'][w] in different banks
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
   const int64_t wpe = C * kChunkWords;
@@ -73,8 +73,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
   }
-  uint4* w4 = reinterpret_cast<uint4*>(words);
-  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) w4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < E * kRow; i += kThreads) words[i] = 0u;
 
   bool bad = false;
 #pragma unroll
@@ -103,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
       if (k >= K) break;  // K is the same for every lane
       const int e = e_k[j][k];
       const unsigned grp = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(grp) - 1) words[e * kChunkWords + w] |= grp;
+      if (e >= 0 && lane == __ffs(grp) - 1) words[e * kRow + w] |= grp;
       __syncwarp();
     }
   }
@@ -112,16 +111,15 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   // expert-major store: expert e's 32 words of this chunk are one 128-byte line
   for (int i = tid; i < E * kChunkWords / 4; i += kThreads) {
     const int e = i / (kChunkWords / 4), pc = i % (kChunkWords / 4);
-    reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] = w4[i];
+    const uint32_t* src = words + e * kRow + pc * 4;
+    reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] =
+        make_uint4(src[0], src[1], src[2], src[3]);
   }
   // per-(expert, chunk) population count, stored [E][C]
   for (int e = tid; e < E; e += kThreads) {
     int c = 0;
 #pragma unroll
-    for (int q = 0; q < kChunkWords / 4; ++q) {
-      const uint4 u = w4[e * (kChunkWords / 4) + q];
-      c += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
-    }
+    for (int w = 0; w < kChunkWords; ++w) c += __popc(words[e * kRow + w]);
     cnt[(int64_t)e * C + chunk] = c;
   }
 }
@@ -186,8 +184,9 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ D4, MetaView meta, int64_t max_tiles) {
   extern __shared__ int32_t sm[];
   uint32_t* words = reinterpret_cast<uint32_t*>(sm);  // [E][kRow]
-  int32_t* wpre = sm + E * kRow;                      // [E][kRow]
-  int32_t* off = wpre + E * kRow;                     // [E+1]
+  int32_t* off = sm + E * kRow;                       // [E+1]
+  int32_t* ebase = off + E + 1;                       // [E]: off[e] + base[e][chunk]
+  uint16_t* wpre = reinterpret_cast<uint16_t*>(ebase + E);  // [E][kRow]: set bits before word w
   __shared__ int wsum[32];
   __shared__ int total;
   const int tid = threadIdx.x;
@@ -236,9 +235,10 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
   for (int q = 0; q < kEPT; ++q) {
     const int e = tid + q * kThreads;
     if (e < E) {
-      int r = off[e] + cb[q];
+      ebase[e] = off[e] + cb[q];
+      int r = 0;
       for (int w = 0; w < kChunkWords; ++w) {
-        wpre[e * kRow + w] = r;
+        wpre[e * kRow + w] = (uint16_t)r;
         r += __popc(words[e * kRow + w]);
       }
     }
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
       const int e = e_k[j][k];
       int32_t pos = -1;
       if (e >= 0 && e < E) {
-        pos = wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
+        pos = ebase[e] + wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
         D1[pos] = (int32_t)t;
       }
       D3[t * K + k] = e;
@@ -355,7 +355,7 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
     return MOEBLAZE_OK;
   }
   DispatchWs w = carve(ws, s);
-  const size_t sm1 = (size_t)E * kChunkWords * sizeof(uint32_t);
+  const size_t sm1 = (size_t)E * kRow * sizeof(uint32_t);
   if (sm1 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
   bitmap_kernel<<<(unsigned)C, kThreads, sm1, st>>>(ids, L, E, K, w.bitmap, w.base, C, meta.err);
   MB_CUDA(cudaGetLastError());
@@ -363,7 +363,7 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  const size_t sm3 = (size_t)E * kRow * 8 + (E + 1) * sizeof(int32_t);
+  const size_t sm3 = (size_t)E * kRow * (4 + 2) + (2 * E + 1) * sizeof(int32_t);
   if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
   scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, meta.n_e,
                                                       out.expert_token_indices, out.expert_token_offsets,
