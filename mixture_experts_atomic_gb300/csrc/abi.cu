@@ -72,13 +72,13 @@ bool ok_ptr(const void* p) { return p && aligned16(p); }
 size_t elem(const moeblaze_shape* s) { return s->dtype == MOEBLAZE_BF16 ? 2 : 4; }
 int nbranch(const moeblaze_shape* s) { return s->act == MOEBLAZE_SWIGLU ? 2 : 1; }
 
-// forward scratch: H (rows x h) | y32 (L x d fp32, bf16 only)
-// backward scratch: dAB (rows x nb*h) | Hg (rows x h) | dX32 (L x d fp32, bf16 only)
+// forward scratch: H (rows x h) | y32 (L x d fp32) + tile counters (bf16 only)
+// backward scratch: dAB (rows x nb*h) | Hg (rows x h) | dX32 (L x d fp32) + tile counters (bf16 only)
 size_t fwd_ws(const moeblaze_shape* s) {
   if (s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
   size_t b = align_up((size_t)rows * s->h * elem(s), 256);
-  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256);
+  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
   return b;
 }
 size_t bwd_ws(const moeblaze_shape* s) {
@@ -86,7 +86,7 @@ size_t bwd_ws(const moeblaze_shape* s) {
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
   size_t b = align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256);
   b += align_up((size_t)rows * s->h * elem(s), 256);
-  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256);
+  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
   return b;
 }
 

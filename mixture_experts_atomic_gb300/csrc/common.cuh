@@ -19,6 +19,7 @@ constexpr int kRowPad = 256;             // expert row segments are padded to th
 constexpr int kTileM = 128;              // rows of one GEMM tile
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 8;
+constexpr size_t kSchedBytes = 256;  // tile counters behind the fp32 accumulator of a bf16 forward/backward
 
 // device error word bits
 constexpr int kErrBadRouting = 1;

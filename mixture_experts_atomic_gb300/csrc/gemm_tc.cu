@@ -58,6 +58,12 @@ constexpr int EPI_RING = 4;
 constexpr int EPI_BUF_BYTES = 32 * 64;
 constexpr int EPI_STAGE_BYTES = 4 * EPI_RING * EPI_BUF_BYTES;  // 32 KB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 256;
+// Tiles are claimed dynamically: each CTA takes its first two tiles by its
+// index and every further one from a global counter, two tiles ahead of
+// use, and passes the ids to its MMA and epilogue warps through a queue of
+// TQ slots in shared memory.
+constexpr int TQ = 8;
+constexpr bool kDynamicTiles = true;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -99,7 +105,8 @@ struct Params {
   int ld0;          // row stride (elements) of o0 for the stages that need it
   const __nv_bfloat16* gsrc;  // gathered tensor (x or dY), rows of gld elements
   int gld;
-  float* dg;                  // dH stage: gate gradients (L,K) fp32, or null
+  float* dg;                   // dH stage: gate gradients (L,K) fp32, or null
+  unsigned long long* sched;  // tile counter of this launch (zero at launch)
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -356,6 +363,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt
 
 // token of padded row q of the tile's expert (clamped to the last routed row)
 __device__ __forceinline__ int row_token(const Params& p, const Tile& t, int q) {
+  if (t.n_e == 0) return 0;  // an expert with no tokens: nothing is read for it
   int i = q - t.pad0;
   if (i >= t.n_e) i = t.n_e - 1;
   if (i < 0) i = 0;
@@ -391,6 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 17);
+  // tile-id queue: ids at bars[24 + i], full barriers bars[32 + i], empty barriers bars[40 + i]
+  volatile long long* tq = reinterpret_cast<volatile long long*>(bars + 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -406,6 +416,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     mbar_init(bar(10), 128);
     mbar_init(bar(11), 128);
     mbar_init(bar(12), 1);
+    for (int i = 0; i < TQ; ++i) {
+      mbar_init(bar(32 + i), 1);
+      // readers of a queue slot: the producer warps (thread 0 alone in the
+      // TMA-only stages), the MMA thread and the four epilogue warps
+      mbar_init(bar(40 + i), (CP ? PRODUCER_WARPS : 1) + 1 + 4);
+    }
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -423,6 +439,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
   const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
   int32_t* err = p.meta.err;
+
+  // queue position j lives in slot j % TQ, phase (j / TQ) & 1
+  auto q_post = [&](int j, long long id) -> bool {  // thread 0
+    const int sl = j % TQ;
+    if (!wait_bounded(bar(40 + sl), (uint32_t)((j / TQ) & 1) ^ 1u, abort_s, err)) return false;
+    tq[sl] = id;
+    mbar_arrive(bar(32 + sl));
+    return true;
+  };
+  auto q_take = [&](int j) -> long long {  // one thread per reader; -1 once the CTA gives up
+    const int sl = j % TQ;
+    if (!wait_bounded(bar(32 + sl), (uint32_t)(j / TQ) & 1u, abort_s, err)) return -1;
+    const long long id = tq[sl];
+    mbar_arrive(bar(40 + sl));
+    return id;
+  };
+  // tile of queue position j >= 2 (positions 0 and 1 are blockIdx.x and blockIdx.x + gridDim.x)
+  auto claim = [&](int j) -> long long {
+    if constexpr (kDynamicTiles) return 2ll * gridDim.x + (long long)atomicAdd(p.sched, 1ull);
+    else return (long long)blockIdx.x + (long long)j * gridDim.x;
+  };
 
   if (warp < PRODUCER_WARPS) {
     // ================================================================ producer
@@ -454,19 +491,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           for (int i = 0; i < 4; ++i) ww[i] = row_token(p, tt, tt.pad0 + i * 16 + r16);
         }
       };
+      // the producer warps read queue position j + 1 while they issue tile j
+      auto take = [&](int j) -> long long {
+        long long id = 0;
+        if constexpr (CP) {
+          if (lane == 0) id = q_take(j);
+          id = __shfl_sync(0xffffffffu, id, 0);
+        } else {
+          id = q_take(j);
+        }
+        return id;
+      };
+      if (pt == 0 && q_post(0, blockIdx.x)) q_post(1, (long long)blockIdx.x + gridDim.x);
+      long long tile = take(0);
       Tile t;
-      if (blockIdx.x < total) {
-        t = decode<MODE>(p, blockIdx.x, num_mt);
+      if (tile >= 0 && tile < total) {
+        t = decode<MODE>(p, tile, num_mt);
         load_tile_tokens(t, rtok, wtok);
       }
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const int64_t ntile = tile + gridDim.x;
+      ok = tile >= 0;
+      for (int j = 0; ok && tile < total; ++j) {
+        long long pending = 0;
+        if (pt == 0) pending = claim(j + 2);  // consumed after this tile's loads are issued
+        const long long ntile = take(j + 1);
+        if (ntile < 0) {
+          ok = false;
+          break;
+        }
         Tile tn;
         if (ntile < total) {
           tn = decode<MODE>(p, ntile, num_mt);
           load_tile_tokens(tn, rnext, wfirst);
         }
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
+        if constexpr (CP) {
+          // A tile without k-blocks (an expert with no tokens) issues no
+          // stage that would release the arrivals still held back, and the
+          // queue may make this warp wait on the epilogue, which needs them:
+          // deliver them now.
+          if (t.kblocks == 0 && inflight > 0) {
+            cp_async_wait<0>();
+            fence_proxy_async();
+            for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + STAGES - i) % STAGES));
+            inflight = 0;
+          }
+        }
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if constexpr (CP) {
             // every lane of the four producer warps is here: lane 0 waits, the warp follows
@@ -568,6 +637,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
+        if (!ok) break;
+        if (pt == 0) ok = q_post(j + 2, pending);
+        if constexpr (CP) {
+          if (warp == 0) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        if (!ok) break;
+        tile = ntile;
         if (ntile < total) {
           t = tn;
 #pragma unroll
@@ -596,7 +672,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       int abuf = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int j = 0; ok; ++j) {
+        const long long tile = q_take(j);
+        if (tile < 0) {
+          ok = false;
+          break;
+        }
+        if (tile >= total) break;
         const Tile t = decode<MODE>(p, tile, num_mt);
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
@@ -635,7 +717,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     StoreRing ring{smem_base + STAGES * STAGE_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
-    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int j = 0;; ++j) {
+      long long tile = 0;
+      if (lane == 0) tile = q_take(j);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0 || tile >= total) break;
       const Tile t = decode<MODE>(p, tile, num_mt);
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
@@ -906,7 +992,10 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
   const int64_t LK = s.L * s.K;
   const int64_t rows = max_padded_rows(LK, s.E);
   const int64_t mt_bound = rows / BM;
-  MB_CUDA(cudaMemsetAsync(wsY32, 0, sizeof(float) * s.L * s.d, st));
+  // y32 and, behind it, the tile counters of the two launches start at zero
+  const size_t y32_bytes = (sizeof(float) * s.L * s.d + 255) / 256 * 256;
+  unsigned long long* sched = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(wsY32) + y32_bytes);
+  MB_CUDA(cudaMemsetAsync(wsY32, 0, y32_bytes + kSchedBytes, st));
   stage_event(0, st);
   if (s.L > 0) {
     __nv_bfloat16* A = saved;
@@ -922,6 +1011,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.h + tile_n(sw ? UP_SWIGLU : UP_SILU) - 1) / tile_n(sw ? UP_SWIGLU : UP_SILU);
       p.o0 = A; p.o1 = B; p.o2 = wsH;
+      p.sched = sched + 0;
       const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
       if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
@@ -939,6 +1029,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsY32;
+      p.sched = sched + 1;
       moeblaze_status r = launch<DOWN>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
@@ -961,7 +1052,10 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
   const int64_t mt_bound = rows / BM;
   const __nv_bfloat16* A = saved;
   const __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;
-  MB_CUDA(cudaMemsetAsync(wsdX32, 0, sizeof(float) * s.L * s.d, st));
+  // dX32 and, behind it, the tile counters of the four launches start at zero
+  const size_t dx32_bytes = (sizeof(float) * s.L * s.d + 255) / 256 * 256;
+  unsigned long long* sched = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(wsdX32) + dx32_bytes);
+  MB_CUDA(cudaMemsetAsync(wsdX32, 0, dx32_bytes + kSchedBytes, st));
   stage_event(0, st);
   if (s.L > 0) {
     {  // dH = dY W3^T with the SwiGLU backward epilogue
@@ -975,6 +1069,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.n_tiles = (s.h + 255) / 256;
       p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
       p.dg = dgates;
+      p.sched = sched + 0;
       const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
@@ -993,6 +1088,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = s.h / BK;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsdX32;
+      p.sched = sched + 1;
       moeblaze_status r = launch<DX>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
@@ -1008,6 +1104,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
     p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW1; p.o1 = dW2;
+    p.sched = sched + 2;
     moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }
@@ -1022,6 +1119,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.n_tiles = (s.d + 255) / 256;
     p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW3;
+    p.sched = sched + 3;
     moeblaze_status r = launch<DW3>(p, p.total_w, st);
     if (r != MOEBLAZE_OK) return r;
   }

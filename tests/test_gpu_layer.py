@@ -46,6 +46,21 @@ def test_bf16_layer_small(L, d, h, E, K, act, one):
     full_compare(cfg, _routed_inputs(cfg, 5, one))
 
 
+def test_bf16_layer_most_experts_empty():
+    """60 of 64 experts (the last one among them) get no token: the weight
+    gradient stages then run long stretches of tiles with no k-blocks on
+    every CTA, which must still come out as zero gradients."""
+    cfg = I.MoEConfig("t_swiglu_sparse_experts", 2048, 1024, 768, 64, 2, "swiglu", "bf16", 14, "softmax")
+    inp = I.make_inputs(cfg, "cpu")
+    ids4, gates = I.random_routing(cfg.L, 4, cfg.K, 7)
+    used = torch.tensor([0, 9, 30, 41], dtype=torch.int32)
+    inp["ids"], inp["gates"] = used[ids4.long()].contiguous(), gates
+    errs, layer = full_compare(cfg, inp)
+    empty = [e for e in range(cfg.E) if e not in used.tolist()]
+    assert float(layer.dW1[empty].float().abs().max()) == 0.0
+    assert float(layer.dW3[empty].float().abs().max()) == 0.0
+
+
 def test_fp32_layer_other_shapes():
     cfg = I.MoEConfig("t_f32_silu", 333, 32, 48, 5, 3, "silu", "f32", 12, "softmax")
     full_compare(cfg, _routed_inputs(cfg, 6))
