@@ -672,14 +672,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       int abuf = 0;
       uint32_t aph = 0;
       bool ok = true;
+      long long tile = q_take(0);
+      Tile t;
+      if (tile >= 0 && tile < total) t = decode<MODE>(p, tile, num_mt);
       for (int j = 0; ok; ++j) {
-        const long long tile = q_take(j);
         if (tile < 0) {
           ok = false;
           break;
         }
         if (tile >= total) break;
-        const Tile t = decode<MODE>(p, tile, num_mt);
+        // The next tile's id and description (dependent loads of the expert
+        // tables in the weight stages) are fetched once this tile's first
+        // MMAs are issued, so their latency overlaps the tile's main loop.
+        long long ntile = -1;
+        Tile tn;
+        bool fetched = false;
+        auto fetch_next = [&]() {
+          ntile = q_take(j + 1);
+          if (ntile >= 0 && ntile < total) tn = decode<MODE>(p, ntile, num_mt);
+          fetched = true;
+        };
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
         ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err);
@@ -700,10 +712,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           mma_commit(bar(4 + s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (kb == 0) fetch_next();
         }
         if (!ok) break;
         mma_commit(bar(8 + abuf));
         if (++abuf == 2) { abuf = 0; aph ^= 1u; }
+        if (!fetched) fetch_next();
+        tile = ntile;
+        t = tn;
       }
       // all MMAs issued by this thread retire before TMEM is released
       mma_commit(bar(12));
