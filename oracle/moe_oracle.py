@@ -43,6 +43,8 @@ PINNED = {
     "backward": "central finite differences (fp64), torch.autograd of a dense formulation",
     "backward dgates": "central finite differences in the gates, autograd, hand-worked golden case",
     "forward_rows / backward_rows / weight_grad_slices": "agree with forward/backward on every row and column at small sizes",
+    "router": "hand-worked golden case (ties, bias), K = E equals the full softmax, brute force over all K-subsets, shift invariance",
+    "router_backward": "central finite differences in Wr, x and the bias, torch.autograd of the softmax over the selected logits",
 }
 
 
@@ -356,6 +358,44 @@ def weight_grad_slices(e: int, rows_tokens, row_gates, X_e, dY_e, W1, W2, W3,
     H_r = silu(a_r) * (Xe @ w2[:, wr]) if act == "swiglu" else silu(a_r)
     dW3r = H_r.T @ G
     return dW1c, dW2c, dW3r
+
+
+# ---------------------------------------------------------------------------
+# router: the step before the dispatch (token-choice top-K routing, page 1,
+# assumptions of the problem statement; the workloads' softmax router)
+# ---------------------------------------------------------------------------
+
+def router(x, Wr, bias, K: int):
+    """Token-choice top-K softmax router.
+
+    logits[t, e] = x[t] . Wr[:, e] (+ bias[e]); the K experts of token t are
+    its K largest logits, equal logits ordered by the lower expert index, slot
+    0 the largest; the gates are the softmax over those K logits (the top-K
+    probabilities renormalised to sum 1).  fp64.  Returns ids (L,K) int64,
+    gates (L,K) and the logits (L,E)."""
+    lg = _f64(x) @ _f64(Wr)
+    if bias is not None:
+        lg = lg + _f64(bias)[None, :]
+    ids = np.argsort(-lg, axis=1, kind="stable")[:, :K]
+    top = np.take_along_axis(lg, ids, axis=1)
+    w = np.exp(top - top[:, :1])
+    return ids.astype(np.int64), w / w.sum(axis=1, keepdims=True), lg
+
+
+def router_backward(x, Wr, topk_ids, gates, dgates, E: int):
+    """Gradients through the router, given dgates = dLoss/dgates.
+
+    The selection is piecewise constant in the logits, so only the K selected
+    logits of a token receive a gradient: with g the softmax over them,
+    dlogit[t, ids[t,k]] = g_k (dg_k - sum_j g_j dg_j).  Then dWr = x^T dlogit,
+    dbias = sum_t dlogit[t], dx = dlogit Wr^T.  Returns dWr (d,E), dbias (E),
+    dx (L,d) and the dense dlogit (L,E)."""
+    X = _f64(x); W = _f64(Wr); ids = _i64(topk_ids); g = _f64(gates); dg = _f64(dgates)
+    L = X.shape[0]
+    dl_k = g * (dg - np.sum(g * dg, axis=1, keepdims=True))
+    dl = np.zeros((L, E))
+    np.put_along_axis(dl, ids, dl_k, axis=1)
+    return X.T @ dl, dl.sum(axis=0), dl @ W.T, dl
 
 
 def rel_err(got, ref) -> float:

@@ -328,3 +328,136 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         m.setattr(O, "expert_forward", bad_ef)
         errs = _fd_errors(ids, g, x, W1, W2, W3, dY, "swiglu", E)
         assert max(errs.values()) > 1e-3
+
+
+# ---------------------------------------------------------------- router (the step before the dispatch)
+
+def test_router_golden_hand_worked():
+    gd = _read_golden("router_tiny.txt")
+    Wr = np.array(gd["Wr"], dtype=np.float64).reshape(2, 4)
+    for t in range(3):
+        bias = np.array(gd[f"bias{t}"], dtype=np.float64) if f"bias{t}" in gd else None
+        ids, g, _ = O.router(np.array([gd[f"x{t}"]], dtype=np.float64), Wr, bias, 2)
+        assert ids[0].tolist() == gd[f"ids{t}"]
+        np.testing.assert_allclose(g[0], gd[f"gates{t}"], rtol=0, atol=1e-15)
+
+
+def test_router_k_equals_e_is_the_full_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(60)
+    L, d, E = 40, 16, 7
+    x, Wr, b = rng.standard_normal((L, d)), rng.standard_normal((d, E)), rng.standard_normal(E)
+    ids, g, lg = O.router(x, Wr, b, E)
+    p = softmax(np.einsum("td,de->te", x, Wr) + b, axis=1)
+    for t in range(L):
+        assert sorted(ids[t].tolist()) == list(range(E))
+        assert np.all(np.diff(lg[t, ids[t]]) <= 0)
+        np.testing.assert_allclose(g[t], p[t, ids[t]], rtol=1e-12)
+
+
+def _router_bruteforce(logits, K):
+    """Every K-subset: the one with the largest sum, among those the smallest
+    sorted index tuple; slots ordered by value, then index; gates by a loop."""
+    import itertools
+    E = len(logits)
+    best = None
+    for sub in itertools.combinations(range(E), K):
+        key = (sum(logits[e] for e in sub), [-e for e in sub])
+        if best is None or key > best[0]:
+            best = (key, sub)
+    chosen = sorted(best[1], key=lambda e: (-logits[e], e))
+    w = [math.exp(logits[e] - logits[chosen[0]]) for e in chosen]
+    return chosen, [v / sum(w) for v in w]
+
+
+def test_router_matches_bruteforce_over_subsets():
+    rng = np.random.default_rng(61)
+    for K in (1, 2, 3, 6):
+        # small integer features and weights: many exact ties between logits
+        x = rng.integers(-2, 3, size=(30, 3)).astype(np.float64)
+        Wr = rng.integers(-1, 2, size=(3, 6)).astype(np.float64)
+        ids, g, lg = O.router(x, Wr, None, K)
+        for t in range(30):
+            chosen, gates = _router_bruteforce(lg[t].tolist(), K)
+            assert ids[t].tolist() == chosen
+            np.testing.assert_allclose(g[t], gates, rtol=1e-13)
+
+
+def test_router_shift_invariance():
+    rng = np.random.default_rng(62)
+    x, Wr = rng.standard_normal((25, 8)), rng.standard_normal((8, 9))
+    ids0, g0, _ = O.router(x, Wr, None, 3)
+    ids1, g1, _ = O.router(x, Wr, np.full(9, 4.5), 3)
+    assert np.array_equal(ids0, ids1)
+    np.testing.assert_allclose(g0, g1, rtol=1e-12)
+
+
+def _router_loss(x, Wr, b, ids, dg):
+    """sum_t,k dg * gates with the selection held at `ids` (fp64)."""
+    lg = x @ Wr + b
+    top = np.take_along_axis(lg, ids, axis=1)
+    w = np.exp(top - top.max(axis=1, keepdims=True))
+    return float(np.sum(dg * w / w.sum(axis=1, keepdims=True)))
+
+
+def _router_fd_errors(rb=O.router_backward):
+    rng = np.random.default_rng(63)
+    L, d, E, K = 5, 4, 6, 3
+    x, Wr, b = rng.standard_normal((L, d)), rng.standard_normal((d, E)), rng.standard_normal(E)
+    ids, g, lg = O.router(x, Wr, b, K)
+    srt = np.sort(lg, axis=1)[:, ::-1]
+    assert np.min(srt[:, K - 1] - srt[:, K]) > 1e-3  # no near-tie at the selection boundary
+    dg = rng.standard_normal((L, K))
+    dWr, db, dx, _ = rb(x, Wr, ids, g, dg, E)
+    eps, errs = 1e-6, {}
+    for name, arr, grad in (("Wr", Wr, dWr), ("x", x, dx), ("bias", b, db)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a1 = arr.copy(); a1[idx] += eps
+            a2 = arr.copy(); a2[idx] -= eps
+            args1 = {"x": x, "Wr": Wr, "bias": b}; args1[name] = a1
+            args2 = {"x": x, "Wr": Wr, "bias": b}; args2[name] = a2
+            num[idx] = (_router_loss(args1["x"], args1["Wr"], args1["bias"], ids, dg)
+                        - _router_loss(args2["x"], args2["Wr"], args2["bias"], ids, dg)) / (2 * eps)
+        errs[name] = float(np.max(np.abs(num - grad)) / max(1e-12, np.max(np.abs(num))))
+    return errs
+
+
+def test_router_backward_finite_differences():
+    errs = _router_fd_errors()
+    assert max(errs.values()) < 1e-6, errs
+
+
+def test_router_backward_matches_autograd():
+    rng = np.random.default_rng(64)
+    L, d, E, K = 50, 12, 10, 4
+    x, Wr, b = rng.standard_normal((L, d)), rng.standard_normal((d, E)), rng.standard_normal(E)
+    ids, g, _ = O.router(x, Wr, b, K)
+    dg = rng.standard_normal((L, K))
+    dWr, db, dx, _ = O.router_backward(x, Wr, ids, g, dg, E)
+    tx, tW, tb = (torch.tensor(v, dtype=torch.float64, requires_grad=True) for v in (x, Wr, b))
+    sel = torch.gather(tx @ tW + tb, 1, torch.from_numpy(ids))
+    (torch.softmax(sel, dim=1) * torch.from_numpy(dg)).sum().backward()
+    np.testing.assert_allclose(dWr, tW.grad.numpy(), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(db, tb.grad.numpy(), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(dx, tx.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_router_pins_catch_planted_mistakes():
+    # 1) the centring term of the softmax gradient dropped -> finite differences disagree
+    def bad_rb(x, Wr, topk_ids, gates, dgates, E):
+        X = O._f64(x); ids = O._i64(topk_ids); g = O._f64(gates); dg = O._f64(dgates)
+        dl = np.zeros((X.shape[0], E))
+        np.put_along_axis(dl, ids, g * dg, axis=1)
+        return X.T @ dl, dl.sum(axis=0), dl @ O._f64(Wr).T, dl
+    assert max(_router_fd_errors(bad_rb).values()) > 1e-2
+    # 2) ties broken towards the higher index -> the hand-worked golden case disagrees
+    gd = _read_golden("router_tiny.txt")
+    lg = np.array(gd["x0"], dtype=np.float64) @ np.array(gd["Wr"], dtype=np.float64).reshape(2, 4)
+    wrong = sorted(range(4), key=lambda e: (-lg[e], -e))[:2]  # equal logits to the higher index
+    assert wrong != gd["ids0"]
+    # 3) gates over all E experts instead of the K selected -> the K = E softmax pin's
+    #    renormalisation check fails for K < E
+    ids, g, lg = O.router(np.array([gd["x0"]], dtype=np.float64), np.array(gd["Wr"], dtype=np.float64).reshape(2, 4), None, 2)
+    full = np.exp(lg[0] - lg[0].max()); full /= full.sum()
+    assert abs(full[ids[0]].sum() - 1.0) > 1e-3 and abs(g[0].sum() - 1.0) < 1e-15
