@@ -205,6 +205,52 @@ MOEBLAZE_API moeblaze_status moeblaze_backward(const moeblaze_shape* s, const vo
                                   const void* saved, void* dX, void* dW1, void* dW2, void* dW3,
                                   float* dgates, void* ws, size_t ws_bytes, moeblaze_stream stream);
 
+/* ------------------------------------------------------------------ router
+ * The token-choice top-K softmax router, the step before the dispatch
+ * (MoEBlaze, awesome-system-papers page, assumptions of the problem
+ * statement: token-choice, top-K routing), and its backward, which takes the
+ * gate gradients of moeblaze_backward.  Shape fields used: L, d, E, K, dtype
+ * (h and act are ignored).  Supported: E <= 256, K <= min(E, 8), d a
+ * multiple of 64; otherwise MOEBLAZE_ERR_UNSUPPORTED.  fp32 arithmetic.
+ *
+ * moeblaze_router_forward:
+ *   x       device (L,d) dtype, 16-byte aligned
+ *   Wr      device (d,E) fp32 row-major (column e is expert e's weights)
+ *   bias    device (E) fp32 or NULL
+ *   topk_ids device (L,K) int32, overwritten: the K largest logits
+ *           x[t].Wr[:,e] + bias[e], equal logits ordered by the lower expert
+ *           index, slot 0 the largest
+ *   gates   device (L,K) fp32, overwritten: the softmax over the K selected
+ *           logits (they sum to 1 per token)
+ * No scratch.  Ready to feed moeblaze_dispatch_build and moeblaze_forward. */
+MOEBLAZE_API moeblaze_status moeblaze_router_forward(const moeblaze_shape* s, const void* x, const float* Wr,
+                                                     const float* bias, int32_t* topk_ids, float* gates,
+                                                     moeblaze_stream stream);
+
+/* Bytes of scratch moeblaze_router_backward needs for shape s (0 when s is
+ * not supported). */
+MOEBLAZE_API size_t moeblaze_router_backward_workspace_bytes(const moeblaze_shape* s);
+
+/* moeblaze_router_backward: gradients through the router given
+ * dgates = dLoss/dgates.  The selection is piecewise constant, so only the
+ * selected logits get a gradient: dlogit[t, ids[t,k]] = g_k (dg_k - sum_j
+ * g_j dg_j).  Then dWr = x^T dlogit, dbias = sum_t dlogit[t] and
+ * dx = dlogit Wr^T (the router's share of the input gradient; the caller
+ * adds it to the layer's dX).
+ *   x, Wr   as moeblaze_router_forward
+ *   topk_ids, gates  device (L,K): the router forward's outputs
+ *   dgates  device (L,K) fp32 (moeblaze_backward's dgates)
+ *   dWr     device (d,E) fp32, overwritten
+ *   dbias   device (E) fp32, overwritten, or NULL
+ *   dx      device (L,d) dtype, overwritten, 16-byte aligned, or NULL
+ *   ws      device moeblaze_router_backward_workspace_bytes(s) bytes
+ * dWr and dbias are summed over the tokens in a fixed order (repeatable to
+ * the bit).  Ids must be pairwise distinct per token and < E. */
+MOEBLAZE_API moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, const void* x, const float* Wr,
+                                                      const int32_t* topk_ids, const float* gates,
+                                                      const float* dgates, float* dWr, float* dbias, void* dx,
+                                                      void* ws, size_t ws_bytes, moeblaze_stream stream);
+
 /* Synchronise `stream` and read the device error word of `disp->meta`:
  * *code = 0 when every kernel since the last dispatch_build on this meta
  * finished normally; otherwise a bitwise OR of 1 (bad routing) and 2 (a

@@ -30,6 +30,7 @@ EXPORTS = [
     "moeblaze_forward", "moeblaze_backward", "moeblaze_device_error", "moeblaze_status_string",
     "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
     "moeblaze_dispatch_build_static",
+    "moeblaze_router_forward", "moeblaze_router_backward", "moeblaze_router_backward_workspace_bytes",
 ]
 
 # fixed scratch of moeblaze_dispatch_build_static (MOEBLAZE_STATIC_SCRATCH_BYTES)
@@ -77,6 +78,12 @@ def lib():
         L.moeblaze_forward.restype = ctypes.c_int
         L.moeblaze_backward.argtypes = [SP, P, P, P, DP, P, P, P, P, P, P, P, P, P, P, sz, P]
         L.moeblaze_backward.restype = ctypes.c_int
+        L.moeblaze_router_forward.argtypes = [SP, P, P, P, P, P, P]
+        L.moeblaze_router_forward.restype = ctypes.c_int
+        L.moeblaze_router_backward_workspace_bytes.argtypes = [SP]
+        L.moeblaze_router_backward_workspace_bytes.restype = sz
+        L.moeblaze_router_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, sz, P]
+        L.moeblaze_router_backward.restype = ctypes.c_int
         L.moeblaze_device_error.argtypes = [SP, DP, ctypes.POINTER(ctypes.c_int32), P]
         L.moeblaze_device_error.restype = ctypes.c_int
         L.moeblaze_status_string.argtypes = [ctypes.c_int]
@@ -136,6 +143,19 @@ def moeblaze_backward(shape, dY, x, gates, disp, W1, W2, W3, saved, dX, dW1, dW2
                       stream) -> int:
     return lib().moeblaze_backward(ctypes.byref(shape), dY, x, gates, ctypes.byref(disp), W1, W2, W3, saved, dX,
                                    dW1, dW2, dW3, dgates, ws, ws_bytes, stream)
+
+
+def moeblaze_router_forward(shape, x, Wr, bias, topk_ids, gates, stream) -> int:
+    return lib().moeblaze_router_forward(ctypes.byref(shape), x, Wr, bias, topk_ids, gates, stream)
+
+
+def moeblaze_router_backward_workspace_bytes(shape: Shape) -> int:
+    return lib().moeblaze_router_backward_workspace_bytes(ctypes.byref(shape))
+
+
+def moeblaze_router_backward(shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws, ws_bytes, stream) -> int:
+    return lib().moeblaze_router_backward(ctypes.byref(shape), x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws,
+                                          ws_bytes, stream)
 
 
 def moeblaze_device_error(shape, disp, stream):
@@ -276,6 +296,24 @@ class StageEvents:
 
     def elapsed_ms(self):
         return [self.events[i].elapsed_time(self.events[i + 1]) for i in range(len(self.events) - 1)]
+
+
+def router_forward(shape: Shape, x, Wr, bias, topk_ids, gates, stream=None):
+    """Token-choice top-K softmax router: fills topk_ids (L,K) int32 and gates (L,K) fp32."""
+    st = moeblaze_router_forward(shape, _ptr(x), _ptr(Wr), _ptr(bias), _ptr(topk_ids), _ptr(gates), _stream(stream))
+    _check(st, "moeblaze_router_forward")
+
+
+def router_backward(shape: Shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws=None, stream=None):
+    """Router gradients from the gate gradients: fills dWr (d,E) fp32, dbias (E) fp32 and dx (L,d) (dbias and dx
+    may be None).  `ws` is a device byte tensor of moeblaze_router_backward_workspace_bytes(shape) bytes
+    (allocated here when None)."""
+    n = moeblaze_router_backward_workspace_bytes(shape)
+    if ws is None:
+        ws = _bytes(n, Wr.device)
+    st = moeblaze_router_backward(shape, _ptr(x), _ptr(Wr), _ptr(topk_ids), _ptr(gates), _ptr(dgates), _ptr(dWr),
+                                  _ptr(dbias), _ptr(dx), _ptr(ws), n, _stream(stream))
+    _check(st, "moeblaze_router_backward")
 
 
 def device_error(shape: Shape, disp: DispatchBuffers, stream=None) -> int:

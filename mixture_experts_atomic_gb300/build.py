@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoeblaze.so")
-SOURCES = ["abi.cu", "dispatch.cu", "identity.cu", "simt.cu", "gemm_tc.cu"]
+SOURCES = ["abi.cu", "dispatch.cu", "identity.cu", "simt.cu", "gemm_tc.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -68,6 +68,17 @@ moeblaze_status check_dispatch(const moeblaze_dispatch* d) {
 }
 
 bool ok_ptr(const void* p) { return p && aligned16(p); }
+bool ok_ptr4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// shape checks of the router entry points (h and act are not used)
+moeblaze_status check_router_shape(const moeblaze_shape* s) {
+  if (!s) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L < 0 || s->E < 1 || s->K < 1 || s->d < 1 || s->K > s->E) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->dtype != MOEBLAZE_F32 && s->dtype != MOEBLAZE_BF16) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->E > kMaxRouterE || s->K > kMaxK || s->d % 64 != 0) return MOEBLAZE_ERR_UNSUPPORTED;
+  if (s->L * (int64_t)s->K >= (int64_t(1) << 31)) return MOEBLAZE_ERR_UNSUPPORTED;
+  return MOEBLAZE_OK;
+}
 
 size_t elem(const moeblaze_shape* s) { return s->dtype == MOEBLAZE_BF16 ? 2 : 4; }
 int nbranch(const moeblaze_shape* s) { return s->act == MOEBLAZE_SWIGLU ? 2 : 1; }
@@ -269,6 +280,35 @@ moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_di
   if (c & kErrBadRouting) return MOEBLAZE_ERR_BAD_ROUTING;
   if (c & kErrTimeout) return MOEBLAZE_ERR_TIMEOUT;
   return MOEBLAZE_OK;
+}
+
+size_t moeblaze_router_backward_workspace_bytes(const moeblaze_shape* s) {
+  if (check_router_shape(s) != MOEBLAZE_OK) return 0;
+  return router_ws_bytes(*s);
+}
+
+moeblaze_status moeblaze_router_forward(const moeblaze_shape* s, const void* x, const float* Wr, const float* bias,
+                                        int32_t* topk_ids, float* gates, moeblaze_stream stream) {
+  moeblaze_status r = check_router_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if (!ok_ptr4(Wr) || (bias && !ok_ptr4(bias))) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L > 0 && (!ok_ptr(x) || !ok_ptr4(topk_ids) || !ok_ptr4(gates))) return MOEBLAZE_ERR_INVALID_ARG;
+  return launch_router_forward(*s, x, Wr, bias, topk_ids, gates, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, const void* x, const float* Wr,
+                                         const int32_t* topk_ids, const float* gates, const float* dgates,
+                                         float* dWr, float* dbias, void* dx, void* ws, size_t ws_bytes,
+                                         moeblaze_stream stream) {
+  moeblaze_status r = check_router_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if (!ok_ptr4(Wr) || !ok_ptr4(dWr) || (dbias && !ok_ptr4(dbias))) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L > 0 && (!ok_ptr(x) || !ok_ptr4(topk_ids) || !ok_ptr4(gates) || !ok_ptr4(dgates) || (dx && !ok_ptr(dx))))
+    return MOEBLAZE_ERR_INVALID_ARG;
+  if (ws_bytes < router_ws_bytes(*s)) return MOEBLAZE_ERR_WORKSPACE;
+  if (s->L > 0 && !ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
+  return launch_router_backward(*s, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -110,6 +110,15 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
                             float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
 
+// router.cu
+constexpr int kMaxRouterE = 256;
+size_t router_ws_bytes(const moeblaze_shape& s);
+moeblaze_status launch_router_forward(const moeblaze_shape& s, const void* x, const float* Wr, const float* bias,
+                                      int32_t* ids, float* gates, cudaStream_t st);
+moeblaze_status launch_router_backward(const moeblaze_shape& s, const void* x, const float* Wr, const int32_t* ids,
+                                       const float* gates, const float* dgates, float* dWr, float* dbias, void* dx,
+                                       void* ws, cudaStream_t st);
+
 // shared helpers (abi.cu)
 int sm_count();
 void count_launch(int n = 1);

@@ -250,6 +250,18 @@ def softmax_router(cfg: MoEConfig, x: torch.Tensor, chunk: int = 1 << 15):
     return ids, gates
 
 
+def router_weights(cfg: MoEConfig, device="cpu"):
+    """The router parameters of a softmax workload, as handed to a router
+    kernel: Wr (d,E) fp32 ~ N(0, 1/d) (the values softmax_router uses) and,
+    for the biased router, the bias (E) ~ N(0, 1.5) (variance) rounded to
+    fp32; bias None otherwise."""
+    Wr = normal_block(cfg.seed, STREAM_WR, 0, (cfg.d, cfg.E), device, 1.0 / math.sqrt(cfg.d), torch.float32)
+    bias = None
+    if cfg.router == "softmax_bias":
+        bias = normal_block(cfg.seed, STREAM_BIAS, 0, (cfg.E,), device, math.sqrt(ROUTER_BIAS_VAR), torch.float32)
+    return Wr, bias
+
+
 def zipf_router(cfg: MoEConfig, device="cpu", chunk: int = 1 << 16):
     """K distinct ids per token drawn one after another without replacement
     from p_e ~ (e+1)^-s (renormalised over the experts not yet drawn; slot

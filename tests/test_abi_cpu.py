@@ -128,3 +128,24 @@ def test_product_path_does_not_import_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, fn
+
+
+def test_router_validation_codes():
+    _lib()
+    ok = B.make_shape(4096, 1024, 0, 8, 2, B.BF16, "silu")
+    ws = B.moeblaze_router_backward_workspace_bytes(ok)
+    assert ws > 0
+    # more than 256 experts, d not a multiple of 64: unsupported
+    for bad in (B.make_shape(4096, 1024, 0, 300, 2, B.BF16, "silu"), B.make_shape(4096, 96, 0, 8, 2, B.BF16, "silu")):
+        assert B.moeblaze_router_forward(bad, FAKE, FAKE, None, FAKE, FAKE, None) == B.ERR_UNSUPPORTED
+        assert B.moeblaze_router_backward_workspace_bytes(bad) == 0
+    # K > E, missing Wr, misaligned x, missing outputs: invalid
+    assert B.moeblaze_router_forward(B.make_shape(16, 64, 0, 2, 3, B.F32, "silu"), FAKE, FAKE, None, FAKE, FAKE,
+                                     None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_router_forward(ok, FAKE, None, None, FAKE, FAKE, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_router_forward(ok, MISALIGNED, FAKE, None, FAKE, FAKE, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_router_forward(ok, FAKE, FAKE, None, None, FAKE, None) == B.ERR_INVALID_ARG
+    assert B.moeblaze_router_backward(ok, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, ws, None) \
+        == B.ERR_INVALID_ARG
+    assert B.moeblaze_router_backward(ok, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, ws - 1, None) \
+        == B.ERR_WORKSPACE
