@@ -11,11 +11,13 @@
 //   dlogit[t, ids[t,k]] = g_k (dg_k - sum_j g_j dg_j)    (0 for the others)
 //   dx = dlogit Wr^T,  dWr = x^T dlogit,  dbias = sum_t dlogit[t]
 //
-// Both directions are small GEMMs with N = E (at most 256) on CUDA cores in
-// fp32: a CTA owns a 64-row tile and the fp32 products are register-blocked
-// over the experts.  The weight-gradient sums are split over token ranges
-// into per-split partials that a last kernel adds in a fixed order, so every
-// result is bitwise repeatable.
+// All three are small GEMMs with N = E (at most 256) on CUDA cores in fp32.
+// A CTA owns a 64-row tile (tokens, or rows of Wr), its products are
+// register-blocked over the experts, and the streamed operand (x, Wr) comes
+// through a multi-stage cp.async pipeline of 64-wide chunks so that several
+// chunks of every CTA are in flight.  The weight-gradient sums are split
+// over token ranges into per-split partials that a last kernel adds in a
+// fixed order, so every result is bitwise repeatable.
 #include <cfloat>
 #include <climits>
 
@@ -25,7 +27,7 @@ namespace moeblaze {
 namespace {
 
 constexpr int kRT = 64;        // rows of a CTA tile (tokens, or rows of Wr)
-constexpr int kRK = 32;        // reduction chunk staged in shared memory
+constexpr int kRC = 64;        // width of a streamed chunk
 constexpr int kRThreads = 256;
 
 // thread layout of a 64 x EP tile: TE threads across the experts (expert
@@ -36,7 +38,18 @@ struct RLayout {
   static constexpr int EPT = EP / TE;
   static constexpr int TTH = kRThreads / TE;
   static constexpr int RPT = kRT / TTH;
+  static constexpr int STAGES = EP >= 128 ? 2 : 3;
 };
+
+// row pitch (elements) of a staged 64-wide chunk of x: 16-byte multiple, and
+// rows 2 or 4 apart land on different banks
+template <typename T>
+struct XPitch {
+  static constexpr int value = sizeof(T) == 2 ? 72 : 68;
+};
+
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(float v) { return v; }
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -57,22 +70,51 @@ __device__ __forceinline__ void store8(float* p, const float* v) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// acc[i][j] += sum_c A[row_i][c] * B[c][expert_j] over one staged chunk
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, bool valid) {
+  // a 16-byte copy, zero-filled when !valid (the source is not read)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// 64 rows x 64 columns of a row-major (rows, ld) matrix, rows >= nrows zero
+template <typename T>
+__device__ __forceinline__ void stage_rows(T* dst, const T* src, int64_t row0, int64_t nrows, int64_t ld, int64_t col0,
+                                           int tid) {
+  constexpr int P = XPitch<T>::value;
+  constexpr int V = 16 / sizeof(T);             // elements per 16-byte copy
+  constexpr int PER_ROW = kRC / V;              // copies per row
+  for (int i = tid; i < kRT * PER_ROW; i += kRThreads) {
+    const int r = i / PER_ROW, c = (i % PER_ROW) * V;
+    const bool ok = row0 + r < nrows;
+    cp16(saddr(dst + r * P + c), ok ? (const void*)(src + (row0 + r) * ld + col0 + c) : (const void*)src, ok);
+  }
+}
+
+// rows k0..k0+63 of Wr (d,E) as 64 x EP fp32, experts >= E zero (16-byte
+// copies when every row of Wr starts on a 16-byte boundary, else 4-byte)
 template <int EP>
-__device__ __forceinline__ void tile_fma(const float (*As)[kRK + 1], const float (*Bs)[EP], int te, int tr,
-                                         float (&acc)[RLayout<EP>::RPT][RLayout<EP>::EPT]) {
-  using Ly = RLayout<EP>;
-#pragma unroll 4
-  for (int c = 0; c < kRK; ++c) {
-    float av[Ly::RPT], bv[Ly::EPT];
-#pragma unroll
-    for (int i = 0; i < Ly::RPT; ++i) av[i] = As[tr * Ly::RPT + i][c];
-#pragma unroll
-    for (int j = 0; j < Ly::EPT; ++j) bv[j] = Bs[c][j * Ly::TE + te];
-#pragma unroll
-    for (int i = 0; i < Ly::RPT; ++i)
-#pragma unroll
-      for (int j = 0; j < Ly::EPT; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+__device__ __forceinline__ void stage_wr(float* dst, const float* Wr, int k0, int E, int tid) {
+  if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0) {
+    constexpr int PER_ROW = EP / 4;
+    for (int i = tid; i < kRC * PER_ROW; i += kRThreads) {
+      const int r = i / PER_ROW, c = (i % PER_ROW) * 4;
+      const bool ok = c < E;
+      cp16(saddr(dst + r * EP + c), ok ? (const void*)(Wr + (int64_t)(k0 + r) * E + c) : (const void*)Wr, ok);
+    }
+  } else {
+    for (int i = tid; i < kRC * EP; i += kRThreads) {
+      const int r = i / EP, c = i % EP;
+      const bool ok = c < E;
+      cp4(saddr(dst + r * EP + c), ok ? (const void*)(Wr + (int64_t)(k0 + r) * E + c) : (const void*)Wr, ok);
+    }
   }
 }
 
@@ -83,30 +125,55 @@ __global__ void __launch_bounds__(kRThreads) router_fwd_kernel(const T* __restri
                                                                int K, int32_t* __restrict__ ids,
                                                                float* __restrict__ gates) {
   using Ly = RLayout<EP>;
-  __shared__ float xs[kRT][kRK + 1];
-  __shared__ __align__(16) float ws[kRK][EP];
+  constexpr int S = Ly::STAGES, P = XPitch<T>::value;
+  constexpr int XS = kRT * P;  // elements of one x stage
+  extern __shared__ __align__(16) uint8_t rsm[];
+  T* xs = reinterpret_cast<T*>(rsm);
+  float* ws = reinterpret_cast<float*>(rsm + S * XS * sizeof(T));
   const int tid = threadIdx.x, te = tid % Ly::TE, tr = tid / Ly::TE;
   const int64_t t0 = (int64_t)blockIdx.x * kRT;
+  const int nch = d / kRC;
   float acc[Ly::RPT][Ly::EPT];
 #pragma unroll
   for (int i = 0; i < Ly::RPT; ++i)
 #pragma unroll
     for (int j = 0; j < Ly::EPT; ++j) acc[i][j] = 0.f;
 
-  const int lr = tid >> 2, lc = (tid & 3) * 8;  // this thread's 8 elements of the 64 x 32 x tile
-  for (int k0 = 0; k0 < d; k0 += kRK) {
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (t0 + lr < L) load8(x + (t0 + lr) * d + k0 + lc, v);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) xs[lr][lc + u] = v[u];
-    for (int i = tid; i < kRK * EP; i += kRThreads) {
-      const int r = i / EP, c = i % EP;
-      ws[r][c] = c < E ? Wr[(int64_t)(k0 + r) * E + c] : 0.f;
+  for (int c = 0; c < S - 1; ++c) {
+    if (c < nch) {
+      stage_rows<T>(xs + c * XS, x, t0, L, d, (int64_t)c * kRC, tid);
+      stage_wr<EP>(ws + c * kRC * EP, Wr, c * kRC, E, tid);
     }
-    __syncthreads();
-    tile_fma<EP>(xs, ws, te, tr, acc);
-    __syncthreads();
+    cp_commit();
   }
+  for (int c = 0; c < nch; ++c) {
+    cp_wait<S - 2>();
+    __syncthreads();
+    {  // the chunk S-1 ahead goes into the stage that chunk c-1 used
+      const int n = c + S - 1;
+      if (n < nch) {
+        stage_rows<T>(xs + (n % S) * XS, x, t0, L, d, (int64_t)n * kRC, tid);
+        stage_wr<EP>(ws + (n % S) * kRC * EP, Wr, n * kRC, E, tid);
+      }
+      cp_commit();
+    }
+    const T* xa = xs + (c % S) * XS;
+    const float* wb = ws + (c % S) * kRC * EP;
+#pragma unroll 4
+    for (int k = 0; k < kRC; ++k) {
+      float av[Ly::RPT], bv[Ly::EPT];
+#pragma unroll
+      for (int i = 0; i < Ly::RPT; ++i) av[i] = to_f32(xa[(tr * Ly::RPT + i) * P + k]);
+#pragma unroll
+      for (int j = 0; j < Ly::EPT; ++j) bv[j] = wb[k * EP + j * Ly::TE + te];
+#pragma unroll
+      for (int i = 0; i < Ly::RPT; ++i)
+#pragma unroll
+        for (int j = 0; j < Ly::EPT; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+  }
+  cp_wait<0>();
 
   // bias; the padding experts (e >= E) can never be chosen
 #pragma unroll
@@ -174,20 +241,143 @@ __global__ void __launch_bounds__(kRThreads) router_fwd_kernel(const T* __restri
   }
 }
 
+// Forward for few experts (EP <= 16) when Wr fits in shared memory: a
+// GEMV over the token rows.  Wr (d, EP) is staged once per CTA; each warp
+// takes 4 tokens at a time, its lanes read 16-byte pieces of the 4 rows
+// (columns lane*8 + 256*i) and accumulate 4 x EP partial logits, which a
+// butterfly reduction completes; lane k of the warp then ranks token k's
+// logits (larger first, equal to the lower index) and writes its ids and
+// gates.  The x rows stream from HBM once, coalesced.
+template <typename T, int EP>
+__global__ void __launch_bounds__(512) router_fwd_gemv_kernel(const T* __restrict__ x, const float* __restrict__ Wr,
+                                                              const float* __restrict__ bias, int64_t L, int d, int E,
+                                                              int K, int32_t* __restrict__ ids,
+                                                              float* __restrict__ gates) {
+  constexpr int TPW = 4;  // tokens per warp pass
+  extern __shared__ __align__(16) uint8_t rsm[];
+  // Wr as [d][EP] with 4 floats of padding after every 8 rows: the lanes of
+  // a warp read rows 8 apart, which then fall on different banks
+  float* ws = reinterpret_cast<float*>(rsm);
+  for (int i = threadIdx.x; i < d * EP; i += blockDim.x) {
+    const int r = i / EP, c = i % EP;
+    const bool ok = c < E;
+    cp4(saddr(ws + r * EP + (r >> 3) * 4 + c), ok ? (const void*)(Wr + (int64_t)r * E + c) : (const void*)Wr, ok);
+  }
+  cp_commit();
+  cp_wait<0>();
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t0 = warp * TPW; t0 < L; t0 += nwarps * TPW) {
+    float acc[TPW][EP];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[q][e] = 0.f;
+#pragma unroll 2
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      float xv[TPW][8];
+#pragma unroll
+      for (int q = 0; q < TPW; ++q) {
+        if (t0 + q < L) {
+          load8(x + (t0 + q) * d + c0, xv[q]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) xv[q][u] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4* wr = reinterpret_cast<const float4*>(ws + (c0 + u) * EP + (c0 >> 3) * 4);
+#pragma unroll
+        for (int e4 = 0; e4 < EP / 4; ++e4) {
+          const float4 w = wr[e4];
+#pragma unroll
+          for (int q = 0; q < TPW; ++q) {
+            acc[q][4 * e4 + 0] = fmaf(xv[q][u], w.x, acc[q][4 * e4 + 0]);
+            acc[q][4 * e4 + 1] = fmaf(xv[q][u], w.y, acc[q][4 * e4 + 1]);
+            acc[q][4 * e4 + 2] = fmaf(xv[q][u], w.z, acc[q][4 * e4 + 2]);
+            acc[q][4 * e4 + 3] = fmaf(xv[q][u], w.w, acc[q][4 * e4 + 3]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], off);
+    // lane q ranks token t0 + q
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) {
+      const int64_t t = t0 + q;
+      if (lane != q || t >= L) continue;
+      float lg[EP];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) lg[e] = e < E ? acc[q][e] + (bias ? bias[e] : 0.f) : -FLT_MAX;
+      uint32_t taken = 0;
+      float selv[kMaxK], w[kMaxK], sum = 0.f;
+      int seli[kMaxK];
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        selv[k] = 0.f;
+        seli[k] = 0;
+        if (k < K) {
+          float bv = -FLT_MAX;
+          int bi = INT_MAX;
+#pragma unroll
+          for (int e = 0; e < EP; ++e)
+            if (!((taken >> e) & 1u) && e < E && (lg[e] > bv || (lg[e] == bv && e < bi))) {
+              bv = lg[e];
+              bi = e;
+            }
+          selv[k] = bv;
+          seli[k] = bi;
+          taken |= 1u << bi;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        w[k] = k < K ? expf(selv[k] - selv[0]) : 0.f;
+        sum += w[k];
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        if (k < K) {
+          ids[t * K + k] = seli[k];
+          gates[t * K + k] = w[k] / sum;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ backward
 // dlogit of the selected experts (kept in the workspace for dWr) and
-// dx = dlogit Wr^T for one 64-token tile
+// dx = dlogit Wr^T for one 64-token tile, Wr streamed in 64-row chunks
 template <typename T, int EP>
 __global__ void __launch_bounds__(kRThreads) router_dx_kernel(const float* __restrict__ Wr,
                                                               const int32_t* __restrict__ ids,
                                                               const float* __restrict__ gates,
                                                               const float* __restrict__ dgates, int64_t L, int d, int E,
                                                               int K, float* __restrict__ dl, T* __restrict__ dx) {
+  constexpr int S = 3;
   __shared__ float dls[kRT][kMaxK];
   __shared__ int ids_s[kRT][kMaxK];
-  __shared__ float ws[kRK][EP + 1];
+  extern __shared__ __align__(16) uint8_t rsm[];
+  float* ws = reinterpret_cast<float*>(rsm);  // S stages of 64 x EP
   const int tid = threadIdx.x;
   const int64_t t0 = (int64_t)blockIdx.x * kRT;
+  const int nch = d / kRC;
+  if (dx) {
+#pragma unroll
+    for (int c = 0; c < S - 1; ++c) {
+      if (c < nch) stage_wr<EP>(ws + c * kRC * EP, Wr, c * kRC, E, tid);
+      cp_commit();
+    }
+  }
   if (tid < kRT) {
     const int64_t t = t0 + tid;
     float g[kMaxK], dg[kMaxK], s = 0.f;
@@ -195,7 +385,8 @@ __global__ void __launch_bounds__(kRThreads) router_dx_kernel(const float* __res
     for (int k = 0; k < kMaxK; ++k) {
       g[k] = (k < K && t < L) ? gates[t * K + k] : 0.f;
       dg[k] = (k < K && t < L) ? dgates[t * K + k] : 0.f;
-      ids_s[tid][k] = (k < K && t < L) ? ids[t * K + k] : 0;
+      const int e = (k < K && t < L) ? ids[t * K + k] : 0;
+      ids_s[tid][k] = ((unsigned)e < (unsigned)E) ? e : 0;
       s = fmaf(g[k], dg[k], s);
     }
 #pragma unroll
@@ -205,71 +396,114 @@ __global__ void __launch_bounds__(kRThreads) router_dx_kernel(const float* __res
       if (k < K && t < L) dl[t * K + k] = v;
     }
   }
-  __syncthreads();
   if (!dx) return;
-  const int row = tid >> 2, c8 = (tid & 3) * 8;
-  for (int k0 = 0; k0 < d; k0 += kRK) {
-    for (int i = tid; i < kRK * EP; i += kRThreads) {
-      const int r = i / EP, c = i % EP;
-      ws[r][c] = c < E ? Wr[(int64_t)(k0 + r) * E + c] : 0.f;
-    }
+  const int row = tid >> 2, c16 = (tid & 3) * 16;  // 16 outputs of one token per thread
+  for (int c = 0; c < nch; ++c) {
+    cp_wait<S - 2>();
     __syncthreads();
-    float out[8];
+    {
+      const int n = c + S - 1;
+      if (n < nch) stage_wr<EP>(ws + (n % S) * kRC * EP, Wr, n * kRC, E, tid);
+      cp_commit();
+    }
+    const float* wb = ws + (c % S) * kRC * EP;
+    float out[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 16; ++u) {
       float a = 0.f;
 #pragma unroll
       for (int k = 0; k < kMaxK; ++k)
-        if (k < K && (unsigned)ids_s[row][k] < (unsigned)E) a = fmaf(dls[row][k], ws[c8 + u][ids_s[row][k]], a);
+        if (k < K) a = fmaf(dls[row][k], wb[(c16 + u) * EP + ids_s[row][k]], a);
       out[u] = a;
     }
-    if (t0 + row < L) store8(dx + (t0 + row) * d + k0 + c8, out);
-    __syncthreads();
+    if (t0 + row < L) {
+      T* o = dx + (t0 + row) * d + (int64_t)c * kRC + c16;
+      store8(o, out);
+      store8(o + 8, out + 8);
+    }
   }
+  cp_wait<0>();
 }
 
 // partial dWr (and dbias) of one 64-row block of Wr over one token split:
-// part[s][j][e] = sum_{t in split s} x[t, j] dlogit[t, e]
+// part[s][j][e] = sum_{t in split s} x[t, j] dlogit[t, e].  Each 64-token
+// chunk stages x[t, j0..j0+63] and the chunk's ids and dlogits by cp.async,
+// then expands the dlogits into a dense 64 x EP tile.
 template <typename T, int EP>
 __global__ void __launch_bounds__(kRThreads) router_dwr_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
                                                                const float* __restrict__ dl, int64_t L, int d, int E,
                                                                int K, int64_t split, float* __restrict__ part,
                                                                float* __restrict__ part_b) {
   using Ly = RLayout<EP>;
-  __shared__ float xs[kRT][kRK + 1];            // xs[j][c] = x[t_c, j0 + j]
-  __shared__ __align__(16) float ds[kRK][EP];   // ds[c][e] = dlogit[t_c, e]
+  constexpr int S = 3, P = XPitch<T>::value;
+  constexpr int XS = kRT * P;
+  extern __shared__ __align__(16) uint8_t rsm[];
+  T* xs = reinterpret_cast<T*>(rsm);                                            // S x [64 tokens][P]
+  float* dd = reinterpret_cast<float*>(rsm + S * XS * sizeof(T));              // [64 tokens][EP]
+  int32_t* is = reinterpret_cast<int32_t*>(dd + kRT * EP);                     // S x [64 * kMaxK]
+  float* ls = reinterpret_cast<float*>(is + S * kRT * kMaxK);                  // S x [64 * kMaxK]
   const int tid = threadIdx.x, te = tid % Ly::TE, tr = tid / Ly::TE;
   const int j0 = blockIdx.x * kRT;
   const int64_t ts = (int64_t)blockIdx.y * split;
   const int64_t tend = min(L, ts + split);
+  const int nch = (int)((tend - ts + kRT - 1) / kRT);
   float acc[Ly::RPT][Ly::EPT];
 #pragma unroll
   for (int i = 0; i < Ly::RPT; ++i)
 #pragma unroll
     for (int j = 0; j < Ly::EPT; ++j) acc[i][j] = 0.f;
   float bacc = 0.f;
-  const int lc = tid >> 3, lj = (tid & 7) * 8;  // token lc of the chunk, columns lj..lj+7
-  for (int64_t c0 = ts; c0 < tend; c0 += kRK) {
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (c0 + lc < tend) load8(x + (c0 + lc) * d + j0 + lj, v);
+  auto stage = [&](int c) {
+    const int st = c % S;
+    const int64_t c0 = ts + (int64_t)c * kRT;
+    stage_rows<T>(xs + st * XS, x, c0, tend, d, j0, tid);
+    for (int i = tid; i < kRT * K; i += kRThreads) {
+      const bool ok = c0 * K + i < tend * K;
+      cp4(saddr(is + st * kRT * kMaxK + i), ok ? (const void*)(ids + c0 * K + i) : (const void*)ids, ok);
+      cp4(saddr(ls + st * kRT * kMaxK + i), ok ? (const void*)(dl + c0 * K + i) : (const void*)dl, ok);
+    }
+  };
 #pragma unroll
-    for (int u = 0; u < 8; ++u) xs[lj + u][lc] = v[u];
-    for (int i = tid; i < kRK * EP; i += kRThreads) (&ds[0][0])[i] = 0.f;
+  for (int c = 0; c < S - 1; ++c) {
+    if (c < nch) stage(c);
+    cp_commit();
+  }
+  for (int c = 0; c < nch; ++c) {
+    cp_wait<S - 2>();
+    __syncthreads();  // chunk c landed; every thread is done with chunk c-1 and its dense tile
+    {
+      const int n = c + S - 1;
+      if (n < nch) stage(n);
+      cp_commit();
+    }
+    const int st = c % S;
+    for (int i = tid; i < kRT * EP; i += kRThreads) dd[i] = 0.f;
     __syncthreads();
-    if (tid < kRK && c0 + tid < tend) {
-      const int64_t t = c0 + tid;
+    if (tid < kRT) {
       for (int k = 0; k < K; ++k) {
-        const int e = ids[t * K + k];
-        if ((unsigned)e < (unsigned)E) ds[tid][e] = dl[t * K + k];
+        const int e = is[st * kRT * kMaxK + tid * K + k];
+        if ((unsigned)e < (unsigned)E) dd[tid * EP + e] = ls[st * kRT * kMaxK + tid * K + k];
       }
     }
     __syncthreads();
-    tile_fma<EP>(xs, ds, te, tr, acc);
-    if (blockIdx.x == 0 && tid < EP) {
-      for (int c = 0; c < kRK; ++c) bacc += ds[c][tid];
+    const T* xa = xs + st * XS;
+#pragma unroll 4
+    for (int t = 0; t < kRT; ++t) {
+      float av[Ly::RPT], bv[Ly::EPT];
+#pragma unroll
+      for (int i = 0; i < Ly::RPT; ++i) av[i] = to_f32(xa[t * P + tr * Ly::RPT + i]);
+#pragma unroll
+      for (int j = 0; j < Ly::EPT; ++j) bv[j] = dd[t * EP + j * Ly::TE + te];
+#pragma unroll
+      for (int i = 0; i < Ly::RPT; ++i)
+#pragma unroll
+        for (int j = 0; j < Ly::EPT; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
-    __syncthreads();
+    if (blockIdx.x == 0 && tid < EP) {
+      for (int t = 0; t < kRT; ++t) bacc += dd[t * EP + tid];
+    }
   }
+  cp_wait<0>();
   float* dst = part + (int64_t)blockIdx.y * d * E;
 #pragma unroll
   for (int i = 0; i < Ly::RPT; ++i) {
@@ -306,21 +540,53 @@ int padded_experts(int E) {
 }
 
 // token splits of the weight-gradient sums: enough CTAs to fill the GPU a
-// few times over, at least one 32-token chunk per split
+// few times over, at least one 64-token chunk per split
 int64_t router_splits(const moeblaze_shape& s) {
   const int64_t jb = s.d / kRT;
   int64_t S = (4 * (int64_t)sm_count() + jb - 1) / jb;
-  const int64_t chunks = (s.L + kRK - 1) / kRK;
+  const int64_t chunks = (s.L + kRT - 1) / kRT;
   if (S > chunks) S = chunks;
   return S < 1 ? 1 : S;
 }
 
 template <typename T, int EP>
+size_t fwd_smem() {
+  return RLayout<EP>::STAGES * ((size_t)kRT * XPitch<T>::value * sizeof(T) + (size_t)kRC * EP * sizeof(float));
+}
+template <int EP>
+size_t dx_smem() {
+  return 3 * (size_t)kRC * EP * sizeof(float);
+}
+template <typename T, int EP>
+size_t dwr_smem() {
+  return 3 * (size_t)kRT * XPitch<T>::value * sizeof(T) + (size_t)kRT * EP * sizeof(float) +
+         3 * 2 * (size_t)kRT * kMaxK * 4;
+}
+
+constexpr size_t kGemvWrBytes = 160 * 1024;  // largest Wr staged whole by the GEMV forward
+
+template <typename T, int EP>
 moeblaze_status fwd_ep(const moeblaze_shape& s, const void* x, const float* Wr, const float* bias, int32_t* ids,
                        float* gates, cudaStream_t st) {
+  if constexpr (EP <= 16) {
+    const size_t wb = ((size_t)s.d * EP + (size_t)s.d / 2) * sizeof(float);
+    if (wb <= kGemvWrBytes) {
+      auto kern = router_fwd_gemv_kernel<T, EP>;
+      MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wb));
+      const int threads = 512;
+      int64_t blocks = (s.L + (threads / 32) * 4 - 1) / ((threads / 32) * 4);
+      if (blocks > (int64_t)sm_count()) blocks = sm_count();  // one persistent CTA per SM
+      kern<<<(unsigned)blocks, threads, wb, st>>>(static_cast<const T*>(x), Wr, bias, s.L, s.d, s.E, s.K, ids, gates);
+      MB_CUDA(cudaGetLastError());
+      count_launch();
+      return MOEBLAZE_OK;
+    }
+  }
+  auto kern = router_fwd_kernel<T, EP>;
+  const size_t sm = fwd_smem<T, EP>();
+  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
   const unsigned grid = (unsigned)((s.L + kRT - 1) / kRT);
-  router_fwd_kernel<T, EP><<<grid, kRThreads, 0, st>>>(static_cast<const T*>(x), Wr, bias, s.L, s.d, s.E, s.K, ids,
-                                                      gates);
+  kern<<<grid, kRThreads, sm, st>>>(static_cast<const T*>(x), Wr, bias, s.L, s.d, s.E, s.K, ids, gates);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
@@ -331,18 +597,27 @@ moeblaze_status bwd_ep(const moeblaze_shape& s, const void* x, const float* Wr, 
                        const float* gates, const float* dgates, float* dWr, float* dbias, void* dx, void* ws,
                        cudaStream_t st) {
   const int64_t S = router_splits(s);
-  const int64_t split = ((s.L + S - 1) / S + kRK - 1) / kRK * kRK;
+  const int64_t split = ((s.L + S - 1) / S + kRT - 1) / kRT * kRT;
   char* w = static_cast<char*>(ws);
   float* dl = reinterpret_cast<float*>(w);
   float* part = reinterpret_cast<float*>(w + align_up(sizeof(float) * s.L * s.K, 256));
   float* part_b = part + (size_t)S * s.d * s.E;
   const unsigned tiles = (unsigned)((s.L + kRT - 1) / kRT);
-  router_dx_kernel<T, EP><<<tiles, kRThreads, 0, st>>>(Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, dl,
-                                                       static_cast<T*>(dx));
-  MB_CUDA(cudaGetLastError());
-  router_dwr_kernel<T, EP><<<dim3((unsigned)(s.d / kRT), (unsigned)S), kRThreads, 0, st>>>(
-      static_cast<const T*>(x), ids, dl, s.L, s.d, s.E, s.K, split, part, part_b);
-  MB_CUDA(cudaGetLastError());
+  {
+    auto kern = router_dx_kernel<T, EP>;
+    const size_t sm = dx_smem<EP>();
+    MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<tiles, kRThreads, sm, st>>>(Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, dl, static_cast<T*>(dx));
+    MB_CUDA(cudaGetLastError());
+  }
+  {
+    auto kern = router_dwr_kernel<T, EP>;
+    const size_t sm = dwr_smem<T, EP>();
+    MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<dim3((unsigned)(s.d / kRT), (unsigned)S), kRThreads, sm, st>>>(static_cast<const T*>(x), ids, dl, s.L, s.d,
+                                                                          s.E, s.K, split, part, part_b);
+    MB_CUDA(cudaGetLastError());
+  }
   const int64_t n = (int64_t)s.d * s.E;
   int64_t blocks = (n + s.E + 255) / 256;
   if (blocks > 8 * (int64_t)sm_count()) blocks = 8 * (int64_t)sm_count();
