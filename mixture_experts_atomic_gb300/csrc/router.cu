@@ -409,12 +409,12 @@ __global__ void __launch_bounds__(kRThreads) router_dx_kernel(const float* __res
     const float* wb = ws + (c % S) * kRC * EP;
     float out[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      float a = 0.f;
+    for (int u = 0; u < 16; ++u) out[u] = 0.f;
+    for (int k = 0; k < K; ++k) {  // the slot's dlogit and expert column, hoisted
+      const float dv = dls[row][k];
+      const float* wcol = wb + c16 * EP + ids_s[row][k];
 #pragma unroll
-      for (int k = 0; k < kMaxK; ++k)
-        if (k < K) a = fmaf(dls[row][k], wb[(c16 + u) * EP + ids_s[row][k]], a);
-      out[u] = a;
+      for (int u = 0; u < 16; ++u) out[u] = fmaf(dv, wcol[u * EP], out[u]);
     }
     if (t0 + row < L) {
       T* o = dx + (t0 + row) * d + (int64_t)c * kRC + c16;
@@ -517,6 +517,74 @@ __global__ void __launch_bounds__(kRThreads) router_dwr_kernel(const T* __restri
   if (blockIdx.x == 0 && tid < E) part_b[(int64_t)blockIdx.y * E + tid] = bacc;
 }
 
+// dWr for few experts (EP <= 16): a thread owns 8 consecutive rows of Wr
+// (columns j of x) for all EP experts and reads its 16-byte piece of each
+// token row of x straight from global memory (coalesced across the CTA);
+// the chunk's dlogits are expanded to a dense 64 x EP tile in shared memory
+// and read as broadcasts.  part[s][j][e] as in router_dwr_kernel.
+template <typename T, int EP>
+__global__ void __launch_bounds__(256) router_dwr_small_kernel(const T* __restrict__ x,
+                                                               const int32_t* __restrict__ ids,
+                                                               const float* __restrict__ dl, int64_t L, int d, int E,
+                                                               int K, int64_t split, float* __restrict__ part,
+                                                               float* __restrict__ part_b) {
+  __shared__ __align__(16) float dd[kRT][EP];
+  const int tid = threadIdx.x;
+  const int j = (blockIdx.x * blockDim.x + tid) * 8;  // first of this thread's 8 columns
+  const bool jv = j < d;
+  const int64_t ts = (int64_t)blockIdx.y * split;
+  const int64_t tend = min(L, ts + split);
+  float acc[8][EP];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
+  float bacc = 0.f;
+  for (int64_t c0 = ts; c0 < tend; c0 += kRT) {
+    __syncthreads();  // every thread is done with the previous chunk's tile
+    for (int i = tid; i < kRT * EP; i += blockDim.x) (&dd[0][0])[i] = 0.f;
+    __syncthreads();
+    if (tid < kRT && c0 + tid < tend) {
+      const int64_t t = c0 + tid;
+      for (int k = 0; k < K; ++k) {
+        const int e = ids[t * K + k];
+        if ((unsigned)e < (unsigned)E) dd[tid][e] = dl[t * K + k];
+      }
+    }
+    __syncthreads();
+    const int n = (int)min((int64_t)kRT, tend - c0);
+    if (blockIdx.x == 0 && tid < EP)
+      for (int t = 0; t < n; ++t) bacc += dd[t][tid];
+    if (!jv) continue;
+#pragma unroll 4
+    for (int t = 0; t < n; ++t) {
+      float xv[8];
+      load8(x + (c0 + t) * d + j, xv);
+      const float4* dr = reinterpret_cast<const float4*>(&dd[t][0]);
+#pragma unroll
+      for (int e4 = 0; e4 < EP / 4; ++e4) {
+        const float4 w = dr[e4];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[u][4 * e4 + 0] = fmaf(xv[u], w.x, acc[u][4 * e4 + 0]);
+          acc[u][4 * e4 + 1] = fmaf(xv[u], w.y, acc[u][4 * e4 + 1]);
+          acc[u][4 * e4 + 2] = fmaf(xv[u], w.z, acc[u][4 * e4 + 2]);
+          acc[u][4 * e4 + 3] = fmaf(xv[u], w.w, acc[u][4 * e4 + 3]);
+        }
+      }
+    }
+  }
+  float* dst = part + (int64_t)blockIdx.y * d * E;
+  if (jv) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e < E) dst[(int64_t)(j + u) * E + e] = acc[u][e];
+  }
+  if (blockIdx.x == 0 && tid < E) part_b[(int64_t)blockIdx.y * E + tid] = bacc;
+}
+
 __global__ void router_reduce_kernel(const float* __restrict__ part, const float* __restrict__ part_b, int64_t n,
                                      int E, int S, float* __restrict__ dWr, float* __restrict__ dbias) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n + E; i += (int64_t)gridDim.x * blockDim.x) {
@@ -539,10 +607,16 @@ int padded_experts(int E) {
   return ep;
 }
 
+// column blocks of the dWr kernel: 64 rows of Wr per CTA, or for few
+// experts 8 rows per thread of a 256-thread CTA
+int64_t router_col_blocks(const moeblaze_shape& s) {
+  return padded_experts(s.E) <= 16 ? (s.d + 2047) / 2048 : s.d / kRT;
+}
+
 // token splits of the weight-gradient sums: enough CTAs to fill the GPU a
 // few times over, at least one 64-token chunk per split
 int64_t router_splits(const moeblaze_shape& s) {
-  const int64_t jb = s.d / kRT;
+  const int64_t jb = router_col_blocks(s);
   int64_t S = (4 * (int64_t)sm_count() + jb - 1) / jb;
   const int64_t chunks = (s.L + kRT - 1) / kRT;
   if (S > chunks) S = chunks;
@@ -610,7 +684,11 @@ moeblaze_status bwd_ep(const moeblaze_shape& s, const void* x, const float* Wr, 
     kern<<<tiles, kRThreads, sm, st>>>(Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, dl, static_cast<T*>(dx));
     MB_CUDA(cudaGetLastError());
   }
-  {
+  if constexpr (EP <= 16) {
+    router_dwr_small_kernel<T, EP><<<dim3((unsigned)router_col_blocks(s), (unsigned)S), 256, 0, st>>>(
+        static_cast<const T*>(x), ids, dl, s.L, s.d, s.E, s.K, split, part, part_b);
+    MB_CUDA(cudaGetLastError());
+  } else {
     auto kern = router_dwr_kernel<T, EP>;
     const size_t sm = dwr_smem<T, EP>();
     MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
