@@ -35,7 +35,7 @@ from mixture_experts_atomic_gb300 import binding as B  # noqa: E402
 from mixture_experts_atomic_gb300 import inputs as I  # noqa: E402
 
 METRIC = "MoE layer fwd+bwd tokens/s (bf16), tensor-pipe %; dispatch-build HBM GB/s"
-FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 L2_BYTES = 129 * 1024 * 1024
 GEMM_SRC = "mixture_experts_atomic_gb300/csrc/gemm_tc.cu"
 IDENTITY_SRC = "mixture_experts_atomic_gb300/csrc/identity.cu"
@@ -314,9 +314,65 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches_per_step": launches / max(1, args.steps),
         "clocks": clk,
     }
+    if cfg.router in ("softmax", "softmax_bias"):
+        out["router"] = run_router(cfg, inp, dev, flush, pk)
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, cfg, layer, inp, dev, world)
     del flush
+    return out
+
+
+def fp32_alu_tflops(pk):
+    """CUDA-core fp32 peak: 152 SMs x 128 fp32 lanes x 2 FLOP (FMA) x the
+    maximum SM clock (MEASURED_PEAKS' sm_max_mhz, else 2070 MHz)."""
+    mhz = pk.get("sm_max_mhz", 2070.0)
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def run_router(cfg, inp, dev, flush, pk, iters=10):
+    """The workload's softmax router (the step before the dispatch) and its
+    backward, timed outside the layer step with CUDA events, L2 flushed
+    before each call.  Algorithmic bytes: forward x read, ids and gates
+    written, Wr read; backward x read, dx written, ids/gates/dgates read, Wr
+    read, dWr written.  FLOPs 2LdE (forward) and 4LdE (backward)."""
+    from mixture_experts_atomic_gb300 import binding as B
+    x = inp["x"]
+    Wr, b = I.router_weights(cfg, dev)
+    sh = B.make_shape(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act)
+    ids = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device=dev)
+    gates = torch.empty((cfg.L, cfg.K), dtype=torch.float32, device=dev)
+    dg = torch.randn(cfg.L, cfg.K, device=dev)
+    dWr, db, dx = torch.empty_like(Wr), torch.empty(cfg.E, device=dev), torch.empty_like(x)
+    ws = torch.empty(B.moeblaze_router_backward_workspace_bytes(sh), dtype=torch.uint8, device=dev)
+    calls = {"forward": lambda: B.router_forward(sh, x, Wr, b, ids, gates),
+             "backward": lambda: B.router_backward(sh, x, Wr, ids, gates, dg, dWr, db, dx, ws)}
+    s_x = cfg.L * cfg.d * cfg.elem_bytes
+    work = {"forward": (s_x + 8 * cfg.L * cfg.K + 4 * cfg.d * cfg.E, 2 * cfg.L * cfg.d * cfg.E),
+            "backward": (2 * s_x + 12 * cfg.L * cfg.K + 8 * cfg.d * cfg.E, 4 * cfg.L * cfg.d * cfg.E)}
+    alu = fp32_alu_tflops(pk)
+    ridge = alu * 1e12 / (pk["hbm_gbs"] * 1e9)  # FLOP per byte where the two bounds meet
+    out = {"fp32_alu_peak_tflops": alu}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        nbytes, flops = work[name]
+        if flops / nbytes > ridge:
+            ach = flops / (ms * 1e-3) / 1e12
+            roof = {"bound": "alu", "achieved": ach, "peak": alu, "unit": "TFLOP/s", "frac": ach / alu}
+        else:
+            ach = nbytes / (ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
+        out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "flops": flops, "roofline": roof}
     return out
 
 
