@@ -63,3 +63,82 @@ class MoELayer:
 
     def meta(self):
         return B.meta_arrays(self.shape, self.disp)
+
+
+class StepPipeline:
+    """Runs layer steps whose inputs live in pinned host memory and whose
+    outputs (y, dX) go back to pinned host memory, overlapping the copies
+    with the compute of the neighbouring steps:
+
+      copy stream     H2D(inputs i+1) into the other input slot, while step i computes
+      compute stream  dispatch, forward, backward of step i
+      out stream      D2H(y_i) right after forward i (overlaps backward i),
+                      D2H(dX_i) after backward i (overlaps the next dispatch and forward)
+
+    The next forward waits for D2H(y_i) and the next backward for D2H(dX_i)
+    before overwriting y and dX; an input slot is reused only after the step
+    that read it has finished.  Every step's copies are part of the run."""
+
+    def __init__(self, layer: MoELayer, keys=("x", "ids", "gates", "dY")):
+        self.layer = layer
+        self.keys = keys
+        self.slots = None
+        self.copy = torch.cuda.Stream()
+        self.out = torch.cuda.Stream()
+        self.comp = torch.cuda.current_stream()
+
+    def _ensure_slots(self, batch):
+        if self.slots is None:
+            self.slots = [{k: torch.empty(batch[k].shape, dtype=batch[k].dtype, device="cuda") for k in self.keys}
+                          for _ in range(2)]
+            self.in_ready = [torch.cuda.Event() for _ in range(2)]
+            self.slot_free = [torch.cuda.Event() for _ in range(2)]
+            self.y_done = torch.cuda.Event()
+            self.dx_done = torch.cuda.Event()
+            self.fwd_done = torch.cuda.Event()
+            self.bwd_done = torch.cuda.Event()
+
+    def _h2d(self, i, batch):
+        s = i % 2
+        with torch.cuda.stream(self.copy):
+            if i >= 2:
+                self.copy.wait_event(self.slot_free[s])
+            for k in self.keys:
+                self.slots[s][k].copy_(batch[k], non_blocking=True)
+            self.in_ready[s].record(self.copy)
+
+    def run(self, batches, outputs, weights):
+        """batches[i]: dict of pinned host tensors (x, ids, gates, dY);
+        outputs[i]: (y_host, dX_host) pinned; weights: (W1, W2, W3) on the device."""
+        L = self.layer
+        n = len(batches)
+        if n == 0:
+            return
+        self._ensure_slots(batches[0])
+        self._h2d(0, batches[0])
+        for i in range(n):
+            s = i % 2
+            if i + 1 < n:
+                self._h2d(i + 1, batches[i + 1])
+            d = self.slots[s]
+            self.comp.wait_event(self.in_ready[s])
+            L.dispatch(d["ids"])
+            if i > 0:
+                self.comp.wait_event(self.y_done)
+            L.forward(d["x"], d["gates"], *weights)
+            self.fwd_done.record(self.comp)
+            with torch.cuda.stream(self.out):
+                self.out.wait_event(self.fwd_done)
+                outputs[i][0].copy_(L.y, non_blocking=True)
+                self.y_done.record(self.out)
+            if i > 0:
+                self.comp.wait_event(self.dx_done)
+            L.backward(d["dY"], d["x"], d["gates"], *weights)
+            self.bwd_done.record(self.comp)
+            self.slot_free[s].record(self.comp)
+            with torch.cuda.stream(self.out):
+                self.out.wait_event(self.bwd_done)
+                outputs[i][1].copy_(L.dX, non_blocking=True)
+                self.dx_done.record(self.out)
+        self.comp.wait_stream(self.out)
+        self.comp.wait_stream(self.copy)

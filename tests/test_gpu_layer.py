@@ -94,3 +94,37 @@ def test_workload_sampled(ci):
 
 def test_identity_workload_sampled():
     sampled_compare(I.CONFIGS[4], n_tok=64)
+
+
+def test_step_pipeline_matches_plain_steps():
+    """The pipelined runner (host inputs -> device, compute, device -> host,
+    copies overlapped across steps) gives, for three different batches, the
+    same y and dX bits as plain steps (K = 2: every reduction is
+    order-independent)."""
+    from mixture_experts_atomic_gb300.layer import MoELayer, StepPipeline
+    cfg = I.MoEConfig("t_pipeline", 1000, 256, 384, 5, 2, "swiglu", "bf16", 31, "softmax")
+    base = I.make_inputs(cfg, "cpu")
+    W = tuple(base[k].cuda() for k in ("W1", "W2", "W3"))
+    batches = []
+    for i in range(3):
+        ids, gates = I.random_routing(cfg.L, cfg.E, cfg.K, 40 + i)
+        g = torch.Generator().manual_seed(50 + i)
+        x = torch.randn(cfg.L, cfg.d, generator=g).to(torch.bfloat16)
+        dY = torch.randn(cfg.L, cfg.d, generator=g).to(torch.bfloat16)
+        batches.append({"x": x, "ids": ids, "gates": gates, "dY": dY})
+    ref = MoELayer.for_config(cfg, "cuda", with_dgates=False)
+    want = []
+    for bt in batches:
+        dev = {k: v.cuda() for k, v in bt.items()}
+        dev.update(dict(zip(("W1", "W2", "W3"), W)))
+        ref.step(dev)
+        want.append((ref.y.cpu().clone(), ref.dX.cpu().clone()))
+    layer = MoELayer.for_config(cfg, "cuda", with_dgates=False)
+    host = [{k: v.pin_memory() for k, v in bt.items()} for bt in batches]
+    outs = [(torch.empty((cfg.L, cfg.d), dtype=torch.bfloat16).pin_memory(),
+             torch.empty((cfg.L, cfg.d), dtype=torch.bfloat16).pin_memory()) for _ in batches]
+    StepPipeline(layer).run(host, outs, W)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    for (y, dx), (wy, wdx) in zip(outs, want):
+        assert torch.equal(y, wy) and torch.equal(dx, wdx)
