@@ -385,15 +385,17 @@ def run_e2e(args, cfg, layer, inp, dev, world):
     from mixture_experts_atomic_gb300.layer import StepPipeline
     keys = ("x", "ids", "gates", "dY")
     host = {k: inp[k].cpu().pin_memory() for k in keys}
-    outs = [(torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory(),
-             torch.empty(layer.dX.shape, dtype=layer.dX.dtype).pin_memory()) for _ in range(2)]
+    # one host output pair serves every step: the output stream copies into
+    # it one step after another
+    out = (torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory(),
+           torch.empty(layer.dX.shape, dtype=layer.dX.dtype).pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs[0])
+    d2h = sum(t.numel() * t.element_size() for t in out)
     W = (inp.get("W1"), inp.get("W2"), inp.get("W3"))
     pipe = StepPipeline(layer, keys)
 
     def run(n):
-        pipe.run([host] * n, [outs[i % 2] for i in range(n)], W)
+        pipe.run([host] * n, [out] * n, W)
 
     run(max(2, args.warmup))
     torch.cuda.synchronize()
