@@ -18,7 +18,7 @@
 //               plain stores).
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
-// [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile
+// [pad_off[e], pad_off[e+1]), 128-row aligned, so every 128-row M tile
 // belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
 // routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
 // gather a valid token and are zero where they feed a reduction.
