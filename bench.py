@@ -416,6 +416,39 @@ def run_e2e(args, cfg, layer, inp, dev, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "copies": "overlapped with the neighbouring steps' compute"}
 
 
+def run_dispatch_only(args, local_rank):
+    """The dispatch build alone on the workload's routing (ids only; no
+    activations or weights are allocated), CUDA-event timed, L2 flushed."""
+    cfg = I.CONFIGS[args.config]  # already scaled by --tokens
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ids, _ = I.make_routing(cfg, None, dev) if cfg.router == "zipf" else I.make_routing(cfg, I.make_x(cfg, dev), dev)
+    shape = B.make_shape(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act)
+    disp = B.alloc_dispatch(shape, dev)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        B.dispatch_build(shape, ids, disp)
+    ts = []
+    for _ in range(args.steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.dispatch_build(shape, ids, disp)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert B.device_error(shape, disp) == 0
+    ms = statistics.median(ts)
+    nb = dispatch_bytes(cfg)
+    pk, src = peaks()
+    ach = nb / (ms * 1e-3) / 1e9
+    return {"metric": "dispatch build HBM GB/s", "config": {"workload": cfg.name, "L": cfg.L, "E": cfg.E, "K": cfg.K},
+            "ms": ms, "algorithmic_bytes": nb, "steps": args.steps, "warmup": args.warmup,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / pk["hbm_gbs"], "peak_source": src}}
+
+
 def run_reference(args, cfg):
     """The CPU oracle as the reference arm: each step runs it on a bounded
     sample of the workload's tokens (same shapes otherwise)."""
@@ -454,6 +487,8 @@ def main():
                     help="run the workload with this many tokens instead (smaller profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["dispatch"], default=None,
+                    help="time only the dispatch build of the workload (allocates only its routing and index buffers)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -465,6 +500,10 @@ def main():
         cfg = cfg.scaled(L=args.tokens, name=f"{cfg.name}_tokens{args.tokens}")
         I.CONFIGS[args.config] = cfg
 
+    if args.only == "dispatch":
+        if rank == 0:
+            print(json.dumps(run_dispatch_only(args, local_rank)), flush=True)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

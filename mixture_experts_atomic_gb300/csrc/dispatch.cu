@@ -10,15 +10,16 @@
 //                      (expert, chunk) popcount.
 //   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
 //                      counts -> chunk bases and n_e.
-//   K3 scatter_kernel  one CTA per chunk.  Scans n_e over experts ->
-//                      expert_token_offsets; a prefix walk over each
-//                      expert's 32 popcounts gives every word its first
-//                      position; each token then places its K slots:
-//                      pos = off[e] + base[c][e] + wordprefix + popc(bits below).
+//   K2b offsets_kernel one CTA: expert_token_offsets (the scan of n_e), the
+//                      padded row offsets, the GEMM tile table and the
+//                      experts' descending-load order.
+//   K3 scatter_kernel  one CTA per chunk.  A shuffle scan over each expert's
+//                      32 popcounts gives every word its first position;
+//                      each token then places its K slots:
+//                      pos = off[e] + base[e][c] + wordprefix + popc(bits below).
 //                      Writes token_index_map and token_expert_indices
-//                      coalesced (token-major) and expert_token_indices[pos].
-//                      CTA 0 also writes the padded row offsets, the GEMM tile
-//                      table and the experts' descending-load order.
+//                      token-major (one vector per token) and
+//                      expert_token_indices[pos].
 //
 // No global atomics on the data path (the device error word is the only
 // atomic, and only for invalid routing).
@@ -75,19 +76,25 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   }
   for (int i = tid; i < E * kRow; i += kThreads) words[i] = 0u;
 
+  // routing checks: ids in range, pairwise distinct per token (K*(K-1)/2 compares)
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j)
+  for (int j = 0; j < kPasses; ++j) {
+    const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
+    if (t >= L) continue;
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) {
-      if (k >= K) continue;
+      if (k >= K) break;
       const int e = e_k[j][k];
-      const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
-      if (t < L && (e < 0 || e >= E)) { bad = true; e_k[j][k] = -1; }
+      if (e < 0 || e >= E) {
+        bad = true;
+        e_k[j][k] = -1;
+      }
 #pragma unroll
-      for (int i = 0; i < kMaxK; ++i)
-        if (i < k && e_k[j][k] >= 0 && e_k[j][k] == e_k[j][i]) bad = true;
+      for (int i = 0; i < k; ++i)
+        if (e_k[j][k] >= 0 && e_k[j][k] == e_k[j][i]) bad = true;
     }
+  }
   if (bad) atomicOr(err, kErrBadRouting);
   __syncthreads();
 
@@ -108,19 +115,24 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   }
   __syncthreads();
 
-  // expert-major store: expert e's 32 words of this chunk are one 128-byte line
-  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) {
-    const int e = i / (kChunkWords / 4), pc = i % (kChunkWords / 4);
-    const uint32_t* src = words + e * kRow + pc * 4;
-    reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] =
-        make_uint4(src[0], src[1], src[2], src[3]);
-  }
-  // per-(expert, chunk) population count, stored [E][C]
-  for (int e = tid; e < E; e += kThreads) {
-    int c = 0;
-#pragma unroll
-    for (int w = 0; w < kChunkWords; ++w) c += __popc(words[e * kRow + w]);
-    cnt[(int64_t)e * C + chunk] = c;
+  // expert-major store, 4 words (16 bytes) per thread, and the per-(expert,
+  // chunk) popcount: the 8 threads of one expert are 8 consecutive lanes and
+  // add their counts with shuffles (counts stored [E][C] for the scan)
+  for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
+    const int i = i0 + tid;
+    const bool v = i < E * 8;
+    const int e = i >> 3, pc = i & 7;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (v) {
+      const uint32_t* src = words + e * kRow + pc * 4;
+      u = make_uint4(src[0], src[1], src[2], src[3]);
+      reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] = u;
+    }
+    int c = __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    if (v && pc == 0) cnt[(int64_t)e * C + chunk] = c;
   }
 }
 
@@ -171,37 +183,82 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
   if (threadIdx.x == 0) n_e[e] = total;
 }
 
-// K3: one CTA per chunk.  Every global read (expert totals, chunk bases,
-// bitmap words, ids) is issued first; a block scan of n_e gives
-// expert_token_offsets; one thread per expert walks its 32 words to give
-// each word its first position; each token then places its K slots:
-// pos = off[e] + base[e][c] + wordprefix + popc(bits below).
-__global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
-                                                           const uint32_t* __restrict__ bitmap, int64_t C,
-                                                           const int32_t* __restrict__ base,
-                                                           const int32_t* __restrict__ n_e, int32_t* __restrict__ D1,
-                                                           int32_t* __restrict__ D2, int32_t* __restrict__ D3,
-                                                           int32_t* __restrict__ D4, MetaView meta, int64_t max_tiles) {
-  extern __shared__ int32_t sm[];
-  uint32_t* words = reinterpret_cast<uint32_t*>(sm);  // [E][kRow]
-  int32_t* off = sm + E * kRow;                       // [E+1]
-  int32_t* ebase = off + E + 1;                       // [E]: off[e] + base[e][chunk]
-  uint16_t* wpre = reinterpret_cast<uint16_t*>(ebase + E);  // [E][kRow]: set bits before word w
+// K2b: one CTA.  expert_token_offsets (exclusive scan of n_e) and the GEMM
+// metadata: padded row offsets, tile count, tile -> expert table and the
+// experts in descending order of load.  Computed once here instead of in
+// every chunk's CTA.
+__global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __restrict__ n_e, int E,
+                                                           int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles) {
+  __shared__ int32_t off[kMaxE + 1];
+  __shared__ int32_t poff[kMaxE + 1];
   __shared__ int wsum[32];
   __shared__ int total;
-  const int tid = threadIdx.x;
-  const int64_t chunk = blockIdx.x;
-  const int64_t wpe = C * kChunkWords;
-  constexpr int kEPT = kMaxE / kThreads;  // experts per thread
-
-  // ---- all global reads first
-  int nv[kEPT], cb[kEPT];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kEPT = kMaxE / kThreads;
+  int carry = 0, pcarry = 0;
 #pragma unroll
   for (int q = 0; q < kEPT; ++q) {
     const int e = tid + q * kThreads;
-    nv[q] = e < E ? n_e[e] : 0;
-    cb[q] = e < E ? base[(int64_t)e * C + chunk] : 0;
+    const int n = e < E ? n_e[e] : 0;
+    const int pn = (n + kRowPad - 1) / kRowPad * kRowPad;
+    const int pre = block_excl_scan(n, wsum, &total);
+    const int tot = total;
+    const int ppre = block_excl_scan(pn, wsum, &total);
+    if (e < E) {
+      off[e] = carry + pre;
+      poff[e] = pcarry + ppre;
+    }
+    carry += tot;
+    pcarry += total;
   }
+  if (tid == 0) {
+    off[E] = carry;
+    poff[E] = pcarry;
+    *meta.num_m_tiles = pcarry / kTileM;
+    *meta.padded_rows = pcarry;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += kThreads) {
+    D2[e] = off[e];
+    meta.pad_off[e] = poff[e];
+  }
+  // tile table: one warp per expert writes its range of 128-row tiles
+  for (int e = warp; e < E; e += kThreads / 32)
+    for (int32_t m = poff[e] / kTileM + lane; m < poff[e + 1] / kTileM; m += 32) meta.tile_expert[m] = e;
+  for (int64_t m = poff[E] / kTileM + tid; m < max_tiles; m += kThreads) meta.tile_expert[m] = -1;
+  // descending load, equal loads by index
+  for (int e = tid; e < E; e += kThreads) {
+    const int32_t me = off[e + 1] - off[e];
+    int rank = 0;
+    for (int j = 0; j < E; ++j) {
+      const int32_t nj = off[j + 1] - off[j];
+      rank += (nj > me) || (nj == me && j < e);
+    }
+    meta.order[rank] = e;
+  }
+}
+
+// K3: one CTA per chunk.  Every global read (expert offsets, chunk bases,
+// bitmap words, ids) is issued first; the word prefixes of every expert
+// come from a shuffle scan over its 32 words (4 per thread); each (token,
+// slot) then gets pos = off[e] + base[e][c] + wordprefix + popc(bits below).
+// token_expert_indices and token_index_map are written token-major, one
+// vector per token, and expert_token_indices[pos] = token.
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
+                                                           const uint32_t* __restrict__ bitmap, int64_t C,
+                                                           const int32_t* __restrict__ base,
+                                                           const int32_t* __restrict__ off, int32_t* __restrict__ D1,
+                                                           int32_t* __restrict__ D3, int32_t* __restrict__ D4) {
+  extern __shared__ int32_t sm[];
+  uint32_t* words = reinterpret_cast<uint32_t*>(sm);         // [E][kRow]
+  int32_t* ebase = sm + E * kRow;                            // [E]: off[e] + base[e][chunk]
+  uint16_t* wpre = reinterpret_cast<uint16_t*>(ebase + E);   // [E][kRow]: set bits before word w (odd row stride)
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t chunk = blockIdx.x;
+  const int64_t wpe = C * kChunkWords;
+
+  // ---- all global reads first
+  for (int e = tid; e < E; e += kThreads) ebase[e] = off[e] + base[(int64_t)e * C + chunk];
   int e_k[kPasses][kMaxK];
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
@@ -215,31 +272,33 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
     uint32_t* dst = words + e * kRow + pc * 4;
     dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
   }
-
-  // ---- expert offsets (exclusive scan of n_e over experts); thread tid
-  // owns experts tid and tid + 256, scanned as two ordered halves
-  int pre0 = block_excl_scan(nv[0], wsum, &total);
-  const int tot0 = total;
-  if (tid < E) off[tid] = pre0;
-  if constexpr (kEPT > 1) {
-    int pre1 = block_excl_scan(nv[1], wsum, &total);
-    if (tid + kThreads < E) off[tid + kThreads] = tot0 + pre1;
-    if (tid == 0) off[E] = tot0 + total;
-  } else {
-    if (tid == 0) off[E] = tot0;
-  }
   __syncthreads();
 
-  // ---- first position of every (expert, word): one thread per expert
+  // ---- word prefixes: thread i covers words 4g..4g+3 of expert i/8 (g = i%8);
+  // the 8 threads of an expert are consecutive lanes and scan their counts
+  // with shuffles
+  for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
+    const int i = i0 + tid;
+    const bool v = i < E * 8;
+    const int e = i >> 3, g = i & 7;
+    int c[4] = {0, 0, 0, 0};
+    if (v) {
 #pragma unroll
-  for (int q = 0; q < kEPT; ++q) {
-    const int e = tid + q * kThreads;
-    if (e < E) {
-      ebase[e] = off[e] + cb[q];
-      int r = 0;
-      for (int w = 0; w < kChunkWords; ++w) {
-        wpre[e * kRow + w] = (uint16_t)r;
-        r += __popc(words[e * kRow + w]);
+      for (int q = 0; q < 4; ++q) c[q] = __popc(words[e * kRow + 4 * g + q]);
+    }
+    const int mine = c[0] + c[1] + c[2] + c[3];
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((lane & 7) >= o) incl += u;
+    }
+    if (v) {
+      int r = incl - mine;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wpre[e * kRow + 4 * g + q] = (uint16_t)r;
+        r += c[q];
       }
     }
   }
@@ -253,56 +312,35 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
     if (t >= L) continue;
     const int w = tl >> 5, b = tl & 31;
     const uint32_t below = (1u << b) - 1u;
+    int d3[kMaxK], d4[kMaxK];
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) {
-      if (k >= K) continue;
-      const int e = e_k[j][k];
-      int32_t pos = -1;
-      if (e >= 0 && e < E) {
-        pos = ebase[e] + wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
-        D1[pos] = (int32_t)t;
-      }
-      D3[t * K + k] = e;
-      D4[t * K + k] = pos;
-    }
-  }
-
-  if (chunk == 0) {
-    // offsets, padded offsets, tile table, load order (CTA 0 only)
-    __shared__ int32_t poff[kMaxE + 1];
-    for (int e = tid; e <= E; e += kThreads) D2[e] = off[e];
-    if (tid == 0) {
-      int32_t r = 0;
-      for (int e = 0; e < E; ++e) {
-        poff[e] = r;
-        meta.pad_off[e] = r;
-        const int32_t n = off[e + 1] - off[e];
-        r += (n + kRowPad - 1) / kRowPad * kRowPad;
-      }
-      poff[E] = r;
-      meta.pad_off[E] = r;
-      *meta.num_m_tiles = r / kTileM;
-      *meta.padded_rows = r;
-    }
-    __syncthreads();
-    const int32_t ntiles = poff[E] / kTileM;
-    // tile table: one warp per expert writes its range of 128-row tiles
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int e = warp; e < E; e += kThreads / 32)
-      for (int32_t m = poff[e] / kTileM + lane; m < poff[e + 1] / kTileM; m += 32) meta.tile_expert[m] = e;
-    for (int64_t m = ntiles + tid; m < max_tiles; m += kThreads) meta.tile_expert[m] = -1;
-#pragma unroll
-    for (int q = 0; q < kEPT; ++q) {
-      const int e = tid + q * kThreads;
-      if (e < E) {
-        const int32_t me = off[e + 1] - off[e];
-        int rank = 0;
-        for (int j = 0; j < E; ++j) {
-          const int32_t nj = off[j + 1] - off[j];
-          rank += (nj > me) || (nj == me && j < e);
+      d3[k] = e_k[j][k];
+      d4[k] = -1;
+      if (k < K) {
+        const int e = e_k[j][k];
+        if (e >= 0 && e < E) {
+          const int pos = ebase[e] + wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
+          D1[pos] = (int32_t)t;
+          d4[k] = pos;
         }
-        meta.order[rank] = e;
       }
+    }
+    int32_t* o3 = D3 + t * K;
+    int32_t* o4 = D4 + t * K;
+    if (K == 4) {
+      *reinterpret_cast<int4*>(o3) = make_int4(d3[0], d3[1], d3[2], d3[3]);
+      *reinterpret_cast<int4*>(o4) = make_int4(d4[0], d4[1], d4[2], d4[3]);
+    } else if (K == 2) {
+      *reinterpret_cast<int2*>(o3) = make_int2(d3[0], d3[1]);
+      *reinterpret_cast<int2*>(o4) = make_int2(d4[0], d4[1]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k)
+        if (k < K) {
+          o3[k] = d3[k];
+          o4[k] = d4[k];
+        }
     }
   }
 }
@@ -363,11 +401,14 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  const size_t sm3 = (size_t)E * kRow * (4 + 2) + (2 * E + 1) * sizeof(int32_t);
+  offsets_kernel<<<1, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  const size_t sm3 = (size_t)E * kRow * 4 + (size_t)E * sizeof(int32_t) + (size_t)E * kRow * 2;
   if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, meta.n_e,
-                                                      out.expert_token_indices, out.expert_token_offsets,
-                                                      out.token_expert_indices, out.token_index_map, meta, mt);
+  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, out.expert_token_offsets,
+                                                      out.expert_token_indices, out.token_expert_indices,
+                                                      out.token_index_map);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
