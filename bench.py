@@ -94,18 +94,22 @@ def stage_flops(cfg):
 
 
 def dispatch_bytes(cfg):
-    """Algorithmic bytes of the dispatch build: ids read, three (L,K) maps and
-    the offsets written, the bit-packed bitmap written once and read once."""
+    """Algorithmic bytes of the dispatch build (the per-token figure of the
+    method's dispatch): ids read (4LK), D1, D3, D4 written (12LK), the
+    offsets, and the bit-packed L x E bitmap written once and read twice
+    (3LE/8; these kernels fuse the count into the bitmap pass and read it
+    once, so they move LE/8 fewer)."""
     LK = cfg.L * cfg.K
-    return 4 * LK + 12 * LK + 4 * (cfg.E + 1) + 2 * (cfg.L * cfg.E // 8)
+    return 4 * LK + 12 * LK + 4 * (cfg.E + 1) + 3 * (cfg.L * cfg.E // 8)
 
 
 def identity_bytes(cfg):
-    """Algorithmic bytes of one identity gather/combine pass: every source
-    row read once, every output row written once, token_index_map,
-    expert_token_indices and gates read once."""
+    """Algorithmic bytes of one identity gather/combine pass: every routed
+    row read (LK rows; the K copies of a token's row are the same row, and
+    only the first reaches DRAM), every output row written once, D1, D4 and
+    the gates read."""
     s = cfg.elem_bytes
-    return 2 * cfg.L * cfg.d * s + 12 * cfg.L * cfg.K
+    return (cfg.L * cfg.K + cfg.L) * cfg.d * s + 12 * cfg.L * cfg.K
 
 
 # ------------------------------------------------------------------ clocks

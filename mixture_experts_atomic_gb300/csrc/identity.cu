@@ -26,6 +26,7 @@ namespace {
 constexpr int kWin = 8;           // tokens per CTA
 constexpr int kThreads = 256;
 constexpr int kChunkBytes = 1024;  // bytes of one routed row per column chunk
+constexpr int kStages = 2;         // column chunks in flight per CTA
 constexpr int kPieces = kChunkBytes / 16;
 
 template <typename T>
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
                                                                     int64_t LK) {
   constexpr int V = Vec<T>::N;                 // elements per 16-byte piece
   constexpr int CH = kChunkBytes / sizeof(T);  // columns per chunk
-  extern __shared__ __align__(16) uint8_t stage[];  // [2][n][kChunkBytes]
+  extern __shared__ __align__(16) uint8_t stage[];  // [kStages][n][kChunkBytes]
   __shared__ int32_t pos_in[kWin * kMaxK], pos_s[kWin * kMaxK], tok_s[kWin * kMaxK];
   __shared__ float g_in[kWin * kMaxK], g_s[kWin * kMaxK];
   __shared__ int32_t slot_of[kWin][kMaxK];
@@ -114,10 +115,10 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
 
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
   const int nchunks = (d + CH - 1) / CH;
-  // gather: the n routed rows of chunk c, in expert-major order, into buffer c & 1
+  // gather: the n routed rows of chunk c, in expert-major order, into buffer c % kStages
   auto gather = [&](int c) {
     const int col0 = c * CH;
-    const uint32_t buf = sbase + (c & 1) * n * kChunkBytes;
+    const uint32_t buf = sbase + (c % kStages) * n * kChunkBytes;
     for (int pc = tid; pc < n * kPieces; pc += kThreads) {
       const int i = pc / kPieces, off = pc % kPieces;
       const int j = tok_s[i];
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
   // combine: each output piece sums its row's staged slots with their gates
   auto combine = [&](int c) {
     const int col0 = c * CH;
-    const uint8_t* buf = stage + (c & 1) * n * kChunkBytes;
+    const uint8_t* buf = stage + (c % kStages) * n * kChunkBytes;
     for (int pc = tid; pc < kWin * kPieces; pc += kThreads) {
       const int j = pc / kPieces, off = pc % kPieces;
       const int col = col0 + off * V;
@@ -147,18 +148,24 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
       Vec<T>::store(dst + (t0 + j) * d + col, acc);
     }
   };
-  gather(0);
-  for (int c = 0; c < nchunks; ++c) {
-    if (c + 1 < nchunks) {
-      gather(c + 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();
-    combine(c);
-    __syncthreads();  // buffer c & 1 is refilled by gather(c + 2)
+  // kStages chunks in flight while chunk c is awaited; one commit group per
+  // chunk (empty past the end)
+#pragma unroll
+  for (int c = 0; c < kStages - 1; ++c) {
+    if (c < nchunks) gather(c);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
   }
+  for (int c = 0; c < nchunks; ++c) {
+    // chunk c + kStages - 1 goes into the buffer chunk c - 1 used (combined
+    // before the trailing barrier of the previous iteration)
+    if (c + kStages - 1 < nchunks) gather(c + kStages - 1);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+    __syncthreads();  // chunk c landed for every thread
+    combine(c);
+    __syncthreads();  // chunk c's buffer may be refilled
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // Gate gradients of the identity expert: dg[t,k] = <dY[t], x[t]> for every
@@ -206,16 +213,16 @@ moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src
   if (s.L == 0) return MOEBLAZE_OK;
   const int64_t LK = s.L * s.K;
   const dim3 grid((unsigned)((s.L + kWin - 1) / kWin));
-  const size_t smem = 2 * (size_t)kWin * s.K * kChunkBytes;
+  const size_t smem = kStages * (size_t)kWin * s.K * kChunkBytes;
   if (s.dtype == MOEBLAZE_BF16) {
     auto k = identity_combine_kernel<__nv_bfloat16>;
-    if (smem > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), disp.expert_token_indices,
                                     disp.token_index_map, gates, reinterpret_cast<__nv_bfloat16*>(dst), s.L, s.d,
                                     s.K, LK);
   } else {
     auto k = identity_combine_kernel<float>;
-    if (smem > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const float*>(src), disp.expert_token_indices,
                                     disp.token_index_map, gates, reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK);
   }

@@ -66,9 +66,9 @@ def test_fp32_layer_other_shapes():
     full_compare(cfg, _routed_inputs(cfg, 6))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_identity_layer_small(dtype):
-    cfg = I.MoEConfig("t_identity", 1500, 1024 if dtype == "bf16" else 512, 0, 16, 4, "identity", dtype, 13, "zipf")
+@pytest.mark.parametrize("dtype,K", [("bf16", 4), ("f32", 4), ("bf16", 3), ("bf16", 8)])
+def test_identity_layer_small(dtype, K):
+    cfg = I.MoEConfig("t_identity", 1500, 1024 if dtype == "bf16" else 512, 0, 16, K, "identity", dtype, 13, "zipf")
     inp = I.make_inputs(cfg, "cpu")
     full_compare(cfg, inp)
 
