@@ -10,9 +10,9 @@
 //                      (expert, chunk) popcount.
 //   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
 //                      counts -> chunk bases and n_e.
-//   K2b offsets_kernel one CTA: expert_token_offsets (the scan of n_e), the
-//                      padded row offsets, the GEMM tile table and the
-//                      experts' descending-load order.
+//   K2b offsets_kernel expert_token_offsets (the scan of n_e), the padded
+//                      row offsets, the GEMM tile table (split over a few
+//                      CTAs) and the experts' descending-load order.
 //   K3 scatter_kernel  one CTA per chunk.  A shuffle scan over each expert's
 //                      32 popcounts gives every word its first position;
 //                      each token then places its K slots:
@@ -183,17 +183,18 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
   if (threadIdx.x == 0) n_e[e] = total;
 }
 
-// K2b: one CTA.  expert_token_offsets (exclusive scan of n_e) and the GEMM
-// metadata: padded row offsets, tile count, tile -> expert table and the
-// experts in descending order of load.  Computed once here instead of in
-// every chunk's CTA.
+// K2b: expert_token_offsets (exclusive scan of n_e) and the GEMM metadata:
+// padded row offsets, tile count, tile -> expert table and the experts in
+// descending order of load.  Every CTA scans the (at most 512) counts; the
+// tile table is split over the CTAs (binary search in the padded offsets),
+// CTA 0 writes the rest.  Computed once instead of in every chunk's CTA.
 __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __restrict__ n_e, int E,
                                                            int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles) {
   __shared__ int32_t off[kMaxE + 1];
   __shared__ int32_t poff[kMaxE + 1];
   __shared__ int wsum[32];
   __shared__ int total;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   constexpr int kEPT = kMaxE / kThreads;
   int carry = 0, pcarry = 0;
 #pragma unroll
@@ -214,18 +215,35 @@ __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __rest
   if (tid == 0) {
     off[E] = carry;
     poff[E] = pcarry;
-    *meta.num_m_tiles = pcarry / kTileM;
-    *meta.padded_rows = pcarry;
   }
   __syncthreads();
+  // tile table: tile m of this CTA's range -> the expert whose padded rows hold it
+  const int64_t ntiles = pcarry / kTileM;
+  const int64_t per = (max_tiles + gridDim.x - 1) / gridDim.x;
+  const int64_t m0 = (int64_t)blockIdx.x * per, m1 = min(max_tiles, m0 + per);
+  for (int64_t m = m0 + tid; m < m1; m += kThreads) {
+    int32_t v = -1;
+    if (m < ntiles) {
+      const int64_t row = m * kTileM;
+      int lo = 0, hi = E - 1;  // last e with poff[e] <= row (non-empty segments only own rows)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (poff[mid] <= row) lo = mid;
+        else hi = mid - 1;
+      }
+      v = lo;
+    }
+    meta.tile_expert[m] = v;
+  }
+  if (blockIdx.x != 0) return;
+  if (tid == 0) {
+    *meta.num_m_tiles = (int32_t)ntiles;
+    *meta.padded_rows = pcarry;
+  }
   for (int e = tid; e <= E; e += kThreads) {
     D2[e] = off[e];
     meta.pad_off[e] = poff[e];
   }
-  // tile table: one warp per expert writes its range of 128-row tiles
-  for (int e = warp; e < E; e += kThreads / 32)
-    for (int32_t m = poff[e] / kTileM + lane; m < poff[e + 1] / kTileM; m += 32) meta.tile_expert[m] = e;
-  for (int64_t m = poff[E] / kTileM + tid; m < max_tiles; m += kThreads) meta.tile_expert[m] = -1;
   // descending load, equal loads by index
   for (int e = tid; e < E; e += kThreads) {
     const int32_t me = off[e + 1] - off[e];
@@ -401,7 +419,12 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  offsets_kernel<<<1, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt);
+  {
+    int64_t g = (mt + 4095) / 4096;  // about 16 tile entries per thread
+    if (g > sm_count()) g = sm_count();
+    if (g < 1) g = 1;
+    offsets_kernel<<<(unsigned)g, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt);
+  }
   MB_CUDA(cudaGetLastError());
   count_launch();
   const size_t sm3 = (size_t)E * kRow * 4 + (size_t)E * sizeof(int32_t) + (size_t)E * kRow * 2;
