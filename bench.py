@@ -196,6 +196,21 @@ def cpu_cores():
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's step time: every rank runs its own replica on its
+    own batch, so the job advances at the pace of the slowest."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput: every rank's tokens in the slowest rank's step."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def flush_l2(buf):
     buf.add_(1)
 
@@ -273,12 +288,8 @@ def run_ours(args, rank, world, local_rank):
     stages["dispatch"] = statistics.mean(disp_ms)
     stages["forward"] = statistics.mean(fwd_ms)
     stages["backward"] = statistics.mean(bwd_ms)
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * cfg.L / (ms * 1e-3)
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    value = job_tokens_per_s(world, cfg.L, ms)
 
     pk, src = peaks()
     # a kernel timed inside a step that ran power-capped is held to the
@@ -411,12 +422,8 @@ def run_e2e(args, cfg, layer, inp, dev, world):
     run(args.steps)
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * cfg.L / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    return {"value": job_tokens_per_s(world, cfg.L, ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "copies": "overlapped with the neighbouring steps' compute"}
 
 
