@@ -14,8 +14,10 @@
 //               fp32 accumulators in TMEM, two accumulator buffers so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 5-8   epilogue: tcgen05.ld of the accumulator rows and the fused
-//               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward,
-//               plain stores).
+//               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward
+//               with the gate gradients, plain stores).
+// The CTAs claim tiles from a per-launch counter (weight-gradient tiles in
+// descending order of expert load), so skewed expert loads balance.
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
 // [pad_off[e], pad_off[e+1]), 128-row aligned, so every 128-row M tile
@@ -63,7 +65,6 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 256;
 // use, and passes the ids to its MMA and epilogue warps through a queue of
 // TQ slots in shared memory.
 constexpr int TQ = 8;
-constexpr bool kDynamicTiles = true;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -456,10 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     return id;
   };
   // tile of queue position j >= 2 (positions 0 and 1 are blockIdx.x and blockIdx.x + gridDim.x)
-  auto claim = [&](int j) -> long long {
-    if constexpr (kDynamicTiles) return 2ll * gridDim.x + (long long)atomicAdd(p.sched, 1ull);
-    else return (long long)blockIdx.x + (long long)j * gridDim.x;
-  };
+  auto claim = [&]() -> long long { return 2ll * gridDim.x + (long long)atomicAdd(p.sched, 1ull); };
 
   if (warp < PRODUCER_WARPS) {
     // ================================================================ producer
@@ -512,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       ok = tile >= 0;
       for (int j = 0; ok && tile < total; ++j) {
         long long pending = 0;
-        if (pt == 0) pending = claim(j + 2);  // consumed after this tile's loads are issued
+        if (pt == 0) pending = claim();  // for position j + 2, posted after this tile's loads are issued
         const long long ntile = take(j + 1);
         if (ntile < 0) {
           ok = false;
