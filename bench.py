@@ -59,14 +59,24 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def code_sha256(path):
+    """sha256 of a CUDA/C++ source with its comments and whitespace removed,
+    so that a change of wording alone keeps a capture valid."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
 def traffic_per_launch(workload, stage, source):
     """DRAM bytes (read + write) per launch of one kernel (`stage`) on one
     workload, from a committed ncu summary under profiles/ that names the
-    kernel's source file and its sha256 at capture; None when there is no
-    such summary or the source has changed since."""
-    import hashlib
-    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
-    key = ["traffic-per-launch", f"workload={workload}", f"file={source}", f"source-sha256={sha}"]
+    kernel's source file and its code hash at capture (code_sha256); None
+    when there is no such summary or the code has changed since."""
+    sha = code_sha256(os.path.join(ROOT, source))
+    key = ["traffic-per-launch", f"workload={workload}", f"file={source}", f"code-sha256={sha}"]
     for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
         if not name.endswith(".md"):
             continue
