@@ -20,6 +20,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import shutil
 import statistics
 import subprocess
@@ -492,7 +493,7 @@ def run_reference(args, cfg):
             "dtype": "f64", "data": "synthetic (seeded counter-based generator; random-init weights)",
             "config": {"workload": cfg.name, "L": cfg.L, "d": cfg.d, "h": cfg.h, "E": cfg.E, "K": cfg.K,
                        "act": cfg.act},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "machine": platform.machine(),
                              "sample": f"first {ntok} tokens of the workload per step (same d, h, E, K)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -538,6 +539,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, ntok, dt = oracle_sample(cfg)
         out["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                               "machine": platform.machine(),
                                "sample": f"first {ntok} tokens of the workload (same d, h, E, K), "
                                          f"{dt:.1f} s of fp64 CPU work"}
     if rank == 0:
