@@ -3,11 +3,12 @@
 //
 //   K1 bitmap_kernel   one CTA per chunk of 1024 tokens.  Builds the chunk's
 //                      token-expert bitmap in shared memory (bit t%32 of word
-//                      [e][t/32]; every (t,e) bit written once, lanes with the
-//                      same expert elected by match_any so no two lanes touch
-//                      one word), writes it transposed (expert-major, each
-//                      expert's 32 words = one 128-byte line) and the per
-//                      (expert, chunk) popcount.
+//                      [e][t/32]; every (t,e) bit written once: the lanes of a
+//                      warp with the same expert are found by bit-plane
+//                      ballots and only the lowest one writes, so no two
+//                      lanes touch one word), writes it transposed
+//                      (expert-major, each expert's 32 words = one 128-byte
+//                      line) and the per (expert, chunk) popcount.
 //   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
 //                      counts -> chunk bases and n_e.
 //   K2b offsets_kernel expert_token_offsets (the scan of n_e), the padded
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
   const int64_t wpe = C * kChunkWords;
+  const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest expert id
 
   int e_k[kPasses][kMaxK];
 #pragma unroll
@@ -99,7 +101,10 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   __syncthreads();
 
   // Word [e][w] collects the lanes of this warp routed to e.  Within one
-  // slot k the lanes sharing an expert are grouped by match_any and only the
+  // slot k each lane finds the lanes that share its expert: one ballot per
+  // bit of the id, keeping the lanes whose bit agrees with its own (and a
+  // first ballot dropping lanes with no valid id).  This is the mask
+  // match_any would give, from ballots, which cost less to issue.  Only the
   // group's lowest lane writes; distinct groups write distinct words.
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
@@ -108,7 +113,12 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
     for (int k = 0; k < kMaxK; ++k) {
       if (k >= K) break;  // K is the same for every lane
       const int e = e_k[j][k];
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      unsigned grp = __ballot_sync(0xffffffffu, e >= 0);
+      for (int b = 0; b < nbits; ++b) {
+        const bool bit = (e >> b) & 1;
+        const unsigned plane = __ballot_sync(0xffffffffu, bit);
+        grp &= bit ? plane : ~plane;
+      }
       if (e >= 0 && lane == __ffs(grp) - 1) words[e * kRow + w] |= grp;
       __syncwarp();
     }
@@ -186,12 +196,14 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
 // K2b: expert_token_offsets (exclusive scan of n_e) and the GEMM metadata:
 // padded row offsets, tile count, tile -> expert table and the experts in
 // descending order of load.  Every CTA scans the (at most 512) counts; the
-// tile table is split over the CTAs (binary search in the padded offsets),
-// CTA 0 writes the rest.  Computed once instead of in every chunk's CTA.
+// tile table (binary search in the padded offsets) and the load ranks are
+// split over the CTAs, and CTA 0 writes the offsets.  Computed once instead
+// of in every chunk's CTA.
 __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __restrict__ n_e, int E,
                                                            int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles) {
   __shared__ int32_t off[kMaxE + 1];
   __shared__ int32_t poff[kMaxE + 1];
+  __shared__ int32_t cnt[kMaxE];
   __shared__ int wsum[32];
   __shared__ int total;
   const int tid = threadIdx.x;
@@ -235,6 +247,23 @@ __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __rest
     }
     meta.tile_expert[m] = v;
   }
+  // descending load, equal loads by index: the rank of expert e is the
+  // number of experts j with n_j > n_e, or n_j == n_e and j < e.  One warp
+  // per expert, the experts spread over all CTAs.
+  for (int e = tid; e < E; e += kThreads) cnt[e] = off[e + 1] - off[e];
+  __syncthreads();
+  const int lane = tid & 31, nwarps = kThreads / 32;
+  for (int e = blockIdx.x * nwarps + (tid >> 5); e < E; e += gridDim.x * nwarps) {
+    const int32_t me = cnt[e];
+    int rank = 0;
+    for (int j = lane; j < E; j += 32) {
+      const int32_t nj = cnt[j];
+      rank += (nj > me) || (nj == me && j < e);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (lane == 0) meta.order[rank] = e;
+  }
   if (blockIdx.x != 0) return;
   if (tid == 0) {
     *meta.num_m_tiles = (int32_t)ntiles;
@@ -243,16 +272,6 @@ __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __rest
   for (int e = tid; e <= E; e += kThreads) {
     D2[e] = off[e];
     meta.pad_off[e] = poff[e];
-  }
-  // descending load, equal loads by index
-  for (int e = tid; e < E; e += kThreads) {
-    const int32_t me = off[e + 1] - off[e];
-    int rank = 0;
-    for (int j = 0; j < E; ++j) {
-      const int32_t nj = off[j + 1] - off[j];
-      rank += (nj > me) || (nj == me && j < e);
-    }
-    meta.order[rank] = e;
   }
 }
 
@@ -420,7 +439,7 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   MB_CUDA(cudaGetLastError());
   count_launch();
   {
-    int64_t g = (mt + 4095) / 4096;  // about 16 tile entries per thread
+    int64_t g = (mt + 1023) / 1024;  // about 4 tile entries (binary searches) per thread
     if (g > sm_count()) g = sm_count();
     if (g < 1) g = 1;
     offsets_kernel<<<(unsigned)g, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt);

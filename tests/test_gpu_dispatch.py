@@ -36,13 +36,18 @@ def test_dispatch_matches_oracle(L, E, K, seed, one):
     assert layer.device_error() == 0
 
 
-def test_dispatch_every_token_on_one_expert():
-    L, E = 5000, 6
-    ids = torch.full((L, 1), 4, dtype=torch.int32)
+@pytest.mark.parametrize("L,E,e", [(5000, 6, 4), (1057, 8, 7), (33, 16, 15), (1, 256, 255), (2081, 2, 1)])
+def test_dispatch_every_token_on_one_expert(L, E, e):
+    """Every token on expert e.  With e = E-1 a power of two minus one, the
+    expert id has every low bit set, the same bits as the lanes past the last
+    token of a ragged chunk: those lanes must not join the expert's group."""
+    ids = torch.full((L, 1), e, dtype=torch.int32)
     layer = _layer(L, E, 1)
     layer.dispatch(ids.cuda())
     D1, D2, _, _ = check_dispatch(layer, ids, E)
-    assert np.array_equal(D1, np.arange(L)) and D2.tolist() == [0, 0, 0, 0, 0, L, L]
+    assert np.array_equal(D1, np.arange(L))
+    assert D2.tolist() == [0] * (e + 1) + [L] * (E - e)
+    assert layer.device_error() == 0
 
 
 def test_dispatch_empty_input():
