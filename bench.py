@@ -114,6 +114,45 @@ def dispatch_bytes(cfg):
     return 4 * LK + 12 * LK + 4 * (cfg.E + 1) + 3 * (cfg.L * cfg.E // 8)
 
 
+def materialising_bytes(cfg):
+    """Activation bytes a materialising MoE layer keeps from the forward for
+    the backward (MoEBlaze summary page, "问题与动机": the routing buffer is
+    O(L*K*d), the first MLP's output O(L*h) per active expert, and SwiGLU adds
+    several point-wise tensors).  Counted here as the routed copy of x
+    (L*K*d) plus, per routed row, a, b, sigma(a), SiLU(a) and H (5*h) for
+    SwiGLU or a and SiLU(a) (2*h) for SiLU; the identity expert keeps the
+    routed buffer alone.  Elements of the layer dtype."""
+    LK, s = cfg.L * cfg.K, cfg.elem_bytes
+    per_row = {"swiglu": 5 * cfg.h, "silu": 2 * cfg.h, "identity": 0}[cfg.act]
+    return LK * cfg.d * s + LK * per_row * s
+
+
+def memory_report(cfg, layer, step_alloc_peak):
+    """What this layer keeps from the forward for the backward (the saved A
+    and B, padded expert-major, and the index structures), its scratch, and
+    the same retained figure for a materialising layer.  step_alloc_peak:
+    bytes the torch allocator handed out during one step on top of what was
+    already allocated."""
+    from mixture_experts_atomic_gb300 import binding as B
+    sh = layer.shape
+
+    def nb(t):
+        return t.numel() * t.element_size()
+
+    saved = B.moeblaze_saved_bytes(sh)
+    d = layer.disp
+    index = sum(nb(t) for t in (d.expert_token_indices, d.expert_token_offsets, d.token_expert_indices,
+                                d.token_index_map, d.meta))
+    mat = materialising_bytes(cfg)
+    return {"retained_fwd_to_bwd_bytes": saved + index, "saved_activation_bytes": saved, "index_bytes": index,
+            "scratch_bytes": {"dispatch": B.moeblaze_dispatch_workspace_bytes(sh),
+                              "forward": B.moeblaze_forward_workspace_bytes(sh),
+                              "backward": B.moeblaze_backward_workspace_bytes(sh)},
+            "step_alloc_peak_bytes": int(step_alloc_peak),
+            "materialising_retained_bytes": mat,
+            "materialising_over_retained": mat / (saved + index)}
+
+
 def identity_bytes(cfg):
     """Algorithmic bytes of one identity gather/combine pass: every routed
     row read (LK rows; the K copies of a token's row are the same row, and
@@ -261,6 +300,13 @@ def run_ours(args, rank, world, local_rank):
         one_step()
     torch.cuda.synchronize()
     assert layer.device_error() == 0, "device error during warm-up"
+    # one more untimed step, watched by the torch allocator: every buffer of
+    # the layer exists before the step, so this is what a step allocates
+    alloc0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    one_step()
+    torch.cuda.synchronize()
+    step_alloc_peak = torch.cuda.max_memory_allocated(dev) - alloc0
 
     recs = [{"e0": torch.cuda.Event(enable_timing=True), "e1": torch.cuda.Event(enable_timing=True),
              "e2": torch.cuda.Event(enable_timing=True), "e3": torch.cuda.Event(enable_timing=True),
@@ -340,6 +386,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / max(1, args.steps),
         "clocks": clk,
+        "activation_memory": memory_report(cfg, layer, step_alloc_peak),
     }
     if cfg.router in ("softmax", "softmax_bias"):
         out["router"] = run_router(cfg, inp, dev, flush, pk)
