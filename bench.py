@@ -25,6 +25,7 @@ import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -169,17 +170,24 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, keep: str | None = None):
+        """keep: a path to keep the raw samples at (CSV); by default they go
+        to a temporary file that is removed once summarised."""
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        self.keep = keep
+        self.path = None
 
     def start(self):
         exe = shutil.which("nvidia-smi")
         if not exe:
             return
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
-        self.f = open(self.path, "w")
+        if self.keep:
+            os.makedirs(os.path.dirname(os.path.abspath(self.keep)), exist_ok=True)
+            self.f = open(self.keep, "w")
+        else:
+            self.f = tempfile.NamedTemporaryFile("w", prefix=f"clocks_rank{self.dev}_", suffix=".csv", delete=False)
+        self.path = self.f.name
         self.proc = subprocess.Popen([exe, "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
                                      stderr=subprocess.DEVNULL)
@@ -196,7 +204,11 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.read().splitlines()
+        if not self.keep:
+            os.unlink(self.path)
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < len(self.FIELDS):
                 continue
@@ -311,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     recs = [{"e0": torch.cuda.Event(enable_timing=True), "e1": torch.cuda.Event(enable_timing=True),
              "e2": torch.cuda.Event(enable_timing=True), "e3": torch.cuda.Event(enable_timing=True),
              "fw": B.StageEvents(nf), "bw": B.StageEvents(nbk)} for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank, args.clock_log.format(rank=rank) if args.clock_log else None)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -555,6 +567,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload with this many tokens instead (smaller profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the raw nvidia-smi clock samples of the timed region at this path ({rank} is replaced)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["dispatch"], default=None,
                     help="time only the dispatch build of the workload (allocates only its routing and index buffers)")
