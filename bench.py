@@ -189,13 +189,17 @@ class ClockSampler:
             self.f = tempfile.NamedTemporaryFile("w", prefix=f"clocks_rank{self.dev}_", suffix=".csv", delete=False)
         self.path = self.f.name
         self.proc = subprocess.Popen([exe, "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
-                                      "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                                      stderr=subprocess.DEVNULL)
+        # the timed region starts once the sampler has written its first line
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.03)  # one more sampling interval
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -488,13 +492,16 @@ def run_e2e(args, cfg, layer, inp, dev, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # at most 20 steps: on the largest layers each step moves ~100 GB over the host link
+    n = min(args.steps, 20)
     e0.record()
-    run(args.steps)
+    run(n)
     e1.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
     return {"value": job_tokens_per_s(world, cfg.L, ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "copies": "overlapped with the neighbouring steps' compute"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
+            "copies": "overlapped with the neighbouring steps' compute"}
 
 
 def run_dispatch_only(args, local_rank):
@@ -534,7 +541,10 @@ def run_reference(args, cfg):
     """The CPU oracle as the reference arm: each step runs it on a bounded
     sample of the workload's tokens (same shapes otherwise)."""
     import oracle.moe_oracle as O
-    tps, ntok, dt = oracle_sample(cfg, target_s=6.0)
+    # each step's sample is sized so that all warm-up and timed steps take
+    # about 150 s together (at most 6 s a step)
+    per_step = max(0.1, min(6.0, 150.0 / (args.steps + args.warmup)))
+    tps, ntok, dt = oracle_sample(cfg, target_s=per_step)
     sub = cfg.scaled(L=ntok)
     inp = I.make_inputs(sub, "cpu")
     times = []
@@ -560,7 +570,7 @@ def run_reference(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=1, help="workload index (0..4); default: the SiLU bf16 layer")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
