@@ -189,6 +189,78 @@ def make_shape(L, d, h, E, K, dtype, act) -> Shape:
     return Shape(int(L), int(d), int(h), int(E), int(K), dt, a)
 
 
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def _args(*specs):
+    """Check tensor arguments before their pointers go to C.  Each spec is
+    (tensor, name, shape, dtype, optional); a tensor of an empty shape may
+    be None, as the library takes NULL there.  Every tensor must have exactly
+    that shape and dtype and a dense row-major layout (checked for all of
+    them first), and live on the current CUDA device.  The C library sees
+    only pointers, so a wrong tensor would otherwise be read or written out
+    of bounds on the GPU."""
+    for t, name, shape, dtype, optional in specs:
+        if t is None:
+            # an empty buffer (no tokens) may be passed as NULL
+            if optional or any(int(v) == 0 for v in shape):
+                continue
+            raise ValueError(f"{name}: a tensor is required")
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+        want = tuple(int(v) for v in shape)
+        if tuple(t.shape) != want:
+            raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {want}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous (row-major)")
+    _on_device(*[(spec[0], spec[1]) for spec in specs if spec[0] is not None])
+
+
+def _on_device(*named):
+    for t, name in named:
+        if not t.is_cuda:
+            raise ValueError(f"{name}: must be a CUDA tensor")
+        if t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+
+
+def _bytes_arg(t, name: str, nbytes: int):
+    """A caller-provided byte buffer: at least nbytes, contiguous, on the current CUDA device."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name}: {t.numel() * t.element_size()} bytes, needs {nbytes}")
+    _on_device((t, name))
+
+
+def _weight_specs(shape: Shape, W1, W2, W3, prefix: str = ""):
+    """Specs of the expert weights the activation uses (the others go to C as NULL)."""
+    if shape.act == IDENTITY:
+        return []
+    dt = _TORCH_DTYPE[shape.dtype]
+    E, d, h = shape.E, shape.d, shape.h
+    specs = [(W1, prefix + "W1", (E, d, h), dt, False), (W3, prefix + "W3", (E, h, d), dt, False)]
+    if shape.act == SWIGLU:
+        specs.append((W2, prefix + "W2", (E, d, h), dt, False))
+    return specs
+
+
+def _used_weights(shape: Shape, W1, W2, W3):
+    if shape.act == IDENTITY:
+        return None, None, None
+    return W1, (W2 if shape.act == SWIGLU else None), W3
+
+
+def _check_dispatch_bufs(shape: Shape, bufs: "DispatchBuffers"):
+    LK = shape.L * shape.K
+    for name in ("expert_token_indices", "token_expert_indices", "token_index_map"):
+        _bytes_arg(getattr(bufs, name), name, 4 * LK)
+    _bytes_arg(bufs.expert_token_offsets, "expert_token_offsets", 4 * (shape.E + 1))
+    _bytes_arg(bufs.meta, "meta", moeblaze_dispatch_meta_bytes(shape))
+
+
 def _check(st: int, where: str):
     if st != OK:
         raise MoEBlazeError(st, where)
@@ -232,9 +304,10 @@ def dispatch_build(shape: Shape, topk_ids: torch.Tensor, bufs: Optional[Dispatch
                    validate: bool = False, stream=None) -> DispatchBuffers:
     """Run the three-step dispatch build; returns the buffers holding the
     index structures (views: [:L*K], [:E+1])."""
-    assert topk_ids.is_cuda and topk_ids.dtype == torch.int32 and topk_ids.is_contiguous()
+    _args((topk_ids, "topk_ids", (shape.L, shape.K), torch.int32, False))
     if bufs is None:
         bufs = alloc_dispatch(shape, topk_ids.device)
+    _check_dispatch_bufs(shape, bufs)
     d = bufs.struct()
     st = moeblaze_dispatch_build(shape, _ptr(topk_ids), d, _ptr(bufs.ws), bufs.ws.numel(), validate, _stream(stream))
     _check(st, "moeblaze_dispatch_build")
@@ -261,6 +334,12 @@ def alloc_layer(shape: Shape, device="cuda") -> LayerBuffers:
 
 
 def forward(shape: Shape, x, gates, disp: DispatchBuffers, W1, W2, W3, y, layer: LayerBuffers, stream=None):
+    dt = _TORCH_DTYPE[shape.dtype]
+    _args((x, "x", (shape.L, shape.d), dt, False), (gates, "gates", (shape.L, shape.K), torch.float32, False),
+          (y, "y", (shape.L, shape.d), dt, False), *_weight_specs(shape, W1, W2, W3))
+    W1, W2, W3 = _used_weights(shape, W1, W2, W3)
+    _check_dispatch_bufs(shape, disp)
+    _bytes_arg(layer.saved, "saved", moeblaze_saved_bytes(shape))
     st = moeblaze_forward(shape, _ptr(x), _ptr(gates), disp.struct(), _ptr(W1), _ptr(W2), _ptr(W3), _ptr(y),
                           _ptr(layer.saved), _ptr(layer.fwd_ws), layer.fwd_ws.numel(), _stream(stream))
     _check(st, "moeblaze_forward")
@@ -269,6 +348,15 @@ def forward(shape: Shape, x, gates, disp: DispatchBuffers, W1, W2, W3, y, layer:
 
 def backward(shape: Shape, dY, x, gates, disp: DispatchBuffers, W1, W2, W3, layer: LayerBuffers, dX, dW1, dW2, dW3,
              dgates=None, stream=None):
+    dt = _TORCH_DTYPE[shape.dtype]
+    _args((dY, "dY", (shape.L, shape.d), dt, False), (x, "x", (shape.L, shape.d), dt, False),
+          (gates, "gates", (shape.L, shape.K), torch.float32, False), (dX, "dX", (shape.L, shape.d), dt, False),
+          (dgates, "dgates", (shape.L, shape.K), torch.float32, True),
+          *_weight_specs(shape, W1, W2, W3), *_weight_specs(shape, dW1, dW2, dW3, prefix="d"))
+    W1, W2, W3 = _used_weights(shape, W1, W2, W3)
+    dW1, dW2, dW3 = _used_weights(shape, dW1, dW2, dW3)
+    _check_dispatch_bufs(shape, disp)
+    _bytes_arg(layer.saved, "saved", moeblaze_saved_bytes(shape))
     st = moeblaze_backward(shape, _ptr(dY), _ptr(x), _ptr(gates), disp.struct(), _ptr(W1), _ptr(W2), _ptr(W3),
                            _ptr(layer.saved), _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dW3), _ptr(dgates),
                            _ptr(layer.bwd_ws), layer.bwd_ws.numel(), _stream(stream))
@@ -300,6 +388,10 @@ class StageEvents:
 
 def router_forward(shape: Shape, x, Wr, bias, topk_ids, gates, stream=None):
     """Token-choice top-K softmax router: fills topk_ids (L,K) int32 and gates (L,K) fp32."""
+    _args((x, "x", (shape.L, shape.d), _TORCH_DTYPE[shape.dtype], False),
+          (Wr, "Wr", (shape.d, shape.E), torch.float32, False), (bias, "bias", (shape.E,), torch.float32, True),
+          (topk_ids, "topk_ids", (shape.L, shape.K), torch.int32, False),
+          (gates, "gates", (shape.L, shape.K), torch.float32, False))
     st = moeblaze_router_forward(shape, _ptr(x), _ptr(Wr), _ptr(bias), _ptr(topk_ids), _ptr(gates), _stream(stream))
     _check(st, "moeblaze_router_forward")
 
@@ -308,9 +400,18 @@ def router_backward(shape: Shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx
     """Router gradients from the gate gradients: fills dWr (d,E) fp32, dbias (E) fp32 and dx (L,d) (dbias and dx
     may be None).  `ws` is a device byte tensor of moeblaze_router_backward_workspace_bytes(shape) bytes
     (allocated here when None)."""
+    _args((x, "x", (shape.L, shape.d), _TORCH_DTYPE[shape.dtype], False),
+          (Wr, "Wr", (shape.d, shape.E), torch.float32, False),
+          (topk_ids, "topk_ids", (shape.L, shape.K), torch.int32, False),
+          (gates, "gates", (shape.L, shape.K), torch.float32, False),
+          (dgates, "dgates", (shape.L, shape.K), torch.float32, False),
+          (dWr, "dWr", (shape.d, shape.E), torch.float32, False),
+          (dbias, "dbias", (shape.E,), torch.float32, True),
+          (dx, "dx", (shape.L, shape.d), _TORCH_DTYPE[shape.dtype], True))
     n = moeblaze_router_backward_workspace_bytes(shape)
     if ws is None:
         ws = _bytes(n, Wr.device)
+    _bytes_arg(ws, "ws", n)
     st = moeblaze_router_backward(shape, _ptr(x), _ptr(Wr), _ptr(topk_ids), _ptr(gates), _ptr(dgates), _ptr(dWr),
                                   _ptr(dbias), _ptr(dx), _ptr(ws), n, _stream(stream))
     _check(st, "moeblaze_router_backward")

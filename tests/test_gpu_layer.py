@@ -128,3 +128,28 @@ def test_step_pipeline_matches_plain_steps():
     assert layer.device_error() == 0
     for (y, dx), (wy, wdx) in zip(outs, want):
         assert torch.equal(y, wy) and torch.equal(dx, wdx)
+
+
+def test_malformed_arguments_are_refused_before_launch():
+    """A CUDA tensor of the wrong shape, dtype or layout is refused by the
+    binding before any kernel runs, and the layer stays usable."""
+    from mixture_experts_atomic_gb300 import binding as B
+    from mixture_experts_atomic_gb300.layer import MoELayer
+    cfg = I.MoEConfig("t_args", 300, 128, 128, 4, 2, "silu", "bf16", 3, "softmax")
+    inp = {k: v.cuda() for k, v in I.make_inputs(cfg, "cpu").items() if v is not None}
+    layer = MoELayer.for_config(cfg, "cuda")
+    layer.dispatch(inp["ids"])
+    torch.cuda.synchronize()
+    n0 = B.moeblaze_kernel_launches()
+    with pytest.raises(ValueError, match="x: shape"):
+        layer.forward(inp["x"][:, :64].contiguous(), inp["gates"], inp["W1"], None, inp["W3"])
+    with pytest.raises(ValueError, match="gates: dtype"):
+        layer.forward(inp["x"], inp["gates"].double(), inp["W1"], None, inp["W3"])
+    with pytest.raises(ValueError, match="W3: must be contiguous"):
+        layer.forward(inp["x"], inp["gates"], inp["W1"], None, inp["W3"].transpose(1, 2).contiguous().transpose(1, 2))
+    with pytest.raises(ValueError, match="topk_ids: dtype"):
+        layer.dispatch(inp["ids"].long())
+    assert B.moeblaze_kernel_launches() == n0
+    layer.step(inp)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
