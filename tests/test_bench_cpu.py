@@ -41,3 +41,55 @@ def test_library_arm_needs_a_gpu():
     r = _run(["--config", "0", "--steps", "1"], env=env)
     assert r.returncode != 0
     assert not any(ln.startswith("{") for ln in r.stdout.splitlines())
+
+
+def _tree(tmp_path, source, profile):
+    (tmp_path / "profiles").mkdir(parents=True)
+    (tmp_path / "k.cu").write_text(source)
+    (tmp_path / "profiles" / "p.md").write_text(profile)
+    return tmp_path
+
+
+def test_code_hash_ignores_comments_and_whitespace(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    a.write_text("int f(int x) {  // doubles\n  return 2 * x;\n}\n")
+    b.write_text("/* a note */ int f(int x)\n{\n    return 2 * x;   // same code\n}\n")
+    assert bench.code_sha256(str(a)) == bench.code_sha256(str(b))
+    b.write_text("int f(int x) { return 3 * x; }\n")
+    assert bench.code_sha256(str(a)) != bench.code_sha256(str(b))
+
+
+def test_traffic_lookup_follows_the_code(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from a committed ncu summary only
+    while the kernel source still hashes to the value recorded with it."""
+    import bench
+    src = "__global__ void k() {}\n"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "k.cu").write_text(src)
+    sha = bench.code_sha256(str(tmp_path / "k.cu"))
+    _tree(tmp_path / "t", src, f"notes\n\ntraffic-per-launch workload=w file=k.cu code-sha256={sha}\nup 123\ndown 456\n\nmore\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "t"))
+    assert bench.traffic_per_launch("w", "up", "k.cu") == 123
+    assert bench.traffic_per_launch("w", "down", "k.cu") == 456
+    assert bench.traffic_per_launch("w", "dx", "k.cu") is None
+    assert bench.traffic_per_launch("other", "up", "k.cu") is None
+    # a change of comments keeps the figures, a change of code drops them
+    (tmp_path / "t" / "k.cu").write_text("// the kernel\n" + src)
+    assert bench.traffic_per_launch("w", "up", "k.cu") == 123
+    (tmp_path / "t" / "k.cu").write_text("__global__ void k() { return; }\n")
+    assert bench.traffic_per_launch("w", "up", "k.cu") is None
+
+
+def test_committed_traffic_figures_match_the_sources():
+    """Each committed traffic block names a source whose current code hash it
+    was captured on (a stale block would silently give null traffic)."""
+    import bench
+    for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+        for ln in open(os.path.join(ROOT, "profiles", name)).read().splitlines():
+            g = ln.split()
+            if g and g[0] == "traffic-per-launch":
+                fields = dict(x.split("=", 1) for x in g[1:])
+                assert bench.code_sha256(os.path.join(ROOT, fields["file"])) == fields["code-sha256"], \
+                    f"{name}: the kernel changed since this capture; recapture it or drop the block ({ln})"
