@@ -1,7 +1,7 @@
 // extern "C" entry points of the moeblaze library (declared in
 // include/moeblaze.h): argument validation, scratch carving and the order of
 // the stages; every stage runs in the kernels of dispatch.cu, identity.cu,
-// simt.cu and gemm_tc.cu.
+// simt.cu, gemm_tc.cu and router.cu.
 #include <atomic>
 #include <cstring>
 
