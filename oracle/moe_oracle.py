@@ -45,6 +45,7 @@ PINNED = {
     "forward_rows / backward_rows / weight_grad_slices": "agree with forward/backward on every row and column at small sizes",
     "router": "hand-worked golden case (ties, bias), K = E equals the full softmax, brute force over all K-subsets, shift invariance",
     "router_backward": "central finite differences in Wr, x and the bias, torch.autograd of the softmax over the selected logits",
+    "rel_err": "hand-worked cases (negative and all-zero references, NaN and inf in the result) and planted variants of the rule",
 }
 
 

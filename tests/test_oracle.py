@@ -461,3 +461,76 @@ def test_router_pins_catch_planted_mistakes():
     ids, g, lg = O.router(np.array([gd["x0"]], dtype=np.float64), np.array(gd["Wr"], dtype=np.float64).reshape(2, 4), None, 2)
     full = np.exp(lg[0] - lg[0].max()); full /= full.sum()
     assert abs(full[ids[0]].sum() - 1.0) > 1e-3 and abs(g[0].sum() - 1.0) < 1e-15
+
+
+# ---------------------------------------------------------------- the parity checker
+# Every GPU parity test reduces to rel_err(got, ref) <= tol, the tolerance rule
+# max|gpu - ref| / max|ref|.  Its cases are worked by hand here.
+
+# (got, ref, expected value): a value None means "must not compare <= any tol"
+_REL_ERR_CASES = [
+    # |got - ref| = (0.25, 0.5, 0); max|ref| = 4 (the negative entry) -> 0.125
+    ([1.25, 2.5, -4.0], [1.0, 2.0, -4.0], 0.125),
+    # max|got| = 3 differs from max|ref| = 2: the denominator is the reference's
+    ([-3.0, -1.0], [-2.0, -1.0], 0.5),
+    # the largest deviation is a negative one: max of |.|, not of the signed difference
+    ([0.0, 1.0], [2.0, 1.0], 1.0),
+    # all-zero reference: the absolute deviation itself
+    ([0.0, -0.25], [0.0, 0.0], 0.25),
+    ([0.0, 0.0, 0.0], [0.0, 0.0, 0.0], 0.0),
+    # one large deviation among many small ones: a max, not a mean (mean would give 0.0375)
+    ([1.1, 1.0, 1.0, 1.0], [1.0, 1.0, 1.0, 1.0], 0.1),
+    # a NaN in the GPU result never passes a tolerance
+    ([1.0, float("nan")], [1.0, 1.0], None),
+    # an infinite GPU result never passes either
+    ([float("inf"), 1.0], [1.0, 1.0], None),
+]
+
+
+def _rel_err_cases_hold(fn):
+    for got, ref, want in _REL_ERR_CASES:
+        v = fn(np.array(got), np.array(ref))
+        if want is None:
+            if v <= 1e30:
+                return False
+        elif not abs(v - want) <= 1e-15:
+            return False
+    return True
+
+
+def test_rel_err_hand_worked():
+    assert _rel_err_cases_hold(O.rel_err)
+    # 2-D inputs and bf16 torch tensors (widened exactly before subtracting)
+    got = torch.tensor([[1.0, -2.0], [0.5, 3.0]]).to(torch.bfloat16)
+    ref = np.array([[1.0, -2.0], [0.25, 4.0]])
+    assert O.rel_err(got, ref) == 0.25  # max|.| = 1 (3 vs 4), max|ref| = 4
+
+
+def test_rel_err_pins_catch_planted_variants():
+    """Plausible slips in the checker each break at least one hand-worked case."""
+    a = np.abs
+
+    def den_from_got(g, r):      # denominator max|got|
+        return float(np.max(a(g - r)) / np.max(a(g))) if np.max(a(g)) else float(np.max(a(g - r)))
+
+    def no_abs(g, r):            # max(got - ref) / max(ref)
+        return float(np.max(g - r) / np.max(r)) if np.max(r) else float(np.max(g - r))
+
+    def mean_not_max(g, r):      # mean deviation
+        return float(np.mean(a(g - r)) / np.max(a(r))) if np.max(a(r)) else float(np.mean(a(g - r)))
+
+    def zero_for_zero_ref(g, r):  # 0 whenever the reference is all zero
+        d = np.max(a(r))
+        return float(np.max(a(g - r)) / d) if d else 0.0
+
+    def nan_ignored(g, r):       # nanmax lets a NaN through
+        d = np.nanmax(a(r))
+        n = np.nanmax(a(g - r))
+        return float(n / d) if d else float(n)
+
+    def finite_only(g, r):       # drops non-finite entries before comparing
+        m = np.isfinite(g)
+        return O.rel_err(g[m], r[m])
+
+    for bad in (den_from_got, no_abs, mean_not_max, zero_for_zero_ref, nan_ignored, finite_only):
+        assert not _rel_err_cases_hold(bad), bad.__name__
