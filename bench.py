@@ -145,20 +145,34 @@ def memory_report(cfg, layer, step_alloc_peak):
     index = sum(nb(t) for t in (d.expert_token_indices, d.expert_token_offsets, d.token_expert_indices,
                                 d.token_index_map, d.meta))
     mat = materialising_bytes(cfg)
+    scratch = {"dispatch": B.moeblaze_dispatch_workspace_bytes(sh),
+               "forward": B.moeblaze_forward_workspace_bytes(sh),
+               "backward": B.moeblaze_backward_workspace_bytes(sh)}
+    # what the layer holds at once at its high-water mark: the retained
+    # checkpoint and indices plus the larger pass's scratch (the passes run
+    # one after the other and each frees its scratch for the next)
+    peak = saved + index + max(scratch["forward"], scratch["backward"])
     return {"retained_fwd_to_bwd_bytes": saved + index, "saved_activation_bytes": saved, "index_bytes": index,
-            "scratch_bytes": {"dispatch": B.moeblaze_dispatch_workspace_bytes(sh),
-                              "forward": B.moeblaze_forward_workspace_bytes(sh),
-                              "backward": B.moeblaze_backward_workspace_bytes(sh)},
+            "scratch_bytes": scratch,
+            "peak_activation_bytes": peak,
             "step_alloc_peak_bytes": int(step_alloc_peak),
             "materialising_retained_bytes": mat,
-            "materialising_over_retained": mat / (saved + index)}
+            "materialising_over_retained": mat / (saved + index),
+            "materialising_retained_over_peak": mat / peak}
 
 
 def identity_bytes(cfg):
-    """Algorithmic bytes of one identity gather/combine pass: every routed
-    row read (LK rows; the K copies of a token's row are the same row, and
-    only the first reaches DRAM), every output row written once, D1, D4 and
-    the gates read."""
+    """Bytes one identity gather/combine pass must move: x read once (the K
+    routed copies of a token's row are one row), y written once, and D1, D4
+    and the gates read (12*L*K).  This is the roofline figure."""
+    s = cfg.elem_bytes
+    return 2 * cfg.L * cfg.d * s + 12 * cfg.L * cfg.K
+
+
+def identity_routed_bytes(cfg):
+    """The same pass counted with every routed row read on its own (L*K
+    rows), as a routed buffer would be; the K reads of a row after the first
+    come from L2, so this figure can exceed the HBM bandwidth."""
     s = cfg.elem_bytes
     return (cfg.L * cfg.K + cfg.L) * cfg.d * s + 12 * cfg.L * cfg.K
 
@@ -231,26 +245,59 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle sample
 
-def oracle_sample(cfg, target_s=12.0, max_tokens=None):
-    """Time the CPU oracle (forward + backward) on the first L' tokens of the
-    workload, growing L' until one run takes about target_s seconds."""
+class HostInputs:
+    """The workload's inputs for the CPU oracle: the expert weights once, in
+    fp64 (the oracle widens every input to fp64 itself; doing it once here
+    keeps that copy out of each timed call), and the first rows of x, dY,
+    ids and gates on demand.  x, dY and the routing are row-wise, so the
+    first L' rows of the workload are the inputs of its first L' tokens.
+    `src` holds the full workload's tensors (on any device), or is None to
+    generate the rows and weights on the host."""
+
+    def __init__(self, cfg, src=None):
+        self.cfg = cfg
+        self.src = src
+        w = src if src is not None else I.make_weights(cfg, "cpu")
+        self.W = {k: (None if w.get(k) is None else self._f64(w[k])) for k in ("W1", "W2", "W3")}
+
+    @staticmethod
+    def _f64(t):
+        t = t.detach().cpu()
+        return (t.float() if t.dtype == torch.bfloat16 else t).numpy().astype(np.float64)
+
+    def rows(self, n):
+        if self.src is not None:
+            r = {k: self.src[k][:n].cpu() for k in ("ids", "gates", "x", "dY")}
+        else:
+            sub = self.cfg.scaled(L=n)
+            x = I.make_x(sub, "cpu")
+            ids, gates = I.make_routing(sub, x, "cpu")
+            r = {"ids": ids, "gates": gates, "x": x, "dY": I.make_dy(sub, "cpu")}
+        r.update(self.W)
+        return r
+
+
+def oracle_run(cfg, inp):
+    """One forward + backward of the CPU oracle on a prepared sample."""
     import oracle.moe_oracle as O
+    O.forward(inp["ids"], inp["gates"], inp["x"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+    O.backward(inp["ids"], inp["gates"], inp["x"], inp["dY"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+
+
+def oracle_sample(cfg, host, target_s=12.0, max_tokens=None):
+    """Time the CPU oracle (forward + backward) on the first L' tokens of the
+    workload, growing L' until one run takes about target_s / 3 seconds or
+    more; returns (tokens/s, L', seconds) of that last run."""
     Lp = 64
-    tokens_done, elapsed = 0, 0.0
+    cap = min(max_tokens or cfg.L, cfg.L)
     while True:
-        # x, dY and the router are row-wise, so the first Lp rows of the
-        # workload are regenerated exactly (same ids, gates and weights)
-        sub = cfg.scaled(L=Lp)
-        inp = I.make_inputs(sub, "cpu")
+        inp = host.rows(Lp)
         t0 = time.perf_counter()
-        O.forward(inp["ids"], inp["gates"], inp["x"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
-        O.backward(inp["ids"], inp["gates"], inp["x"], inp["dY"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        oracle_run(cfg, inp)
         dt = time.perf_counter() - t0
-        tokens_done, elapsed = Lp, dt
-        if dt >= target_s / 3 or Lp >= (max_tokens or cfg.L):
-            break
-        Lp = min(max_tokens or cfg.L, Lp * max(2, int(target_s / 3 / max(dt, 1e-3))))
-    return tokens_done / elapsed, tokens_done, elapsed
+        if dt >= target_s / 3 or Lp >= cap:
+            return Lp / dt, Lp, dt
+        Lp = min(cap, Lp * max(2, int(target_s / 3 / max(dt, 1e-3))))
 
 
 def cpu_cores():
@@ -371,13 +418,7 @@ def run_ours(args, rank, world, local_rank):
     tpk = pk["bf16_tflops_sustained"] if capped else pk["bf16_tflops"]
     tsrc = f"{src} ({'sustained, sw_power_cap seen' if capped else 'burst'})"
     if identity:
-        nbytes = identity_bytes(cfg)
-        t_ms = statistics.mean(fwd_ms)
-        ach = nbytes / (t_ms * 1e-3) / 1e9
-        roof = {"kernel": "identity_combine_kernel (forward pass)", "bound": "hbm", "achieved": ach,
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                "traffic": traffic_per_launch(cfg.name, "identity_forward", IDENTITY_SRC),
-                "peak_source": src, "algorithmic_bytes": nbytes}
+        roof = identity_roofline(cfg, statistics.mean(fwd_ms), pk, src)
     else:
         fl = stage_flops(cfg)
         dom = max(fl, key=lambda n: stages[n])
@@ -408,7 +449,70 @@ def run_ours(args, rank, world, local_rank):
         out["router"] = run_router(cfg, inp, dev, flush, pk)
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, cfg, layer, inp, dev, world)
-    del flush
+    del flush, layer
+    return out, inp
+
+
+def identity_roofline(cfg, t_ms, pk, src):
+    """Roofline of one identity gather/combine pass against the HBM copy
+    bandwidth, on the bytes the pass must move (identity_bytes); the
+    every-routed-row figure is reported beside it."""
+    nbytes = identity_bytes(cfg)
+    ach = nbytes / (t_ms * 1e-3) / 1e9
+    rb = identity_routed_bytes(cfg)
+    return {"kernel": "identity_combine_kernel (forward pass)", "bound": "hbm", "achieved": ach,
+            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+            "traffic": traffic_per_launch(cfg.name, "identity_forward", IDENTITY_SRC),
+            "peak_source": src, "algorithmic_bytes": nbytes, "ms": t_ms,
+            "routed_row_bytes": rb, "routed_row_GB_per_s": rb / (t_ms * 1e-3) / 1e9}
+
+
+def time_calls(fn, flush, warmup, iters):
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed
+    before every call."""
+    for _ in range(warmup):
+        flush_l2(flush)
+        fn()
+    ts = []
+    for _ in range(iters):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_routing_stress(cfg, dev, warmup, iters, pk, src, flush, combine=True):
+    """The dispatch build and the identity gather/combine on the routing
+    stress workload (Zipf ids over 256 experts), measured on their own:
+    the dispatch build from the ids alone, then one identity forward pass
+    (gather through expert_token_indices, gate-weighted combine) over x."""
+    ids, gates = I.make_routing(cfg, None, dev)
+    shape = B.make_shape(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act)
+    disp = B.alloc_dispatch(shape, dev)
+    n0 = B.moeblaze_kernel_launches()
+    ms = time_calls(lambda: B.dispatch_build(shape, ids, disp), flush, warmup, iters)
+    per_build = (B.moeblaze_kernel_launches() - n0) / (warmup + iters)
+    assert B.device_error(shape, disp) == 0
+    nb = dispatch_bytes(cfg)
+    ach = nb / (ms * 1e-3) / 1e9
+    out = {"dispatch_build": {
+        "workload": cfg.name, "ms": ms, "algorithmic_bytes": nb, "GB_per_s": ach, "launches_per_build": per_build,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / pk["hbm_gbs"], "peak_source": src}}}
+    if combine:
+        x = I.make_x(cfg, dev)
+        y = torch.empty_like(x)
+        lb = B.alloc_layer(shape, dev)
+        t = time_calls(lambda: B.forward(shape, x, gates, disp, None, None, None, y, lb), flush, warmup, iters)
+        assert B.device_error(shape, disp) == 0
+        out["identity_combine"] = identity_roofline(cfg, t, pk, src)
+        out["identity_combine"]["workload"] = cfg.name
+        del x, y
+    del ids, gates, disp
     return out
 
 
@@ -514,20 +618,8 @@ def run_dispatch_only(args, local_rank):
     shape = B.make_shape(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act)
     disp = B.alloc_dispatch(shape, dev)
     flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    for _ in range(args.warmup):
-        flush_l2(flush)
-        B.dispatch_build(shape, ids, disp)
-    ts = []
-    for _ in range(args.steps):
-        flush_l2(flush)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        B.dispatch_build(shape, ids, disp)
-        e1.record()
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1))
+    ms = time_calls(lambda: B.dispatch_build(shape, ids, disp), flush, args.warmup, args.steps)
     assert B.device_error(shape, disp) == 0
-    ms = statistics.median(ts)
     nb = dispatch_bytes(cfg)
     pk, src = peaks()
     ach = nb / (ms * 1e-3) / 1e9
@@ -539,19 +631,18 @@ def run_dispatch_only(args, local_rank):
 
 def run_reference(args, cfg):
     """The CPU oracle as the reference arm: each step runs it on a bounded
-    sample of the workload's tokens (same shapes otherwise)."""
-    import oracle.moe_oracle as O
+    sample of the workload's tokens (same shapes otherwise).  Its inputs are
+    generated on the host (the weights once)."""
     # each step's sample is sized so that all warm-up and timed steps take
     # about 150 s together (at most 6 s a step)
     per_step = max(0.1, min(6.0, 150.0 / (args.steps + args.warmup)))
-    tps, ntok, dt = oracle_sample(cfg, target_s=per_step)
-    sub = cfg.scaled(L=ntok)
-    inp = I.make_inputs(sub, "cpu")
+    host = HostInputs(cfg)
+    tps, ntok, dt = oracle_sample(cfg, host, target_s=3 * per_step)
+    inp = host.rows(ntok)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        O.forward(inp["ids"], inp["gates"], inp["x"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
-        O.backward(inp["ids"], inp["gates"], inp["x"], inp["dY"], inp["W1"], inp["W2"], inp["W3"], cfg.act, E=cfg.E)
+        oracle_run(cfg, inp)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     v = ntok / statistics.mean(times)
@@ -572,7 +663,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=1, help="workload index (0..4); default: the SiLU bf16 layer")
+    ap.add_argument("--config", type=int, default=3,
+                    help="workload index (0..4); default: the Mixtral-like SwiGLU bf16 layer, the largest GEMM workload")
+    ap.add_argument("--no-routing-stress", action="store_true",
+                    help="skip the dispatch build and identity gather/combine measured on the routing stress workload")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload with this many tokens instead (smaller profiling captures)")
@@ -606,13 +700,27 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     B.lib()
-    out = run_ours(args, rank, world, local_rank)
+    out, inp = run_ours(args, rank, world, local_rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, ntok, dt = oracle_sample(cfg)
+        # the oracle on the first tokens of the same inputs (copied to the host)
+        host = HostInputs(cfg, inp)
+        tps, ntok, dt = oracle_sample(cfg, host)
+        del host
         out["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                                "machine": platform.machine(),
                                "sample": f"first {ntok} tokens of the workload (same d, h, E, K), "
                                          f"{dt:.1f} s of fp64 CPU work"}
+    del inp
+    torch.cuda.empty_cache()
+    stress = I.CONFIGS[4]
+    if not args.no_routing_stress and cfg.act != "identity":
+        # the dispatch build and the gather/combine on the workload whose
+        # index structures are largest (2M tokens, 256 experts, Zipf ids)
+        dev = torch.device("cuda", local_rank)
+        flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        pk, src = peaks()
+        out["routing_stress"] = run_routing_stress(stress, dev, args.warmup, min(args.steps, 20), pk, src, flush)
+        del flush
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -81,8 +81,15 @@ typedef struct {
  *                                expert_token_indices
  *   meta                         moeblaze_dispatch_meta_bytes() bytes, 16-byte
  *                                aligned: per-expert counts, padded row offsets,
- *                                the GEMM tile table and a device error word;
- *                                read by forward/backward, opaque to the caller.
+ *                                the GEMM tile table, a device error word and
+ *                                the (L, E, K) the build was made for; read by
+ *                                forward/backward, otherwise opaque to the caller.
+ * A dispatch serves only forward/backward calls with the L, E and K of the
+ * shape it was built for.  Their kernels compare the three with the values
+ * the build recorded in meta before they read any of the structures; on a
+ * mismatch they read none of them, leave their outputs unspecified and set
+ * bit 4 of the device error word (moeblaze_device_error then returns
+ * MOEBLAZE_ERR_INVALID_ARG).
  */
 typedef struct {
   int32_t* expert_token_indices;
@@ -253,11 +260,20 @@ MOEBLAZE_API moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, c
 
 /* Synchronise `stream` and read the device error word of `disp->meta`:
  * *code = 0 when every kernel since the last dispatch_build on this meta
- * finished normally; otherwise a bitwise OR of 1 (bad routing) and 2 (a
- * bounded device-side wait ran out).  Returns MOEBLAZE_ERR_BAD_ROUTING or
- * MOEBLAZE_ERR_TIMEOUT accordingly, MOEBLAZE_OK when *code == 0. */
+ * finished normally; otherwise a bitwise OR of 1 (bad routing), 2 (a
+ * bounded device-side wait ran out) and 4 (a forward/backward call whose L,
+ * E or K differ from the build's).  Returns MOEBLAZE_ERR_BAD_ROUTING,
+ * MOEBLAZE_ERR_TIMEOUT or MOEBLAZE_ERR_INVALID_ARG accordingly (in that order
+ * of precedence), MOEBLAZE_OK when *code == 0. */
 MOEBLAZE_API moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp,
                                       int32_t* code, moeblaze_stream stream);
+
+/* Host-side check of a dispatch against a shape, on a HOST copy of the
+ * first 32 bytes of its meta buffer (the header the build writes): OK when
+ * the build was made for s's L, E and K (for L = 0: when it was made for no
+ * tokens), MOEBLAZE_ERR_INVALID_ARG otherwise or when meta_header is NULL.
+ * The same comparison the forward/backward kernels make on the device. */
+MOEBLAZE_API moeblaze_status moeblaze_dispatch_meta_check(const moeblaze_shape* s, const void* meta_header);
 
 /* Diagnostics.
  *

@@ -29,7 +29,7 @@ EXPORTS = [
     "moeblaze_forward_workspace_bytes", "moeblaze_backward_workspace_bytes", "moeblaze_dispatch_build",
     "moeblaze_forward", "moeblaze_backward", "moeblaze_device_error", "moeblaze_status_string",
     "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
-    "moeblaze_dispatch_build_static",
+    "moeblaze_dispatch_build_static", "moeblaze_dispatch_meta_check",
     "moeblaze_router_forward", "moeblaze_router_backward", "moeblaze_router_backward_workspace_bytes",
 ]
 
@@ -86,6 +86,8 @@ def lib():
         L.moeblaze_router_backward.restype = ctypes.c_int
         L.moeblaze_device_error.argtypes = [SP, DP, ctypes.POINTER(ctypes.c_int32), P]
         L.moeblaze_device_error.restype = ctypes.c_int
+        L.moeblaze_dispatch_meta_check.argtypes = [SP, P]
+        L.moeblaze_dispatch_meta_check.restype = ctypes.c_int
         L.moeblaze_status_string.argtypes = [ctypes.c_int]
         L.moeblaze_status_string.restype = ctypes.c_char_p
         L.moeblaze_version.argtypes = []
@@ -162,6 +164,12 @@ def moeblaze_device_error(shape, disp, stream):
     code = ctypes.c_int32(0)
     st = lib().moeblaze_device_error(ctypes.byref(shape), ctypes.byref(disp), ctypes.byref(code), stream)
     return st, code.value
+
+
+def moeblaze_dispatch_meta_check(shape, meta_header) -> int:
+    """meta_header: a host buffer (bytes-like or ctypes pointer) holding a
+    copy of the first 32 bytes of a dispatch's meta."""
+    return lib().moeblaze_dispatch_meta_check(ctypes.byref(shape), meta_header)
 
 
 def moeblaze_set_stage_events(events, n: int) -> None:
@@ -418,8 +426,10 @@ def router_backward(shape: Shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx
 
 
 def device_error(shape: Shape, disp: DispatchBuffers, stream=None) -> int:
+    """The device error word of a dispatch (0: every kernel since its build
+    finished normally; bits 1 bad routing, 2 timeout, 4 shape mismatch)."""
     st, code = moeblaze_device_error(shape, disp.struct(), _stream(stream))
-    if st not in (OK, ERR_BAD_ROUTING, ERR_TIMEOUT):
+    if st not in (OK, ERR_BAD_ROUTING, ERR_TIMEOUT) and not (st == ERR_INVALID_ARG and code & 4):
         raise MoEBlazeError(st, "moeblaze_device_error")
     return code
 

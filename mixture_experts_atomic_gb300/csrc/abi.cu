@@ -279,7 +279,16 @@ moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_di
   *code = c;
   if (c & kErrBadRouting) return MOEBLAZE_ERR_BAD_ROUTING;
   if (c & kErrTimeout) return MOEBLAZE_ERR_TIMEOUT;
+  if (c & kErrShapeMismatch) return MOEBLAZE_ERR_INVALID_ARG;
   return MOEBLAZE_OK;
+}
+
+moeblaze_status moeblaze_dispatch_meta_check(const moeblaze_shape* s, const void* meta_header) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if (!meta_header) return MOEBLAZE_ERR_INVALID_ARG;
+  return meta_matches(reinterpret_cast<const int32_t*>(meta_header), s->L, s->E, s->K) ? MOEBLAZE_OK
+                                                                                     : MOEBLAZE_ERR_INVALID_ARG;
 }
 
 size_t moeblaze_router_backward_workspace_bytes(const moeblaze_shape* s) {

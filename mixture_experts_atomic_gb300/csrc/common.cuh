@@ -24,15 +24,18 @@ constexpr size_t kSchedBytes = 256;  // tile counters behind the fp32 accumulato
 // device error word bits
 constexpr int kErrBadRouting = 1;
 constexpr int kErrTimeout = 2;
+constexpr int kErrShapeMismatch = 4;  // forward/backward given a dispatch built for another L, E or K
 
 // ---------------------------------------------------------------- meta layout
 // The meta buffer written by the dispatch build and read by the GEMMs:
-//   int32 header[8]          err, num_m_tiles, padded_rows, reserved...
+//   int32 header[8]          err, num_m_tiles, padded_rows, L, E, K, reserved...
 //   int32 n_e[E]             tokens per expert
 //   int32 pad_off[E+1]       padded row offset of each expert (multiples of 256)
 //   int32 order[E]           experts by descending n_e (ties: lower id first)
 //   int32 tile_expert[MT]    expert of each 128-row tile, MT = max_m_tiles (an even count per expert)
+constexpr int kHdrL = 3, kHdrE = 4, kHdrK = 5;  // header words holding the shape the build was made for
 struct MetaView {
+  int32_t* hdr;
   int32_t* err;
   int32_t* num_m_tiles;
   int32_t* padded_rows;
@@ -54,6 +57,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline MetaView meta_view(void* meta, int E) {
   int32_t* p = reinterpret_cast<int32_t*>(meta);
   MetaView m;
+  m.hdr = p;
   m.err = p + 0;
   m.num_m_tiles = p + 1;
   m.padded_rows = p + 2;
@@ -66,6 +70,16 @@ inline MetaView meta_view(void* meta, int E) {
 }
 inline size_t meta_bytes(int64_t LK, int E) {
   return align_up(sizeof(int32_t) * (8 + E + (E + 1) + E + (size_t)max_m_tiles(LK, E)), 256);
+}
+
+// The shape a dispatch build recorded in its meta header against the shape a
+// forward/backward call was given.  The tile table, offsets and counts are
+// sized and laid out by (L, E, K), so a kernel reads nothing else of the
+// dispatch unless this holds.  Used by the kernels on the device header and
+// by moeblaze_dispatch_meta_check on a host copy of it.  A build for L = 0
+// records only L (no kernel reads its structures).
+__host__ __device__ inline bool meta_matches(const int32_t* hdr, int64_t L, int E, int K) {
+  return (int64_t)hdr[kHdrL] == L && (L == 0 || (hdr[kHdrE] == E && hdr[kHdrK] == K));
 }
 
 // ---------------------------------------------------------------- status helper

@@ -13,7 +13,8 @@
 //                      counts -> chunk bases and n_e.
 //   K2b offsets_kernel expert_token_offsets (the scan of n_e), the padded
 //                      row offsets, the GEMM tile table (split over a few
-//                      CTAs) and the experts' descending-load order.
+//                      CTAs), the experts' descending-load order and the
+//                      (L, E, K) the build was made for.
 //   K3 scatter_kernel  one CTA per chunk.  A shuffle scan over each expert's
 //                      32 popcounts gives every word its first position;
 //                      each token then places its K slots:
@@ -200,7 +201,8 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
 // split over the CTAs, and CTA 0 writes the offsets.  Computed once instead
 // of in every chunk's CTA.
 __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __restrict__ n_e, int E,
-                                                           int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles) {
+                                                           int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles,
+                                                           int64_t L, int K) {
   __shared__ int32_t off[kMaxE + 1];
   __shared__ int32_t poff[kMaxE + 1];
   __shared__ int32_t cnt[kMaxE];
@@ -268,6 +270,10 @@ __global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __rest
   if (tid == 0) {
     *meta.num_m_tiles = (int32_t)ntiles;
     *meta.padded_rows = pcarry;
+    // the shape this build was made for, checked by every forward/backward kernel
+    meta.hdr[kHdrL] = (int32_t)L;
+    meta.hdr[kHdrE] = E;
+    meta.hdr[kHdrK] = K;
   }
   for (int e = tid; e <= E; e += kThreads) {
     D2[e] = off[e];
@@ -442,7 +448,7 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
     int64_t g = (mt + 1023) / 1024;  // about 4 tile entries (binary searches) per thread
     if (g > sm_count()) g = sm_count();
     if (g < 1) g = 1;
-    offsets_kernel<<<(unsigned)g, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt);
+    offsets_kernel<<<(unsigned)g, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt, L, K);
   }
   MB_CUDA(cudaGetLastError());
   count_launch();

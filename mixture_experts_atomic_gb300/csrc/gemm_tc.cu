@@ -398,6 +398,14 @@ __host__ __device__ constexpr bool cp_b(int m) { return m == DW3; }
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
+  // A dispatch built for another (L, E, K) lays out its tables differently:
+  // record the mismatch and read none of them (every thread reads the same
+  // three header words, so the whole CTA leaves here together, before any
+  // barrier or TMEM allocation).
+  if (!meta_matches(p.meta.hdr, p.L, p.E, p.K)) {
+    if (threadIdx.x == 0) atomicOr(p.meta.err, kErrShapeMismatch);
+    return;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);

@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
                                                                     const int32_t* __restrict__ D4,
                                                                     const float* __restrict__ gates,
                                                                     T* __restrict__ dst, int64_t L, int d, int K,
-                                                                    int64_t LK) {
+                                                                    int64_t LK, const int32_t* __restrict__ hdr,
+                                                                    int E, int32_t* err) {
   constexpr int V = Vec<T>::N;                 // elements per 16-byte piece
   constexpr int CH = kChunkBytes / sizeof(T);  // columns per chunk
   extern __shared__ __align__(16) uint8_t stage[];  // [kStages][n][kChunkBytes]
@@ -79,6 +80,11 @@ __global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __r
   const int tid = threadIdx.x;
   const int64_t t0 = (int64_t)blockIdx.x * kWin;
   const int n = kWin * K;
+  // a dispatch built for another (L, E, K): record it and read none of its maps
+  if (!meta_matches(hdr, L, E, K)) {
+    if (tid == 0) atomicOr(err, kErrShapeMismatch);
+    return;
+  }
 
   if (tid < n) {
     const int64_t t = t0 + tid / K;
@@ -212,6 +218,7 @@ moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src
                                         const float* gates, void* dst, cudaStream_t st) {
   if (s.L == 0) return MOEBLAZE_OK;
   const int64_t LK = s.L * s.K;
+  const MetaView meta = meta_view(disp.meta, s.E);
   const dim3 grid((unsigned)((s.L + kWin - 1) / kWin));
   const size_t smem = kStages * (size_t)kWin * s.K * kChunkBytes;
   if (s.dtype == MOEBLAZE_BF16) {
@@ -219,12 +226,13 @@ moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src
     MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), disp.expert_token_indices,
                                     disp.token_index_map, gates, reinterpret_cast<__nv_bfloat16*>(dst), s.L, s.d,
-                                    s.K, LK);
+                                    s.K, LK, meta.hdr, s.E, meta.err);
   } else {
     auto k = identity_combine_kernel<float>;
     MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     k<<<grid, kThreads, smem, st>>>(reinterpret_cast<const float*>(src), disp.expert_token_indices,
-                                    disp.token_index_map, gates, reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK);
+                                    disp.token_index_map, gates, reinterpret_cast<float*>(dst), s.L, s.d, s.K, LK,
+                                    meta.hdr, s.E, meta.err);
   }
   MB_CUDA(cudaGetLastError());
   count_launch();

@@ -51,6 +51,13 @@ struct Common {
     return D1[c.off + i];
   }
   __device__ bool valid(const RowCtx& c, int q) const { return q - c.pad0 < c.n; }
+  // the dispatch was built for this call's (L, E, K); otherwise record the
+  // mismatch and read nothing of it (the same answer in every thread)
+  __device__ bool shape_ok() const {
+    if (meta_matches(meta.hdr, L, E, K)) return true;
+    if (threadIdx.x == 0 && threadIdx.y == 0) atomicOr(meta.err, kErrShapeMismatch);
+    return false;
+  }
   __device__ float gate(int t, int e, int* slot = nullptr) const {
     for (int k = 0; k < K; ++k)
       if (D3[(int64_t)t * K + k] == e) {
@@ -67,6 +74,7 @@ struct Common {
 __global__ void up_kernel(Common c, const float* __restrict__ x, const float* __restrict__ W1,
                           const float* __restrict__ W2, float* __restrict__ A, float* __restrict__ B,
                           float* __restrict__ H, int64_t rows, bool swiglu) {
+  if (!c.shape_ok()) return;
   __shared__ float Xs[T][T + 1], W1s[T][T + 1], W2s[T][T + 1];
   __shared__ int toks[T];
   RowCtx r;
@@ -104,6 +112,7 @@ __global__ void up_kernel(Common c, const float* __restrict__ x, const float* __
 // y[t] += g * (H W3_e)[row]
 __global__ void down_kernel(Common c, const float* __restrict__ H, const float* __restrict__ W3,
                             float* __restrict__ y) {
+  if (!c.shape_ok()) return;
   __shared__ float Hs[T][T + 1], Ws[T][T + 1];
   RowCtx r;
   if (!c.row_ctx(blockIdx.x, r)) return;
@@ -129,6 +138,7 @@ __global__ void down_kernel(Common c, const float* __restrict__ H, const float* 
 __global__ void dh_kernel(Common c, const float* __restrict__ dY, const float* __restrict__ W3,
                           const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ dAB,
                           float* __restrict__ Hg, float* __restrict__ dg, bool swiglu) {
+  if (!c.shape_ok()) return;
   __shared__ float Gs[T][T + 1], Ws[T][T + 1];
   __shared__ int toks[T];
   RowCtx r;
@@ -183,6 +193,7 @@ __global__ void dh_kernel(Common c, const float* __restrict__ dY, const float* _
 // ------------------------------------------------ dX = dA W1^T + dB W2^T, combine
 __global__ void dx_kernel(Common c, const float* __restrict__ dAB, const float* __restrict__ W1,
                           const float* __restrict__ W2, float* __restrict__ dX, bool swiglu) {
+  if (!c.shape_ok()) return;
   __shared__ float As[T][T + 1], Ws[T][T + 1];
   RowCtx r;
   if (!c.row_ctx(blockIdx.x, r)) return;
@@ -217,6 +228,7 @@ __global__ void dx_kernel(Common c, const float* __restrict__ dAB, const float* 
 // dW1_e[i][j] = sum_q x[tok q][i] dA[q][j] ; dW2 with dB ; over the expert's rows
 __global__ void dw12_kernel(Common c, const float* __restrict__ x, const float* __restrict__ dAB,
                             float* __restrict__ dW1, float* __restrict__ dW2, bool swiglu) {
+  if (!c.shape_ok()) return;
   __shared__ float Xs[T][T + 1], As[T][T + 1], Bs[T][T + 1];
   __shared__ int toks[T];
   const int e = blockIdx.z;
@@ -256,6 +268,7 @@ __global__ void dw12_kernel(Common c, const float* __restrict__ x, const float* 
 // dW3_e[j][col] = sum_q Hg[q][j] dY[tok q][col]
 __global__ void dw3_kernel(Common c, const float* __restrict__ Hg, const float* __restrict__ dY,
                            float* __restrict__ dW3) {
+  if (!c.shape_ok()) return;
   __shared__ float Hs[T][T + 1], Gs[T][T + 1];
   __shared__ int toks[T];
   const int e = blockIdx.z;

@@ -1,6 +1,8 @@
 """Shared helpers of the GPU parity tests (imported by test_gpu_*.py)."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -29,6 +31,11 @@ def check_dispatch(layer: MoELayer, ids_cpu: torch.Tensor, E: int):
     assert np.array_equal(g1, D1), "expert_token_indices"
     assert np.array_equal(g3, D3), "token_expert_indices"
     assert np.array_equal(g4, D4), "token_index_map"
+    # the header records the (L, E, K) the build was made for; the forward and
+    # backward kernels compare it with their own shape (the same comparison
+    # as this host-side call)
+    hdr = ctypes.create_string_buffer(layer.disp.meta[:32].cpu().numpy().tobytes(), 32)
+    assert B.moeblaze_dispatch_meta_check(layer.shape, hdr) == B.OK
     num_mt, n_e, pad, order = layer.meta()
     n_e = n_e.numpy(); pad = pad.numpy(); order = order.numpy()
     assert np.array_equal(n_e, np.diff(D2))
@@ -67,14 +74,15 @@ def full_compare(cfg, inp_cpu, tol=None, check_saved=True):
         if check_saved:
             A, Bv = layer.saved()
             _, _, pad, _ = layer.meta()
-            A = O._f64(A); Bv = O._f64(Bv) if Bv is not None else None
             ra, rb = [], []
             ga, gb = [], []
+            # only the rows the forward wrote are widened: the padding rows
+            # of a segment and the tail past the last segment hold no data
             for e, s in keep["saved"].items():
                 p0 = int(pad[e]); n = s["a"].shape[0]
-                ra.append(s["a"]); ga.append(A[p0:p0 + n])
+                ra.append(s["a"]); ga.append(O._f64(A[p0:p0 + n]))
                 if Bv is not None:
-                    rb.append(s["b"]); gb.append(Bv[p0:p0 + n])
+                    rb.append(s["b"]); gb.append(O._f64(Bv[p0:p0 + n]))
             errs["A"] = O.rel_err(np.concatenate(ga), np.concatenate(ra))
             if Bv is not None:
                 errs["B"] = O.rel_err(np.concatenate(gb), np.concatenate(rb))
@@ -83,9 +91,31 @@ def full_compare(cfg, inp_cpu, tol=None, check_saved=True):
     return errs, layer
 
 
-def sampled_compare(cfg, n_tok=48, n_cols=3, seed=0, tol=None):
-    """Full-size run on the device; the oracle computes sampled token rows of
-    y and dX and sampled columns/rows of the weight gradients one by one."""
+def spread_indices(n, tile, per_tile, rng, extra=0):
+    """Indices into [0, n) that cover the first, a middle and the last tile
+    of width `tile`: each tile's first and last index plus `per_tile` random
+    ones inside it, and `extra` uniform picks anywhere."""
+    nt = (n + tile - 1) // tile
+    picks = set()
+    for t in sorted({0, nt // 2, nt - 1}):
+        lo, hi = t * tile, min(n, (t + 1) * tile)
+        picks.update([lo, hi - 1])
+        picks.update(rng.choice(np.arange(lo, hi), min(per_tile, hi - lo), replace=False).tolist())
+    if extra:
+        picks.update(rng.choice(n, min(extra, n), replace=False).tolist())
+    return sorted(int(i) for i in picks)
+
+
+def sampled_compare(cfg, n_tok=62, per_tile=10, seed=0, tol=None):
+    """Full-size run on the device; the oracle computes sampled outputs one
+    by one:
+      - y, dX and dgates on n_tok random token rows plus the first and last;
+      - for EVERY expert with tokens, columns of dW1 (and dW2) and rows of
+        dW3 spread over the first, a middle and the last output tile of the
+        GEMM that writes them (128-column tiles of dW1|dW2 for SwiGLU,
+        256 for SiLU; 128-row tiles of dW3), at least 32 of each plus 4
+        uniform picks.
+    Returns the errors and the sampled fractions."""
     tol = TOL[cfg.dtype] if tol is None else tol
     inp = I.make_inputs(cfg, "cuda")
     layer = run_layer(cfg, inp)
@@ -102,16 +132,18 @@ def sampled_compare(cfg, n_tok=48, n_cols=3, seed=0, tol=None):
     dx_ref, dg_ref = O.backward_rows(toks, ids, gates, xr, dyr, W["W1"], W["W2"], W["W3"], cfg.act, with_dgates=True)
     errs = {"y": O.rel_err(layer.y[tt], y_ref), "dX": O.rel_err(layer.dX[tt], dx_ref),
             "dgates": O.rel_err(layer.dgates[tt], dg_ref)}
+    frac = {"token_rows": len(toks) / cfg.L}
     if cfg.act != "identity":
         n_e = np.diff(D2)
-        nz = np.nonzero(n_e)[0]
-        experts = sorted({int(nz[np.argmax(n_e[nz])]), int(nz[np.argmin(n_e[nz])])})
+        experts = [int(e) for e in np.nonzero(n_e)[0]]
         gr = np.zeros(cfg.L * cfg.K)
         g_np = gates.numpy().astype(np.float64)
         for k in range(cfg.K):
             gr[D4[:, k]] = g_np[:, k]
-        hc = sorted(set(rng.choice(cfg.h, n_cols, replace=False).tolist() + [0, cfg.h - 1]))
-        wr = sorted(set(rng.choice(cfg.h, n_cols, replace=False).tolist() + [cfg.h - 1]))
+        ntile = 128 if cfg.act == "swiglu" else 256
+        hc = spread_indices(cfg.h, ntile, per_tile, rng, extra=4)
+        wr = spread_indices(cfg.h, 128, per_tile, rng, extra=4)
+        assert len(hc) >= 32 and len(wr) >= 32
         e1, e2, e3 = [], [], []
         for e in experts:
             seg = D1[D2[e]:D2[e + 1]]
@@ -126,6 +158,8 @@ def sampled_compare(cfg, n_tok=48, n_cols=3, seed=0, tol=None):
         errs["dW3"] = max(e3)
         if e2:
             errs["dW2"] = max(e2)
+        frac.update({"experts_checked": len(experts), "experts_with_tokens": len(experts),
+                     "dW12_columns": len(hc) / cfg.h, "dW3_rows": len(wr) / cfg.h})
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{cfg.name}: {bad} (tol {tol}); all {errs}"
-    return errs
+    return errs, frac

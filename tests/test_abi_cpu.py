@@ -149,3 +149,23 @@ def test_router_validation_codes():
         == B.ERR_INVALID_ARG
     assert B.moeblaze_router_backward(ok, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, ws - 1, None) \
         == B.ERR_WORKSPACE
+
+
+def test_dispatch_meta_check_compares_the_recorded_shape():
+    """The comparison the forward/backward kernels make on the device header
+    (words 3, 4, 5 = the L, E, K the build recorded), run on a host copy."""
+    import struct
+    _lib()
+    s = B.make_shape(70000, 128, 128, 64, 6, B.BF16, "swiglu")
+
+    def hdr(L, E, K):
+        return ctypes.create_string_buffer(struct.pack("<8i", 0, 5, 640, L, E, K, 0, 0), 32)
+
+    assert B.moeblaze_dispatch_meta_check(s, hdr(70000, 64, 6)) == B.OK
+    for L, E, K in [(69999, 64, 6), (70000, 63, 6), (70000, 64, 5), (0, 0, 0)]:
+        assert B.moeblaze_dispatch_meta_check(s, hdr(L, E, K)) == B.ERR_INVALID_ARG, (L, E, K)
+    # a build for no tokens records only L = 0 and serves any L = 0 call
+    s0 = B.make_shape(0, 128, 128, 64, 6, B.BF16, "swiglu")
+    assert B.moeblaze_dispatch_meta_check(s0, hdr(0, 0, 0)) == B.OK
+    assert B.moeblaze_dispatch_meta_check(s0, hdr(1, 64, 6)) == B.ERR_INVALID_ARG
+    assert B.moeblaze_dispatch_meta_check(s, None) == B.ERR_INVALID_ARG

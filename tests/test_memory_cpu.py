@@ -56,6 +56,8 @@ def test_memory_report_retained_is_saved_plus_indices():
     assert rep["retained_fwd_to_bwd_bytes"] == rep["saved_activation_bytes"] + rep["index_bytes"]
     assert rep["materialising_retained_bytes"] == LK * cfg.d * 2 + 5 * LK * cfg.h * 2
     assert 2.6 < rep["materialising_over_retained"] < 2.7
+    sc = rep["scratch_bytes"]
+    assert rep["peak_activation_bytes"] == rep["retained_fwd_to_bwd_bytes"] + max(sc["forward"], sc["backward"])
 
 
 def test_memory_report_identity_keeps_only_indices():

@@ -67,3 +67,14 @@ def test_static_scratch_dispatch_matches_caller_scratch_twice():
     ids2, _ = I.random_routing(16384, 8, 2, 22)
     s2 = B.make_shape(16384, 1024, 4096, 8, 2, B.BF16, "silu")
     _compare(s2, ids2.cuda(), validate=1)
+    # third call: larger than the first, so it reads scratch words neither
+    # earlier call wrote; L is not a multiple of the 1024-token chunk, so its
+    # last chunk is partial
+    ids3, _ = I.random_routing(200001, 64, 6, 23, one_expert=63)
+    s3 = B.make_shape(200001, 128, 128, 64, 6, B.BF16, "swiglu")
+    assert B.moeblaze_dispatch_workspace_bytes(s3) > B.moeblaze_dispatch_workspace_bytes(s1)
+    assert B.moeblaze_dispatch_workspace_bytes(s3) <= B.STATIC_SCRATCH_BYTES
+    _compare(s3, ids3.cuda(), validate=1)
+    # and a small ragged case after it: 1537 tokens, 3 experts, K = 3
+    ids4, _ = I.random_routing(1537, 3, 3, 24)
+    _compare(B.make_shape(1537, 128, 128, 3, 3, B.BF16, "silu"), ids4.cuda(), validate=0)
