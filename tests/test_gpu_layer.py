@@ -73,6 +73,20 @@ def test_identity_layer_small(dtype, K):
     full_compare(cfg, inp)
 
 
+@pytest.mark.parametrize("L,d,E,K,dtype", [
+    (2049, 1000, 64, 8, "bf16"),   # 2000-byte rows in chunks of 1024 + 976 bytes
+    (999, 3000, 32, 3, "bf16"),    # 6000-byte rows in chunks of 2720, 2720, 560 bytes
+    (777, 6144, 256, 4, "bf16"),   # the stress workload's row width: six 2 KB chunks
+    (515, 1500, 8, 1, "f32"),      # K = 1, 6000-byte fp32 rows in one chunk
+])
+def test_identity_layer_ragged_chunks(L, d, E, K, dtype):
+    """The identity gather/combine stages each window's routed rows in
+    column chunks sized to the ring stage; rows whose width is not a multiple
+    of the chunk end in a partial chunk, and the last window is partial."""
+    cfg = I.MoEConfig("t_identity_chunks", L, d, 0, E, K, "identity", dtype, 17, "zipf")
+    full_compare(cfg, I.make_inputs(cfg, "cpu"))
+
+
 def test_empty_layer_zero_grads():
     from mixture_experts_atomic_gb300.layer import MoELayer
     layer = MoELayer(0, 128, 128, 4, 2, torch.bfloat16, "swiglu", "cuda")
