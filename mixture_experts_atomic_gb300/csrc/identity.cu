@@ -4,28 +4,21 @@
 // awesome-system-papers page, section "免物化 token dispatch", Forward and
 // Backward; the backward is the same kernel on dY -> dX).
 //
-// Schedule: a persistent CTA per SM walks windows of 8 tokens (window w, w +
-// gridDim.x, ...) and, inside a window, column chunks of its rows.
-//   producer warp   For a window it reads the 8*K positions of the window's
-//                   (token, slot) pairs from token_index_map, ranks them
-//                   ascending (expert-major order, the order in which the
-//                   grouped expert GEMM walks its rows) and looks each one up
-//                   in expert_token_indices: routed row r of the window is
-//                   token D1[pos_r].  For every column chunk it then copies
-//                   each routed row's chunk, in that order, into a ring stage
-//                   with one bulk TMA copy per row (cp.async.bulk, completion
-//                   counted in bytes on the stage's mbarrier).  The next
-//                   window's positions are fetched while the current one is
-//                   copied.
-//   8 consumer warps  Warp j owns token j of the window: per chunk it sums
-//                   the staged rows of token j times their gates (packed
-//                   fp32x2 FMAs, fp32 accumulation) and writes its output
-//                   chunk once with 16-byte stores.
-// Each routed row is fetched through expert_token_indices; the K fetches of a
-// token's row fall in one window, so the repeats after the first are served
-// by L2.  No atomics; the routed (L*K, d) buffer never exists.  Every
-// mbarrier wait is bounded (globaltimer): on expiry the CTA records
-// kErrTimeout, lets its copies in flight land (bounded) and returns.
+// Schedule: one CTA per window of 8 tokens, all columns.  The window's 8*K
+// (token, slot) positions are read from token_index_map and ranked
+// ascending, which is expert-major order restricted to the window (the order
+// the grouped expert GEMM walks its rows).  Like the GEMM path's producer,
+// the CTA then gathers those routed rows, through expert_token_indices and in
+// that order, into a shared-memory tile with 16-byte cp.async (one 1 KB
+// column chunk of every routed row per stage, two stages in flight); like its
+// epilogue, it then combines: every output piece sums the staged slots of its
+// row times their gates (packed fp32x2 FMAs, fp32 accumulation) and is
+// written once.  A thread copies and combines the same 16-byte column piece
+// of its rows in every chunk, so its source, shared-memory and output
+// addresses are computed once per window.  No atomics; each output row is
+// written once; the K routed rows of a token fall inside one CTA, so HBM
+// serves each source row once and L2 the repeats; the routed (L*K, d) buffer
+// never exists.
 #include <climits>
 
 #include "common.cuh"
@@ -33,38 +26,12 @@
 namespace moeblaze {
 namespace {
 
-constexpr int kWin = 8;                                // tokens per window (one consumer warp each)
-constexpr int kConsumerWarps = kWin;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + the producer warp
-constexpr int kStageBytes = 64 * 1024;                 // routed-row chunks of one window per stage
-constexpr int kStages = 3;
-constexpr uint64_t kTimeoutNs = 4000000000ull;
-constexpr uint64_t kDrainNs = 100000000ull;
-
-// Per stage, written by the producer before the stage's full barrier
-// completes: which staged rows (and gates) belong to each token of the window.
-struct StageDesc {
-  int32_t nslot[kWin];
-  int16_t slot[kWin][kMaxK];
-  float gate[kWin][kMaxK];
-};
-constexpr int kDescBytes = (sizeof(StageDesc) + 15) / 16 * 16;
-constexpr size_t kSmemBytes = 128 + (size_t)kStages * kStageBytes + (size_t)kStages * kDescBytes + 2 * kStages * 8 + 16;
-
-struct IdParams {
-  const uint8_t* src;   // (L, row_bytes): x (forward) or dY (backward)
-  uint8_t* dst;         // (L, row_bytes): y or dX
-  const int32_t* D1;
-  const int32_t* D4;
-  const float* gates;
-  const int32_t* hdr;
-  int32_t* err;
-  int64_t L, LK, nwin;
-  int E, K;
-  int row_bytes;        // d * element size (a multiple of 16)
-  int cb;               // bytes of a row per column chunk (a multiple of 16)
-  int nch;              // column chunks per row
-};
+constexpr int kWin = 8;            // tokens per CTA
+constexpr int kThreads = 256;
+constexpr int kChunkBytes = 1024;  // bytes of one routed row per column chunk
+constexpr int kStages = 2;         // column chunks in flight per CTA
+constexpr int kPieces = kChunkBytes / 16;        // 16-byte pieces of a row chunk
+constexpr int kRowsPerPass = kThreads / kPieces;  // rows the block covers per pass (4)
 
 template <typename T>
 struct Vec;
@@ -103,261 +70,146 @@ struct Vec<float> {
   }
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of `parity` of `bar`: false on expiry (the CTA's
-// abort flag and the device error word are set) or once another role of the
-// CTA has given up (abort_s set).
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int32_t* err,
-                                             uint64_t limit_ns = kTimeoutNs) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (abort_s && *abort_s) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        if (abort_s) *abort_s = 1;
-        if (err) atomicOr(err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-// one routed-row chunk, global -> shared, completion counted on `bar`
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// The producer's view of one window: lane l holds routed rows i = l and
-// i = l + 32 of the window (i = (token - t0) * K + slot) in unranked order.
-struct WinRows {
-  int32_t pos[2];   // position in expert_token_indices (-1: no such row)
-  float g[2];
-  int32_t rank[2];  // staged row: place in ascending position order (expert-major)
-  int32_t tok[2];   // token - t0 by expert_token_indices (-1: not staged)
-  int32_t m[2];     // place among the staged rows of the same token, by rank
-  int32_t cnt;      // lanes < kWin: staged rows of token `lane`
-  int32_t nvalid;   // staged rows of the window (same in every lane)
-};
+// KM: the largest K this instance handles (4 or kMaxK), which sizes the
+// per-thread address tables held in registers.
+template <typename T, int KM>
+__global__ void __launch_bounds__(kThreads) identity_combine_kernel(const T* __restrict__ src,
+                                                                    const int32_t* __restrict__ D1,
+                                                                    const int32_t* __restrict__ D4,
+                                                                    const float* __restrict__ gates,
+                                                                    T* __restrict__ dst, int64_t L, int d, int K,
+                                                                    int64_t LK, const int32_t* __restrict__ hdr,
+                                                                    int E, int32_t* err) {
+  constexpr int V = Vec<T>::N;                 // elements per 16-byte piece
+  constexpr int CH = kChunkBytes / sizeof(T);  // columns per chunk
+  constexpr int kGatherIt = kWin * KM / kRowsPerPass;  // routed rows a thread copies (per chunk)
+  constexpr int kCombineIt = kWin / kRowsPerPass;      // output rows a thread writes (per chunk)
+  extern __shared__ __align__(16) uint8_t stage[];  // [kStages][n][kChunkBytes]
+  __shared__ int32_t pos_in[kWin * kMaxK], pos_s[kWin * kMaxK], tok_s[kWin * kMaxK];
+  __shared__ float g_in[kWin * kMaxK], g_s[kWin * kMaxK];
+  __shared__ int32_t slot_of[kWin][kMaxK];
+  __shared__ float gate_of[kWin][kMaxK];
+  __shared__ int32_t nslot[kWin];
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) identity_combine_kernel(const __grid_constant__ IdParams p) {
-  constexpr int V = Vec<T>::N;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + (size_t)kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes + (size_t)kStages * kDescBytes);
-  volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 2 * kStages);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
+  const int tid = threadIdx.x;
+  const int64_t t0 = (int64_t)blockIdx.x * kWin;
+  const int n = kWin * K;
   // a dispatch built for another (L, E, K): record it and read none of its maps
-  // (the same three header words in every thread: the CTA leaves together)
-  if (!meta_matches(p.hdr, p.L, p.E, p.K)) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrShapeMismatch);
+  if (!meta_matches(hdr, L, E, K)) {
+    if (tid == 0) atomicOr(err, kErrShapeMismatch);
     return;
   }
-  auto full = [&](int s) { return smem_u32(bars + s); };
-  auto empty = [&](int s) { return smem_u32(bars + kStages + s); };
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), kConsumerWarps);
+  if (tid < n) {
+    const int64_t t = t0 + tid / K;
+    int32_t p = INT_MAX;
+    float g = 0.f;
+    if (t < L) {
+      const int32_t q = D4[t * K + (tid % K)];
+      if (q >= 0 && q < LK) { p = q; g = gates[t * K + (tid % K)]; }
     }
-    *abort_s = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    pos_in[tid] = p;
+    g_in[tid] = g;
+  }
+  __syncthreads();
+  if (tid < n) {  // rank = place in ascending position order (expert-major)
+    const int32_t p = pos_in[tid];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += (pos_in[j] < p) || (pos_in[j] == p && j < tid);
+    pos_s[r] = p;
+    g_s[r] = g_in[tid];
+  }
+  __syncthreads();
+  if (tid < n) {  // the gather index; entries outside the window are dropped
+    const int32_t tok = (pos_s[tid] != INT_MAX) ? D1[pos_s[tid]] : -1;
+    tok_s[tid] = (tok >= 0 && tok < L && tok - t0 >= 0 && tok - t0 < kWin) ? (int32_t)(tok - t0) : -1;
+  }
+  __syncthreads();
+  if (tid < kWin) {  // the staged slots (expert-major) that belong to window row tid
+    int m = 0;
+    for (int i = 0; i < n; ++i)
+      if (tok_s[i] == tid && m < kMaxK) { slot_of[tid][m] = i; gate_of[tid][m] = g_s[i]; ++m; }
+    nslot[tid] = m;
   }
   __syncthreads();
 
-  const int n = kWin * p.K;  // routed rows of a window
-  const uint32_t stage0 = smem_u32(smem);
-
-  if (warp == kConsumerWarps) {
-    // ================================================================ producer
-    // first half of a window's preparation: its positions and gates
-    auto load_rows = [&](int64_t w, WinRows& R) {
-      const int64_t t0 = w * kWin;
+  // This thread's 16-byte piece `off` of every row chunk, and the rows it
+  // handles: routed rows r0, r0 + 4, ... (gather) and window rows r0, r0 + 4
+  // (combine).  Their addresses are fixed for the whole window.
+  const int off = tid % kPieces;
+  const int r0 = tid / kPieces;
+  const int dp = (int)(((int64_t)d * sizeof(T)) / 16);  // 16-byte pieces of a row
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+  const T* gsrc[kGatherIt];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = lane + 32 * h;
-        R.pos[h] = -1;
-        R.g[h] = 0.f;
-        if (i < n && t0 + i / p.K < p.L) {
-          const int32_t q = p.D4[t0 * p.K + i];
-          if (q >= 0 && q < p.LK) {
-            R.pos[h] = q;
-            R.g[h] = p.gates[t0 * p.K + i];
-          }
-        }
-      }
-    };
-    // second part: the gather index of each routed row (loads issued here,
-    // used in rank_b) and its expert-major rank
-    auto rank_a = [&](WinRows& R, int32_t* tt) {
-      int32_t key[2];
+  for (int it = 0; it < kGatherIt; ++it) {
+    const int i = r0 + kRowsPerPass * it;
+    gsrc[it] = (i < n && tok_s[i] >= 0) ? src + (t0 + tok_s[i]) * d + off * V : nullptr;
+  }
+  int ns[kCombineIt];
+  uint32_t soff[kCombineIt][KM];
+  float2 sg[kCombineIt][KM];
+  T* ydst[kCombineIt];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        key[h] = R.pos[h] >= 0 ? R.pos[h] : INT_MAX;
-        tt[h] = R.pos[h] >= 0 ? p.D1[R.pos[h]] : -1;  // expert_token_indices: the token of this routed row
-        R.rank[h] = 0;
-      }
-      for (int j = 0; j < n; ++j) {
-        const int32_t kj = __shfl_sync(0xffffffffu, j < 32 ? key[0] : key[1], j & 31);
+  for (int it = 0; it < kCombineIt; ++it) {
+    const int j = r0 + kRowsPerPass * it;
+    ns[it] = (t0 + j < L) ? min(nslot[j], KM) : 0;
+    ydst[it] = dst + (t0 + j) * d + off * V;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = lane + 32 * h;
-          R.rank[h] += (kj < key[h]) || (kj == key[h] && j < i);
-        }
-      }
-    };
-    // third part: rows whose token lies in the window are staged; the
-    // per-token lists in rank order
-    auto rank_b = [&](int64_t w, WinRows& R, const int32_t* tt) {
-      const int64_t t0 = w * kWin;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        R.tok[h] = -1;
-        if (R.pos[h] >= 0 && (int64_t)tt[h] >= t0 && (int64_t)tt[h] < t0 + kWin && (int64_t)tt[h] < p.L)
-          R.tok[h] = (int32_t)(tt[h] - t0);
-      }
-      R.m[0] = R.m[1] = 0;
-      R.cnt = 0;
-      int nv = 0;
-      for (int j = 0; j < n; ++j) {
-        const int32_t tj = __shfl_sync(0xffffffffu, j < 32 ? R.tok[0] : R.tok[1], j & 31);
-        const int32_t rj = __shfl_sync(0xffffffffu, j < 32 ? R.rank[0] : R.rank[1], j & 31);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (R.tok[h] >= 0 && tj == R.tok[h] && rj < R.rank[h]) ++R.m[h];
-        R.cnt += (tj == lane);
-        nv += (tj >= 0);
-      }
-      R.nvalid = nv;
-    };
-
-    int s = 0;
-    uint32_t ph = 0;
-    uint32_t armed = 0, armed_par = 0;  // stages with copies issued, and the parity they complete
-    bool ok = true;
-    WinRows cur, nxt;
-    int32_t tt[2];
-    int64_t w = blockIdx.x;
-    if (w < p.nwin) {
-      load_rows(w, cur);
-      rank_a(cur, tt);
-      rank_b(w, cur, tt);
-    }
-    // the next window is prepared in three parts spread over this window's
-    // chunks, so the latency of its index loads hides behind the copies
-    const int c_b = p.nch > 1 ? 1 : 0;
-    for (; ok && w < p.nwin; w += gridDim.x) {
-      const int64_t wn = w + gridDim.x;
-      if (wn < p.nwin) load_rows(wn, nxt);  // lands while this window's chunks are issued
-      const int64_t t0 = w * kWin;
-      for (int c = 0; c < p.nch; ++c) {
-        bool got = true;
-        if (lane == 0) got = wait_bounded(empty(s), ph ^ 1u, abort_s, p.err);
-        ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int bytes = min(p.cb, p.row_bytes - c * p.cb);
-        StageDesc& D = desc[s];
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (cur.tok[h] >= 0 && cur.m[h] < kMaxK) {
-            D.slot[cur.tok[h]][cur.m[h]] = (int16_t)cur.rank[h];
-            D.gate[cur.tok[h]][cur.m[h]] = cur.g[h];
-          }
-        if (lane < kWin) D.nslot[lane] = min(cur.cnt, kMaxK);
-        __syncwarp();  // the descriptor writes come before lane 0's arrive (release)
-        if (lane == 0) mbar_arrive_expect_tx(full(s), (uint32_t)(cur.nvalid * bytes));
-        __syncwarp();
-        const uint32_t dst = stage0 + (uint32_t)s * kStageBytes;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (cur.tok[h] >= 0)
-            bulk_g2s(dst + (uint32_t)(cur.rank[h] * p.cb), p.src + (t0 + cur.tok[h]) * p.row_bytes + (int64_t)c * p.cb,
-                     (uint32_t)bytes, full(s));
-        armed |= 1u << s;
-        armed_par = (armed_par & ~(1u << s)) | (ph << s);
-        if (++s == kStages) { s = 0; ph ^= 1u; }
-        if (c == 0 && wn < p.nwin) rank_a(nxt, tt);
-        if (c == c_b && wn < p.nwin) rank_b(wn, nxt, tt);
-      }
-      if (ok && wn < p.nwin) cur = nxt;
-    }
-    if (!ok) {
-      // let the copies already issued land before the CTA's shared memory goes away
-      if (lane == 0)
-        for (int i = 0; i < kStages; ++i)
-          if (armed & (1u << i)) wait_bounded(full(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
-      __syncwarp();
-    }
-  } else {
-    // ================================================================ consumers
-    const int j = warp;  // token j of each window
-    int s = 0;
-    uint32_t ph = 0;
-    for (int64_t w = blockIdx.x; w < p.nwin; w += gridDim.x) {
-      const int64_t t = w * kWin + j;
-      bool ok = true;
-      for (int c = 0; c < p.nch; ++c) {
-        bool got = true;
-        if (lane == 0) got = wait_bounded(full(s), ph, abort_s, p.err);
-        ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int bytes = min(p.cb, p.row_bytes - c * p.cb);
-        if (t < p.L) {
-          const StageDesc& D = desc[s];
-          const int ns = D.nslot[j];
-          uint32_t base[kMaxK];
-          float2 g2[kMaxK];
-#pragma unroll
-          for (int m = 0; m < kMaxK; ++m) {
-            base[m] = (uint32_t)D.slot[j][m] * p.cb;
-            g2[m] = make_float2(D.gate[j][m], D.gate[j][m]);
-          }
-          const uint8_t* stg = smem + (size_t)s * kStageBytes;
-          uint8_t* out = p.dst + t * p.row_bytes + (int64_t)c * p.cb;
-          for (int q = lane * 16; q < bytes; q += 32 * 16) {
-            float2 acc[V / 2];
-#pragma unroll
-            for (int i = 0; i < V / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < kMaxK; ++m)
-              if (m < ns) Vec<T>::fma(*reinterpret_cast<const uint4*>(stg + base[m] + q), g2[m], acc);
-            *reinterpret_cast<uint4*>(out + q) = Vec<T>::pack(acc);
-          }
-        }
-        __syncwarp();  // every lane has read the stage
-        if (lane == 0) mbar_arrive(empty(s));
-        if (++s == kStages) { s = 0; ph ^= 1u; }
-      }
-      if (!ok) break;
+    for (int m = 0; m < KM; ++m) {
+      soff[it][m] = (uint32_t)slot_of[j][m] * kChunkBytes + off * 16;
+      sg[it][m] = make_float2(gate_of[j][m], gate_of[j][m]);
     }
   }
+  const int nchunks = (d + CH - 1) / CH;
+  // gather: this thread's pieces of the n routed rows of chunk c, in
+  // expert-major row order, into buffer c % kStages
+  auto gather = [&](int c) {
+    const uint32_t buf = sbase + (uint32_t)((c % kStages) * n * kChunkBytes + r0 * kChunkBytes + off * 16);
+    if (c * kPieces + off < dp) {
+#pragma unroll
+      for (int it = 0; it < kGatherIt; ++it)
+        if (gsrc[it]) cp_async16(buf + it * kRowsPerPass * kChunkBytes, gsrc[it] + (int64_t)c * CH);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // combine: each output piece sums its row's staged slots with their gates
+  auto combine = [&](int c) {
+    if (c * kPieces + off >= dp) return;
+    const uint8_t* buf = stage + (c % kStages) * n * kChunkBytes;
+#pragma unroll
+    for (int it = 0; it < kCombineIt; ++it) {
+      if (ns[it] == 0) continue;
+      float2 acc[V / 2];
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < KM; ++m)
+        if (m < ns[it]) Vec<T>::fma(*reinterpret_cast<const uint4*>(buf + soff[it][m]), sg[it][m], acc);
+      *reinterpret_cast<uint4*>(ydst[it] + (int64_t)c * CH) = Vec<T>::pack(acc);
+    }
+  };
+  // kStages chunks in flight while chunk c is awaited; one commit group per
+  // chunk (empty past the end)
+#pragma unroll
+  for (int c = 0; c < kStages - 1; ++c) {
+    if (c < nchunks) gather(c);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    // chunk c + kStages - 1 goes into the buffer chunk c - 1 used (combined
+    // before the trailing barrier of the previous iteration)
+    if (c + kStages - 1 < nchunks) gather(c + kStages - 1);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+    __syncthreads();  // chunk c landed for every thread
+    combine(c);
+    __syncthreads();  // chunk c's buffer may be refilled
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // Gate gradients of the identity expert: dg[t,k] = <dY[t], x[t]> for every
@@ -403,38 +255,30 @@ moeblaze_status launch_identity_dgates(const moeblaze_shape& s, const void* x, c
 moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,
                                         const float* gates, void* dst, cudaStream_t st) {
   if (s.L == 0) return MOEBLAZE_OK;
+  const int64_t LK = s.L * s.K;
   const MetaView meta = meta_view(disp.meta, s.E);
-  IdParams p;
-  p.src = reinterpret_cast<const uint8_t*>(src);
-  p.dst = reinterpret_cast<uint8_t*>(dst);
-  p.D1 = disp.expert_token_indices;
-  p.D4 = disp.token_index_map;
-  p.gates = gates;
-  p.hdr = meta.hdr;
-  p.err = meta.err;
-  p.L = s.L;
-  p.LK = s.L * s.K;
-  p.nwin = (s.L + kWin - 1) / kWin;
-  p.E = s.E;
-  p.K = s.K;
-  p.row_bytes = s.d * (s.dtype == MOEBLAZE_BF16 ? 2 : 4);  // a multiple of 16 (checked by the ABI)
-  // a stage holds one column chunk of the window's 8*K routed rows
-  const int n = kWin * s.K;
-  p.cb = (kStageBytes / n) / 16 * 16;
-  if (p.cb > p.row_bytes) p.cb = p.row_bytes;
-  p.nch = (p.row_bytes + p.cb - 1) / p.cb;
-  const int64_t g64 = p.nwin < sm_count() ? p.nwin : sm_count();
-  const dim3 grid((unsigned)g64);
+  const dim3 grid((unsigned)((s.L + kWin - 1) / kWin));
+  const size_t smem = kStages * (size_t)kWin * s.K * kChunkBytes;
+  // one instance per element type and K range (the address tables are sized by the largest K)
+  auto run = [&](auto kern, const auto* in, auto* out) -> moeblaze_status {
+    MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    kern<<<grid, kThreads, smem, st>>>(in, disp.expert_token_indices, disp.token_index_map, gates, out, s.L, s.d, s.K,
+                                       LK, meta.hdr, s.E, meta.err);
+    MB_CUDA(cudaGetLastError());
+    return MOEBLAZE_OK;
+  };
+  moeblaze_status r;
   if (s.dtype == MOEBLAZE_BF16) {
-    auto k = identity_combine_kernel<__nv_bfloat16>;
-    MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
-    k<<<grid, kThreads, kSmemBytes, st>>>(p);
+    const auto* in = reinterpret_cast<const __nv_bfloat16*>(src);
+    auto* out = reinterpret_cast<__nv_bfloat16*>(dst);
+    r = s.K <= 4 ? run(identity_combine_kernel<__nv_bfloat16, 4>, in, out)
+                 : run(identity_combine_kernel<__nv_bfloat16, kMaxK>, in, out);
   } else {
-    auto k = identity_combine_kernel<float>;
-    MB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
-    k<<<grid, kThreads, kSmemBytes, st>>>(p);
+    const auto* in = reinterpret_cast<const float*>(src);
+    auto* out = reinterpret_cast<float*>(dst);
+    r = s.K <= 4 ? run(identity_combine_kernel<float, 4>, in, out) : run(identity_combine_kernel<float, kMaxK>, in, out);
   }
-  MB_CUDA(cudaGetLastError());
+  if (r != MOEBLAZE_OK) return r;
   count_launch();
   return MOEBLAZE_OK;
 }
