@@ -449,8 +449,62 @@ def run_ours(args, rank, world, local_rank):
         out["router"] = run_router(cfg, inp, dev, flush, pk)
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, cfg, layer, inp, dev, world)
-    del flush, layer
+    del layer
+    torch.cuda.empty_cache()
+    if not identity and cfg.dtype == "bf16" and not args.no_recompute_leg:
+        out["recompute_h"] = run_recompute_leg(args, cfg, inp, dev, flush, pk, tpk)
+    del flush
     return out, inp
+
+
+def run_recompute_leg(args, cfg, inp, dev, flush, pk, tpk):
+    """The same step with MOEBLAZE_RECOMPUTE_H (no H / Hg temporaries; the
+    down projection and dW3 recompute them from the saved A, B): step time,
+    GEMM stage times and activation memory, beside the default above."""
+    from mixture_experts_atomic_gb300.layer import MoELayer
+    layer = MoELayer.for_config(cfg, dev, with_dgates=False, recompute_h=True)
+    W = (inp.get("W1"), inp.get("W2"), inp.get("W3"))
+
+    def step():
+        layer.dispatch(inp["ids"])
+        layer.forward(inp["x"], inp["gates"], *W)
+        layer.backward(inp["dY"], inp["x"], inp["gates"], *W)
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    n = min(args.steps, 10)
+    names_f, names_b = ["up", "down", "convert_y"], ["dh", "dx", "dw12", "dw3", "convert_dx"]
+    per = {k: [] for k in names_f + names_b}
+    tot = []
+    for _ in range(n):
+        flush_l2(flush)
+        fw, bw = B.StageEvents(4), B.StageEvents(6)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.dispatch(inp["ids"])
+        with fw:
+            layer.forward(inp["x"], inp["gates"], *W)
+        with bw:
+            layer.backward(inp["dY"], inp["x"], inp["gates"], *W)
+        e1.record()
+        torch.cuda.synchronize()
+        tot.append(e0.elapsed_time(e1))
+        for k, v in zip(names_f, fw.elapsed_ms()):
+            per[k].append(v)
+        for k, v in zip(names_b, bw.elapsed_ms()):
+            per[k].append(v)
+    assert layer.device_error() == 0, "device error in the recompute leg"
+    stages = {k: statistics.mean(v) for k, v in per.items()}
+    fl = stage_flops(cfg)
+    ms = statistics.mean(tot)
+    out = {"ms_per_step": ms, "value": cfg.L / (ms * 1e-3), "unit": "tokens/s", "steps": n, "stages_ms": stages,
+           "tflops": {k: fl[k] / (stages[k] * 1e-3) / 1e12 for k in fl},
+           "frac_of_peak": {k: fl[k] / (stages[k] * 1e-3) / 1e12 / tpk for k in fl},
+           "activation_memory": memory_report(cfg, layer, 0)}
+    del layer
+    torch.cuda.empty_cache()
+    return out
 
 
 def identity_roofline(cfg, t_ms, pk, src):
@@ -674,6 +728,8 @@ def main():
     ap.add_argument("--clock-log", default=None,
                     help="keep the raw nvidia-smi clock samples of the timed region at this path ({rank} is replaced)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-recompute-leg", action="store_true",
+                    help="skip timing the step again with MOEBLAZE_RECOMPUTE_H (no H / Hg temporaries)")
     ap.add_argument("--only", choices=["dispatch"], default=None,
                     help="time only the dispatch build of the workload (allocates only its routing and index buffers)")
     args = ap.parse_args()

@@ -62,13 +62,27 @@ enum { MOEBLAZE_F32 = 0, MOEBLAZE_BF16 = 1 };
 enum { MOEBLAZE_SWIGLU = 0, MOEBLAZE_SILU = 1, MOEBLAZE_IDENTITY = 2 };
 
 /* Layer shape.  L tokens, model dim d, expert hidden dim h (ignored for the
- * identity expert), E experts, top-K slots per token. */
+ * identity expert), E experts, top-K slots per token, and option flags. */
 typedef struct {
   int64_t L;
   int32_t d, h, E, K;
   int32_t dtype;  /* MOEBLAZE_F32 | MOEBLAZE_BF16 */
   int32_t act;    /* MOEBLAZE_SWIGLU | MOEBLAZE_SILU | MOEBLAZE_IDENTITY */
+  int32_t flags;  /* 0 or MOEBLAZE_RECOMPUTE_H; other bits: MOEBLAZE_ERR_INVALID_ARG */
 } moeblaze_shape;
+
+/* MOEBLAZE_RECOMPUTE_H: keep no H = SiLU(A)*B (SiLU: SiLU(A)) and no
+ * Hg = g*H temporary (MoEBlaze, awesome-system-papers page, section
+ * "SwiGLU kernel 融合 + activation checkpoint": the fused kernels write only
+ * their final outputs).  Applies to the bf16 SwiGLU and SiLU layers (ignored
+ * otherwise): the down projection and the dW3 GEMM then recompute H and Hg
+ * tile by tile from the saved A and B inside their operand pipelines.  The
+ * forward and the backward workspace each shrink by padded_rows x h
+ * elements (the backward keeps one fp32 gate per padded row instead); those
+ * two GEMMs do the extra recompute.  Results agree with the default within
+ * the bf16 tolerance (SiLU is then evaluated as a/2 (1 + tanh(a/2)) with the
+ * hardware tanh approximation). */
+#define MOEBLAZE_RECOMPUTE_H 1
 
 /* The index structures of MoEBlaze (awesome-system-papers page, section
  * "免物化 token dispatch", data-structure table).  All device, int32,

@@ -39,7 +39,11 @@ STATIC_SCRATCH_BYTES = 8 << 20
 
 class Shape(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+# moeblaze_shape.flags
+RECOMPUTE_H = 1
 
 
 class Dispatch(ctypes.Structure):
@@ -191,10 +195,10 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_shape(L, d, h, E, K, dtype, act) -> Shape:
+def make_shape(L, d, h, E, K, dtype, act, flags: int = 0) -> Shape:
     dt = DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     a = ACT[act] if isinstance(act, str) else int(act)
-    return Shape(int(L), int(d), int(h), int(E), int(K), dt, a)
+    return Shape(int(L), int(d), int(h), int(E), int(K), dt, a, int(flags))
 
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}

@@ -46,6 +46,7 @@ moeblaze_status check_shape(const moeblaze_shape* s) {
   if (s->act != MOEBLAZE_SWIGLU && s->act != MOEBLAZE_SILU && s->act != MOEBLAZE_IDENTITY)
     return MOEBLAZE_ERR_INVALID_ARG;
   if (s->act != MOEBLAZE_IDENTITY && s->h < 1) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->flags & ~MOEBLAZE_RECOMPUTE_H) return MOEBLAZE_ERR_INVALID_ARG;
   if (s->E > kMaxE || s->K > kMaxK) return MOEBLAZE_ERR_UNSUPPORTED;
   if (s->L * (int64_t)s->K + (int64_t)s->E * kRowPad >= (int64_t(1) << 31)) return MOEBLAZE_ERR_UNSUPPORTED;
   if (s->act == MOEBLAZE_IDENTITY) {
@@ -83,20 +84,31 @@ moeblaze_status check_router_shape(const moeblaze_shape* s) {
 size_t elem(const moeblaze_shape* s) { return s->dtype == MOEBLAZE_BF16 ? 2 : 4; }
 int nbranch(const moeblaze_shape* s) { return s->act == MOEBLAZE_SWIGLU ? 2 : 1; }
 
-// forward scratch: H (rows x h) | y32 (L x d fp32) + tile counters (bf16 only)
-// backward scratch: dAB (rows x nb*h) | Hg (rows x h) | dX32 (L x d fp32) + tile counters (bf16 only)
+// MOEBLAZE_RECOMPUTE_H applies to the bf16 expert layers: H and Hg are then
+// recomputed from the saved A, B inside the down-projection and dW3 GEMMs
+// and never stored.
+bool recompute_h(const moeblaze_shape* s) {
+  return s->dtype == MOEBLAZE_BF16 && s->act != MOEBLAZE_IDENTITY && (s->flags & MOEBLAZE_RECOMPUTE_H);
+}
+
+// forward scratch:  H (rows x h; not when recomputed) | y32 (L x d fp32) + tile counters (bf16 only)
+// backward scratch: dAB (rows x nb*h) | Hg (rows x h), or the row gates (rows fp32) when recomputed
+//                   | dX32 (L x d fp32) + tile counters (bf16 only)
 size_t fwd_ws(const moeblaze_shape* s) {
   if (s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
-  size_t b = align_up((size_t)rows * s->h * elem(s), 256);
+  size_t b = recompute_h(s) ? 0 : align_up((size_t)rows * s->h * elem(s), 256);
   if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
   return b;
+}
+size_t hg_bytes(const moeblaze_shape* s) {
+  const int64_t rows = max_padded_rows(s->L * s->K, s->E);
+  return recompute_h(s) ? align_up((size_t)rows * 4, 256) : align_up((size_t)rows * s->h * elem(s), 256);
 }
 size_t bwd_ws(const moeblaze_shape* s) {
   if (s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
-  size_t b = align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256);
-  b += align_up((size_t)rows * s->h * elem(s), 256);
+  size_t b = align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256) + hg_bytes(s);
   if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
   return b;
 }
@@ -220,11 +232,11 @@ moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const f
     return simt_forward(*s, (const float*)x, gates, *disp, (const float*)W1, sw ? (const float*)W2 : nullptr,
                         (const float*)W3, (float*)y, (float*)saved, (float*)w, st);
   }
-  __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(w);
-  float* y32 = reinterpret_cast<float*>(w + align_up((size_t)rows * s->h * 2, 256));
+  const size_t hb = recompute_h(s) ? 0 : align_up((size_t)rows * s->h * 2, 256);
+  __nv_bfloat16* H = hb ? reinterpret_cast<__nv_bfloat16*>(w) : nullptr;
   return tc_forward(*s, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
                     sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (__nv_bfloat16*)y,
-                    (__nv_bfloat16*)saved, H, y32, st);
+                    (__nv_bfloat16*)saved, H, reinterpret_cast<float*>(w + hb), st);
 }
 
 moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x, const float* gates,
@@ -254,17 +266,19 @@ moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const
   char* w = reinterpret_cast<char*>(ws);
   const size_t es = elem(s);
   char* dAB = w;
-  char* Hg = w + align_up((size_t)rows * nbranch(s) * s->h * es, 256);
-  char* dX32 = Hg + align_up((size_t)rows * s->h * es, 256);
+  char* Hg = w + align_up((size_t)rows * nbranch(s) * s->h * es, 256);  // Hg, or the row gates when recomputed
   if (s->dtype == MOEBLAZE_F32) {
     return simt_backward(*s, (const float*)dY, (const float*)x, gates, *disp, (const float*)W1,
                          sw ? (const float*)W2 : nullptr, (const float*)W3, (const float*)saved, (float*)dX,
                          (float*)dW1, sw ? (float*)dW2 : nullptr, (float*)dW3, dgates, (float*)dAB, (float*)Hg, st);
   }
+  char* dX32 = Hg + hg_bytes(s);
+  const bool rec = recompute_h(s);
   return tc_backward(*s, (const __nv_bfloat16*)dY, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
                      sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (const __nv_bfloat16*)saved,
                      (__nv_bfloat16*)dX, (__nv_bfloat16*)dW1, sw ? (__nv_bfloat16*)dW2 : nullptr, (__nv_bfloat16*)dW3,
-                     dgates, (__nv_bfloat16*)dAB, (__nv_bfloat16*)Hg, (float*)dX32, st);
+                     dgates, (__nv_bfloat16*)dAB, rec ? nullptr : (__nv_bfloat16*)Hg, rec ? (float*)Hg : nullptr,
+                     (float*)dX32, st);
 }
 
 moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp, int32_t* code,

@@ -113,16 +113,18 @@ moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const fl
                               const float* saved, float* dX, float* dW1, float* dW2, float* dW3, float* dgates,
                               float* wsdAB, float* wsHg, cudaStream_t st);
 
-// gemm_tc.cu (bf16 tensor-core path)
+// gemm_tc.cu (bf16 tensor-core path).  wsH / wsHg NULL selects the
+// recompute variants (MOEBLAZE_RECOMPUTE_H); wsRowg is used only by them.
 moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, const float* gates,
                            const moeblaze_dispatch& disp, const __nv_bfloat16* W1, const __nv_bfloat16* W2,
-                           const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved,
-                           __nv_bfloat16* wsH, float* wsY32, cudaStream_t st);
+                           const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved, __nv_bfloat16* wsH,
+                           float* wsY32, cudaStream_t st);
 moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, const __nv_bfloat16* x,
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
                             const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
+                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsRowg, float* wsdX32,
+                            cudaStream_t st);
 
 // router.cu
 constexpr int kMaxRouterE = 256;

@@ -26,13 +26,26 @@
 // gather a valid token and are zero where they feed a reduction.
 //
 // Stage                          A (M x K)                B (K x N)             epilogue
-//  UP_SWIGLU  a,b = X W1,X W2    x rows via D1 (gather)   [W1_e | W2_e] tiles   A,B (saved), H=SiLU(a)b
-//  UP_SILU    a = X W1           x rows via D1            W1_e                  A (saved), H=SiLU(a)
-//  DOWN       Y = H W3           H rows                   W3_e                  y32[t] += g Y   (red.add)
-//  DH_*       dH = dY W3^T       dY rows via D1           W3_e (K-major)        dA, dB, Hg (SwiGLU bwd)
+//  UP_SWIGLU  a,b = X W1,X W2    x rows via D1 (gather)   [W1_e | W2_e] tiles   A, B (saved)
+//  UP_SILU    a = X W1           x rows via D1            W1_e                  A (saved)
+//  DOWN_H     Y = H W3           H rows                   W3_e                  y32[t] += g Y   (red.add)
+//  DOWN_*     Y = H W3           H = SiLU(A)*B, from      W3_e                  y32[t] += g Y   (red.add)
+//                                the saved A, B tiles
+//  DH_*       dH = dY W3^T       dY rows via D1           W3_e (K-major)        dA, dB (SwiGLU bwd), Hg or row gates
 //  DX         [dA|dB][W1|W2]^T   dAB rows                 W1_e^T then W2_e^T    dX32[t] += .    (red.add)
 //  DW12/DW1   X^T [dA|dB]        x rows via D1 along K    dAB rows (MN-major)   dW1, dW2
-//  DW3        Hg^T dY            Hg rows (MN-major)       dY rows via D1        dW3
+//  DW3_H      Hg^T dY            Hg rows (MN-major)       dY rows via D1        dW3
+//  DW3_*      Hg^T dY            Hg = g*SiLU(A)*B, from   dY rows via D1        dW3
+//                                the saved A, B (MN-major)
+//
+// By default the up-projection epilogue stores H = SiLU(a) b and the dH
+// epilogue Hg = g SiLU(A) B for the down projection and dW3.  With
+// MOEBLAZE_RECOMPUTE_H neither is ever written to global memory: DOWN_* and
+// DW3_* load the saved A (and B) tiles by TMA and eight transform warps
+// recompute the A operand in shared memory, in place, before the tensor
+// cores read it (SiLU(a) = a/2 (1 + tanh(a/2)) with tanh.approx).  Each
+// stage of the SwiGLU variants also holds the saved-B tile, so their ring
+// has 3 stages of 64 KB.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // kErrTimeout in the device error word, drains its own copies and MMAs with
@@ -50,16 +63,13 @@ constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
 constexpr int PRODUCER_WARPS = 4;
 constexpr int PRODUCER_THREADS = PRODUCER_WARPS * 32;
-constexpr int MMA_WARP = PRODUCER_WARPS;
-constexpr int NUM_THREADS = (PRODUCER_WARPS + 1 + 4) * 32;  // producers, MMA, 4 epilogue warps
-constexpr int LAG = STAGES - 2;               // cp.async groups a producer thread keeps in flight
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
 // epilogue staging for TMA stores: per epilogue warp a ring of EPI_RING
 // buffers of 32 rows x 32 bf16 (64-byte swizzle)
 constexpr int EPI_RING = 4;
 constexpr int EPI_BUF_BYTES = 32 * 64;
 constexpr int EPI_STAGE_BYTES = 4 * EPI_RING * EPI_BUF_BYTES;  // 32 KB
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 256;
+constexpr int BAR_BYTES = 512;                // mbarriers, TMEM address, abort flag, tile queue
 // Tiles are claimed dynamically: each CTA takes its first two tiles by its
 // index and every further one from a global counter, two tiles ahead of
 // use, and passes the ids to its MMA and epilogue warps through a queue of
@@ -68,9 +78,36 @@ constexpr int TQ = 8;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
-enum Mode : int { UP_SWIGLU = 0, UP_SILU, DOWN, DH_SWIGLU, DH_SILU, DX, DW12, DW1, DW3 };
+// DOWN_H / DW3_H read the H / Hg the up-projection / dH epilogue stored;
+// DOWN_SWIGLU, DOWN_SILU, DW3_SWIGLU, DW3_SILU recompute them from the saved
+// A (and B) tiles (MOEBLAZE_RECOMPUTE_H).
+enum Mode : int {
+  UP_SWIGLU = 0, UP_SILU, DOWN_H, DOWN_SWIGLU, DOWN_SILU, DH_SWIGLU, DH_SILU, DX, DW12, DW1, DW3_H, DW3_SWIGLU, DW3_SILU
+};
 
-__host__ __device__ constexpr bool is_wgrad(int m) { return m == DW12 || m == DW1 || m == DW3; }
+__host__ __device__ constexpr bool is_down(int m) { return m == DOWN_H || m == DOWN_SWIGLU || m == DOWN_SILU; }
+__host__ __device__ constexpr bool is_dw3(int m) { return m == DW3_H || m == DW3_SWIGLU || m == DW3_SILU; }
+// stages whose A operand is recomputed from the saved A (and B) tiles
+__host__ __device__ constexpr bool is_fused(int m) {
+  return m == DOWN_SWIGLU || m == DOWN_SILU || m == DW3_SWIGLU || m == DW3_SILU;
+}
+__host__ __device__ constexpr bool fused_sw(int m) { return m == DOWN_SWIGLU || m == DW3_SWIGLU; }
+__host__ __device__ constexpr bool is_wgrad(int m) { return m == DW12 || m == DW1 || is_dw3(m); }
+// Warp roles: producers 0-3, in the fused stages eight transform warps
+// 4-11, then the MMA warp and four epilogue warps.
+__host__ __device__ constexpr int helper_warps(int m) { return is_fused(m) ? 8 : 0; }
+__host__ __device__ constexpr int mma_warp(int m) { return PRODUCER_WARPS + helper_warps(m); }
+__host__ __device__ constexpr int num_threads(int m) { return (mma_warp(m) + 1 + 4) * 32; }
+// threads that recompute the A operand of a fused stage
+__host__ __device__ constexpr int transform_threads(int m) { return helper_warps(m) * 32; }
+// The ring: 4 stages of A (16 KB) + B operand (32 KB); the fused SwiGLU
+// stages add the saved-B tile (16 KB) to every stage and keep 3 of them.
+// The fused stages need no epilogue staging area.
+__host__ __device__ constexpr int stages_of(int m) { return fused_sw(m) ? 3 : STAGES; }
+__host__ __device__ constexpr int stage_bytes_of(int m) { return STAGE_BYTES + (fused_sw(m) ? A_BYTES : 0); }
+__host__ __device__ constexpr int smem_bytes_of(int m) {
+  return stages_of(m) * stage_bytes_of(m) + (is_fused(m) ? 0 : EPI_STAGE_BYTES) + 1024 + BAR_BYTES;
+}
 __host__ __device__ constexpr bool is_dual(int m) { return m == UP_SWIGLU || m == DW12; }
 __host__ __device__ constexpr bool a_mn_major(int m) { return is_wgrad(m); }
 __host__ __device__ constexpr bool b_k_major(int m) { return m == DH_SWIGLU || m == DH_SILU || m == DX; }
@@ -84,6 +121,7 @@ struct Params {
   CUtensorMap tmO0;  // bf16 outputs written by TMA stores (up: A, B, H; dH: dA|dB, Hg)
   CUtensorMap tmO1;
   CUtensorMap tmO2;
+  CUtensorMap tmX;   // fused SwiGLU stages: the saved B, same boxes as tmA
   const int32_t* D1;
   const int32_t* D2;
   const int32_t* D3;
@@ -107,6 +145,7 @@ struct Params {
   const __nv_bfloat16* gsrc;  // gathered tensor (x or dY), rows of gld elements
   int gld;
   float* dg;                   // dH stage: gate gradients (L,K) fp32, or null
+  float* rowg;                 // gate of every padded row (0 for padding rows): written by dH, read by DW3
   unsigned long long* sched;  // tile counter of this launch (zero at launch)
 };
 
@@ -277,6 +316,54 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 
 __device__ __forceinline__ float fast_sigmoid(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+// g * SiLU(a) * b on two bf16 pairs (a, b packed bf16x2), fp32 arithmetic,
+// SiLU(a) = h (1 + tanh h) with h = a/2; the result rounded to bf16x2.
+template <bool GATED_B, bool GATED_ROW>
+__device__ __forceinline__ uint32_t silu_mul2(uint32_t a, uint32_t b, float2 g) {
+  const float2 av = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+  const float2 h = __fmul2_rn(av, make_float2(0.5f, 0.5f));
+  const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
+  float2 r = __ffma2_rn(h, t, h);  // SiLU(a)
+  if constexpr (GATED_B) r = __fmul2_rn(r, make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u)));
+  if constexpr (GATED_ROW) r = __fmul2_rn(r, g);
+  return pack_bf16x2(r.x, r.y);
+}
+// One transform thread's share (tt = 0..255: the producer warps, then the
+// helper warps) of a fused stage's A-operand tile, in place: chunks
+// tt + 256 i (i = 0..3) of the tile's 1024 16-byte chunks.  sA holds the
+// saved A tile, sX the saved B tile at the same positions (SwiGLU).  For DW3
+// the tile is MN-major (two boxes of 64 k-block rows x 128 bytes), so chunk
+// tt + 256 i lies in row tt/8 + 32 (i % 2) of the k-block, whose gate is
+// g2[i % 2]; the down projection applies its gate in the epilogue.
+template <int MODE>
+__device__ __forceinline__ void transform_tile(uint32_t sA, uint32_t sX, int tt, const float* g2) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t off = (uint32_t)(tt + 256 * i) * 16u;
+    const uint4 a = ld_shared_v4(sA + off);
+    uint4 b = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (fused_sw(MODE)) b = ld_shared_v4(sX + off);
+    const float gs = is_dw3(MODE) ? g2[i & 1] : 1.f;
+    const float2 g = make_float2(gs, gs);
+    uint4 o;
+    o.x = silu_mul2<fused_sw(MODE), is_dw3(MODE)>(a.x, b.x, g);
+    o.y = silu_mul2<fused_sw(MODE), is_dw3(MODE)>(a.y, b.y, g);
+    o.z = silu_mul2<fused_sw(MODE), is_dw3(MODE)>(a.z, b.z, g);
+    o.w = silu_mul2<fused_sw(MODE), is_dw3(MODE)>(a.w, b.w, g);
+    st_shared_v4(sA + off, o);
+  }
+}
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
@@ -393,11 +480,16 @@ __device__ __forceinline__ float gate_of(const Params& p, int tok, int e, int* s
 __host__ __device__ constexpr bool cp_a(int m) {
   return m == UP_SWIGLU || m == UP_SILU || m == DH_SWIGLU || m == DH_SILU || m == DW12 || m == DW1;
 }
-__host__ __device__ constexpr bool cp_b(int m) { return m == DW3; }
+__host__ __device__ constexpr bool cp_b(int m) { return is_dw3(m); }
 
 template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
+  // FUSED: transform warps recompute the A operand from the saved tiles
+  constexpr bool FUSED = is_fused(MODE);
+  constexpr int MMA_WARP = mma_warp(MODE);
+  constexpr int NST = stages_of(MODE), SB = stage_bytes_of(MODE);
+  constexpr int LAG = NST - 2;  // cp.async groups a producer thread keeps in flight
   // A dispatch built for another (L, E, K) lays out its tables differently:
   // record the mismatch and read none of them (every thread reads the same
   // three header words, so the whole CTA leaves here together, before any
@@ -408,8 +500,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
-  // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * SB + (FUSED ? 0 : EPI_STAGE_BYTES));
+  // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12],
+  // loaded[48..51] (fused stages: the TMA part of a stage has landed)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_s = reinterpret_cast<volatile int*>(bars + 17);
   // tile-id queue: ids at bars[24 + i], full barriers bars[32 + i], empty barriers bars[40 + i]
@@ -420,9 +513,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(s), CP ? PRODUCER_THREADS : 1);
+    for (int s = 0; s < NST; ++s) {
+      // full: the gathering producer threads (cp.async stages), the transform
+      // warps (fused stages), else thread 0's arrive.expect_tx
+      mbar_init(bar(s), FUSED || CP ? (CP ? PRODUCER_THREADS : 0) + transform_threads(MODE) : 1);
       mbar_init(bar(4 + s), 1);
+      mbar_init(bar(48 + s), 1);
     }
     mbar_init(bar(8), 1);
     mbar_init(bar(9), 1);
@@ -432,8 +528,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     for (int i = 0; i < TQ; ++i) {
       mbar_init(bar(32 + i), 1);
       // readers of a queue slot: the producer warps (thread 0 alone in the
-      // TMA-only stages), the MMA thread and the four epilogue warps
-      mbar_init(bar(40 + i), (CP ? PRODUCER_WARPS : 1) + 1 + 4);
+      // TMA-only stages), the transform warps (fused stages), the MMA thread
+      // and the four epilogue warps
+      mbar_init(bar(40 + i), (CP ? PRODUCER_WARPS : 1) + helper_warps(MODE) + 1 + 4);
     }
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -478,7 +575,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     // straight into the 128B-swizzled layout (8 consecutive threads cover one
     // 128-byte row segment), keep LAG groups in flight, and arrive on the
     // stage's full barrier once their copies of it have landed and been
-    // fenced for the tensor cores (async proxy).
+    // fenced for the tensor cores (async proxy).  In the fused stages the
+    // saved A (and B) tiles go to the stage's `loaded` barrier instead, for
+    // the transform warps, which then complete the full barrier.
     const int pt = threadIdx.x;
     if (CP || pt == 0) {
       int s = 0;
@@ -542,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           if (t.kblocks == 0 && inflight > 0) {
             cp_async_wait<0>();
             fence_proxy_async();
-            for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + STAGES - i) % STAGES));
+            for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + NST - i) % NST));
             inflight = 0;
           }
         }
@@ -557,8 +656,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           if (!ok) break;
           const uint32_t full = bar(s);
-          const uint32_t sA = smem_base + s * STAGE_BYTES;
+          const uint32_t loaded = bar(48 + s);
+          const uint32_t sA = smem_base + s * SB;
           const uint32_t sB = sA + A_BYTES;
+          const uint32_t sX = sB + B_MAX_BYTES;  // fused SwiGLU: the saved-B tile
           const int k0 = kb * BK;
           int wnext[4];
           if constexpr (CP && is_wgrad(MODE)) {
@@ -569,16 +670,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           }
           if (pt == 0) {
             // ---------------- tiled TMA part of the stage
-            const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
-            if (CP) mbar_expect_tx_only(full, tma_bytes);
-            else mbar_expect_tx(full, tma_bytes);
+            if constexpr (FUSED) {
+              const uint32_t tma_bytes = (uint32_t)A_BYTES + (fused_sw(MODE) ? (uint32_t)A_BYTES : 0u) +
+                                         (is_down(MODE) ? (uint32_t)(nmma * BK * 2) : 0u);
+              mbar_expect_tx(loaded, tma_bytes);
+            } else {
+              const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
+              if (CP) mbar_expect_tx_only(full, tma_bytes);
+              else mbar_expect_tx(full, tma_bytes);
+            }
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
-            if constexpr (MODE == DOWN || MODE == DX) {
+            if constexpr (MODE == DX || MODE == DOWN_H) {
               tma_load_2d(sA, &p.tmA, k0, t.row0, full);
-            } else if constexpr (MODE == DW3) {
+            } else if constexpr (MODE == DW3_H) {
               tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
               tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
+            } else if constexpr (is_down(MODE)) {
+              tma_load_2d(sA, &p.tmA, k0, t.row0, loaded);
+              if constexpr (fused_sw(MODE)) tma_load_2d(sX, &p.tmX, k0, t.row0, loaded);
+            } else if constexpr (is_dw3(MODE)) {
+              tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, loaded);
+              tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, loaded);
+              if constexpr (fused_sw(MODE)) {
+                tma_load_2d(sX, &p.tmX, t.row0, t.pad0 + k0, loaded);
+                tma_load_2d(sX + 8192, &p.tmX, t.row0 + 64, t.pad0 + k0, loaded);
+              }
             }
             if constexpr (MODE == UP_SWIGLU) {
               tma_load_2d(sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
@@ -587,8 +704,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
               tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
             } else if constexpr (MODE == UP_SILU) {
               for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
-            } else if constexpr (MODE == DOWN) {
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, full);
+            } else if constexpr (is_down(MODE)) {
+              const uint32_t wb = FUSED ? loaded : full;
+              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, wb);
             } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
               for (int j = 0; j < t.nw / 128; ++j)
                 tma_load_2d(sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
@@ -634,7 +752,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             if (inflight == LAG) {
               cp_async_wait<LAG>();
               fence_proxy_async();
-              mbar_arrive(bar((s + STAGES - LAG) % STAGES));
+              mbar_arrive(bar((s + NST - LAG) % NST));
             } else {
               ++inflight;
             }
@@ -645,7 +763,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
               for (int i = 0; i < 4; ++i) wtok[i] = wnext[i];
             }
           }
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (++s == NST) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         if (pt == 0) ok = q_post(j + 2, pending);
@@ -666,12 +784,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
         // the last `inflight` stages: wait for their copies and arrive
         cp_async_wait<0>();
         fence_proxy_async();
-        for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + STAGES - i) % STAGES));
+        for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + NST - i) % NST));
       }
       if (!ok && pt == 0) {
         // give the TMA copies already issued a bounded chance to land
-        for (int i = 0; i < STAGES; ++i)
-          if (armed & (1u << i)) wait_bounded(bar(i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
+        for (int i = 0; i < NST; ++i)
+          if (armed & (1u << i))
+            wait_bounded(bar(FUSED ? 48 + i : i), (armed_par >> i) & 1u, nullptr, nullptr, kDrainNs);
+      }
+    }
+  } else if (warp < MMA_WARP) {
+    // ================================================================ transform warps
+    // Fused stages only: every stage's A operand is recomputed here, in
+    // place, from the saved tiles its TMA part brought in.  The warps follow
+    // the tile queue and the k-blocks in the producer's order, wait for each
+    // stage's `loaded` barrier, recompute their chunks, fence them for the
+    // tensor cores and arrive on the full barrier.
+    if constexpr (FUSED) {
+      const int tt = threadIdx.x - PRODUCER_THREADS;  // 0..255
+      int hs = 0;
+      uint32_t hph = 0;
+      bool ok = true;
+      for (int j = 0; ok; ++j) {
+        long long tile = 0;
+        if (lane == 0) tile = q_take(j);
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (tile < 0 || tile >= total) break;
+        const Tile t = decode<MODE>(p, tile, num_mt);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          float g2[2] = {1.f, 1.f};
+          if constexpr (is_dw3(MODE)) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) g2[i] = p.rowg[t.pad0 + kb * BK + (tt >> 3) + 32 * i];
+          }
+          bool got = true;
+          if (lane == 0) got = wait_bounded(bar(48 + hs), hph, abort_s, err);
+          ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          // every lane observes the completed phase itself (acquire) before it
+          // reads what the TMA wrote; the phase cannot move on before this
+          // stage's full barrier, which needs every transform thread
+          (void)mbar_try(bar(48 + hs), hph);
+          const uint32_t sA = smem_base + hs * SB;
+          transform_tile<MODE>(sA, sA + A_BYTES + B_MAX_BYTES, tt, g2);
+          fence_proxy_async();
+          mbar_arrive(bar(hs));
+          if (++hs == NST) { hs = 0; hph ^= 1u; }
+        }
       }
     }
   } else if (warp == MMA_WARP) {
@@ -712,7 +871,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
           ok = wait_bounded(bar(s), ph, abort_s, err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sA = smem_base + s * STAGE_BYTES;
+          const uint32_t sA = smem_base + s * SB;
           const uint32_t sB = sA + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
@@ -721,7 +880,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
           mma_commit(bar(4 + s));
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (++s == NST) { s = 0; ph ^= 1u; }
           if (kb == 0) fetch_next();
         }
         if (!ok) break;
@@ -740,7 +899,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
     // ================================================================ epilogue
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter ...
     const int r = quarter * 32 + lane;            // accumulator row of this thread
-    StoreRing ring{smem_base + STAGES * STAGE_BYTES + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
+    StoreRing ring{smem_base + NST * SB + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
     for (int j = 0;; ++j) {
@@ -759,7 +918,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
       if constexpr (!is_wgrad(MODE)) {
         q = t.row0 + r;
         valid = (q - t.pad0) < t.n_e;
-        if constexpr (MODE == DOWN || MODE == DX || DH) {
+        if constexpr (is_down(MODE) || MODE == DX || DH) {
           if (valid) {
             tok = p.D1[t.off + (q - t.pad0)];
             if constexpr (MODE != DX) g = gate_of(p, tok, t.e, &kslot);
@@ -802,30 +961,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             MB_TMEM_LD32(tbase + 32 * c, ra);
             MB_TMEM_LD32(tbase + 128 + 32 * c, rb);
             tmem_wait_ld();
-            float vh[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               va[i] = __uint_as_float(ra[i]);
               vb[i] = __uint_as_float(rb[i]);
-              vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
             }
             staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
             staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, vb, valid, lane);
-            staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vh, valid, lane);
+            if (p.o2) {  // H for the down projection (not with MOEBLAZE_RECOMPUTE_H)
+              float vh[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
+              staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vh, valid, lane);
+            }
           }
         } else if constexpr (MODE == UP_SILU) {
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              va[i] = __uint_as_float(ra[i]);
-              vb[i] = va[i] * fast_sigmoid(va[i]);
-            }
+            for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
             staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
-            staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vb, valid, lane);
+            if (p.o2) {  // H = SiLU(a) for the down projection (not with MOEBLAZE_RECOMPUTE_H)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) vb[i] = va[i] * fast_sigmoid(va[i]);
+              staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vb, valid, lane);
+            }
           }
-        } else if constexpr (MODE == DOWN || MODE == DX) {
+        } else if constexpr (is_down(MODE) || MODE == DX) {
           float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
@@ -885,9 +1048,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_gemm_kernel(const __grid_c
             }
             staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
             if constexpr (SW) staged_store(ring, &p.tmO0, p.h + t.n0 + 32 * c, wrow0, dB, valid, lane);
-            staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
+            // Hg for the dW3 GEMM (not with MOEBLAZE_RECOMPUTE_H)
+            if (p.o1) staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
           }
           if (valid && p.dg) atomicAdd(p.dg + (int64_t)tok * p.K + kslot, dgp);
+          // with MOEBLAZE_RECOMPUTE_H: the row's gate for the dW3 stage, which
+          // recomputes Hg = g SiLU(A) B from the saved A and B (0 on padding
+          // rows); once per row
+          if (p.rowg && t.n0 == 0) p.rowg[q] = valid ? g : 0.f;
         }
       } else {
         // weight gradients: rows of dW_e, plain bf16 stores
@@ -976,9 +1144,9 @@ template <int MODE>
 moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
   if (tiles_bound <= 0) return MOEBLAZE_OK;
   auto kern = moe_gemm_kernel<MODE>;
-  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of(MODE)));
   const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
-  kern<<<(unsigned)g, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  kern<<<(unsigned)g, num_threads(MODE), smem_bytes_of(MODE), st>>>(p);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
@@ -1023,6 +1191,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
                            const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved, __nv_bfloat16* wsH,
                            float* wsY32, cudaStream_t st) {
   const bool sw = s.act == MOEBLAZE_SWIGLU;
+  const bool rec = wsH == nullptr;  // MOEBLAZE_RECOMPUTE_H: no H temporary
   const int64_t LK = s.L * s.K;
   const int64_t rows = max_padded_rows(LK, s.E);
   const int64_t mt_bound = rows / BM;
@@ -1049,14 +1218,15 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
       if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      if (!make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+      if (!rec && !make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
-    {  // down projection + gate-weighted combine into y32
+    {  // down projection of H (stored, or recomputed from the saved tiles) + gate-weighted combine into y32
       Params p = base_params(s, disp, gates);
-      if (!make_map(&p.tmA, wsH, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      if (!make_map(&p.tmA, rec ? A : wsH, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+      if (rec && sw && !make_map(&p.tmX, B, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
       if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 64)) return MOEBLAZE_ERR_CUDA;
       p.N = s.d;
       p.kblocks = s.h / BK;
@@ -1064,7 +1234,9 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsY32;
       p.sched = sched + 1;
-      moeblaze_status r = launch<DOWN>(p, mt_bound * p.n_tiles, st);
+      const int64_t nt = mt_bound * p.n_tiles;
+      moeblaze_status r = !rec ? launch<DOWN_H>(p, nt, st)
+                               : (sw ? launch<DOWN_SWIGLU>(p, nt, st) : launch<DOWN_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
   }
@@ -1078,7 +1250,9 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
                             const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st) {
+                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsRowg, float* wsdX32,
+                            cudaStream_t st) {
+  const bool rec = wsHg == nullptr;  // MOEBLAZE_RECOMPUTE_H: row gates instead of an Hg temporary
   const bool sw = s.act == MOEBLAZE_SWIGLU;
   const int nb = sw ? 2 : 1;
   const int64_t LK = s.L * s.K;
@@ -1102,11 +1276,12 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.ksplit = p.kblocks;
       p.n_tiles = (s.h + 255) / 256;
       p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
+      p.rowg = rec ? wsRowg : nullptr;
       p.dg = dgates;
       p.sched = sched + 0;
       const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      if (!make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+      if (!rec && !make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       p.ld0 = nb * s.h;
       moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
       if (r != MOEBLAZE_OK) return r;
@@ -1143,9 +1318,11 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(3, st);
-  {  // dW3 = Hg^T dY
+  {  // dW3 = Hg^T dY, Hg stored by dH or recomputed from the saved tiles (Hg = g SiLU(A) B)
     Params p = base_params(s, disp, gates);
-    if (!make_map(&p.tmA, wsHg, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    if (!make_map(&p.tmA, rec ? A : wsHg, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    if (rec && sw && !make_map(&p.tmX, B, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    p.rowg = rec ? wsRowg : nullptr;
     p.gsrc = dY;
     p.gld = s.d;
     p.N = s.d;
@@ -1154,7 +1331,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW3;
     p.sched = sched + 3;
-    moeblaze_status r = launch<DW3>(p, p.total_w, st);
+    moeblaze_status r = !rec ? launch<DW3_H>(p, p.total_w, st)
+                             : (sw ? launch<DW3_SWIGLU>(p, p.total_w, st) : launch<DW3_SILU>(p, p.total_w, st));
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(4, st);

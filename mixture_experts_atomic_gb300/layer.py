@@ -13,8 +13,10 @@ from . import binding as B
 
 class MoELayer:
     def __init__(self, L: int, d: int, h: int, E: int, K: int, dtype: torch.dtype, act: str, device="cuda",
-                 with_dgates: bool = True):
-        self.shape = B.make_shape(L, d, h, E, K, dtype, act)
+                 with_dgates: bool = True, recompute_h: bool = False):
+        """recompute_h: keep no H / Hg temporaries (MOEBLAZE_RECOMPUTE_H):
+        smaller scratch, the down projection and dW3 recompute them."""
+        self.shape = B.make_shape(L, d, h, E, K, dtype, act, B.RECOMPUTE_H if recompute_h else 0)
         self.L, self.d, self.h, self.E, self.K = L, d, h, E, K
         self.dtype, self.act, self.device = dtype, act, device
         self.disp = B.alloc_dispatch(self.shape, device)
@@ -31,8 +33,8 @@ class MoELayer:
             self.dW3 = torch.empty((E, h, d), dtype=dtype, device=device)
 
     @classmethod
-    def for_config(cls, cfg, device="cuda", with_dgates: bool = True):
-        return cls(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act, device, with_dgates)
+    def for_config(cls, cfg, device="cuda", with_dgates: bool = True, recompute_h: bool = False):
+        return cls(cfg.L, cfg.d, cfg.h, cfg.E, cfg.K, cfg.torch_dtype, cfg.act, device, with_dgates, recompute_h)
 
     def dispatch(self, ids: torch.Tensor, validate: bool = False):
         B.dispatch_build(self.shape, ids, self.disp, validate=validate)

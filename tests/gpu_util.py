@@ -47,19 +47,19 @@ def check_dispatch(layer: MoELayer, ids_cpu: torch.Tensor, E: int):
     return D1, D2, D3, D4
 
 
-def run_layer(cfg, inp_dev) -> MoELayer:
-    layer = MoELayer.for_config(cfg, "cuda")
+def run_layer(cfg, inp_dev, recompute_h=False) -> MoELayer:
+    layer = MoELayer.for_config(cfg, "cuda", recompute_h=recompute_h)
     layer.step(inp_dev)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     return layer
 
 
-def full_compare(cfg, inp_cpu, tol=None, check_saved=True):
+def full_compare(cfg, inp_cpu, tol=None, check_saved=True, recompute_h=False):
     """Whole-tensor comparison of every output with the oracle."""
     tol = TOL[cfg.dtype] if tol is None else tol
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
-    layer = run_layer(cfg, dev)
+    layer = run_layer(cfg, dev, recompute_h)
     D1, D2, D3, D4 = check_dispatch(layer, inp_cpu["ids"], cfg.E)
     a = inp_cpu
     y, keep = O.forward(a["ids"], a["gates"], a["x"], a["W1"], a["W2"], a["W3"], cfg.act, E=cfg.E, keep=True)
@@ -106,7 +106,7 @@ def spread_indices(n, tile, per_tile, rng, extra=0):
     return sorted(int(i) for i in picks)
 
 
-def sampled_compare(cfg, n_tok=62, per_tile=10, seed=0, tol=None):
+def sampled_compare(cfg, n_tok=62, per_tile=10, seed=0, tol=None, recompute_h=False):
     """Full-size run on the device; the oracle computes sampled outputs one
     by one:
       - y, dX and dgates on n_tok random token rows plus the first and last;
@@ -118,7 +118,7 @@ def sampled_compare(cfg, n_tok=62, per_tile=10, seed=0, tol=None):
     Returns the errors and the sampled fractions."""
     tol = TOL[cfg.dtype] if tol is None else tol
     inp = I.make_inputs(cfg, "cuda")
-    layer = run_layer(cfg, inp)
+    layer = run_layer(cfg, inp, recompute_h)
     ids = inp["ids"].cpu()
     gates = inp["gates"].cpu()
     D1, D2, D3, D4 = check_dispatch(layer, ids, cfg.E)

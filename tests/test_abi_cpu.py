@@ -169,3 +169,28 @@ def test_dispatch_meta_check_compares_the_recorded_shape():
     assert B.moeblaze_dispatch_meta_check(s0, hdr(0, 0, 0)) == B.OK
     assert B.moeblaze_dispatch_meta_check(s0, hdr(1, 64, 6)) == B.ERR_INVALID_ARG
     assert B.moeblaze_dispatch_meta_check(s, None) == B.ERR_INVALID_ARG
+
+
+def test_recompute_flag_sizes_and_validation():
+    """MOEBLAZE_RECOMPUTE_H drops H (padded_rows x h) from the forward
+    scratch and swaps Hg for one fp32 gate per padded row in the backward
+    scratch of the bf16 expert layers; fp32 and identity layers ignore it;
+    unknown flag bits are refused."""
+    _lib()
+    for act in ("swiglu", "silu"):
+        a = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act)
+        r = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act, B.RECOMPUTE_H)
+        rows = -(-(70000 * 2 + 127 * 16) // 128) * 128
+        h_bytes = -(-(rows * 384 * 2) // 256) * 256
+        g_bytes = -(-(rows * 4) // 256) * 256
+        assert B.moeblaze_forward_workspace_bytes(a) - B.moeblaze_forward_workspace_bytes(r) == h_bytes
+        assert B.moeblaze_backward_workspace_bytes(a) - B.moeblaze_backward_workspace_bytes(r) == h_bytes - g_bytes
+        assert B.moeblaze_saved_bytes(a) == B.moeblaze_saved_bytes(r)
+    for dt, act in ((B.F32, "swiglu"), (B.BF16, "identity")):
+        a = B.make_shape(700, 64, 128, 8, 2, dt, act)
+        r = B.make_shape(700, 64, 128, 8, 2, dt, act, B.RECOMPUTE_H)
+        assert B.moeblaze_forward_workspace_bytes(a) == B.moeblaze_forward_workspace_bytes(r)
+        assert B.moeblaze_backward_workspace_bytes(a) == B.moeblaze_backward_workspace_bytes(r)
+    bad = B.make_shape(700, 128, 128, 8, 2, B.BF16, "swiglu", 2)
+    assert B.moeblaze_saved_bytes(bad) == 0
+    assert B.moeblaze_dispatch_build(bad, FAKE, _disp(), FAKE, 1 << 30, 0, None) == B.ERR_INVALID_ARG

@@ -41,12 +41,16 @@ def test_fp32_layer_full_size():
     (4096, 512, 512, 4, 1, "swiglu", None),   # K = 1
     (3000, 256, 640, 12, 2, "silu", 0),
 ])
-def test_bf16_layer_small(L, d, h, E, K, act, one):
+@pytest.mark.parametrize("recompute_h", [False, True])
+def test_bf16_layer_small(L, d, h, E, K, act, one, recompute_h):
+    """recompute_h: the layer keeps no H / Hg; the down projection and dW3
+    recompute them from the saved A, B (its own GEMM variants)."""
     cfg = I.MoEConfig(f"t_{act}_{L}_{d}_{h}_{E}_{K}", L, d, h, E, K, act, "bf16", 11, "softmax")
-    full_compare(cfg, _routed_inputs(cfg, 5, one))
+    full_compare(cfg, _routed_inputs(cfg, 5, one), recompute_h=recompute_h)
 
 
-def test_bf16_layer_most_experts_empty():
+@pytest.mark.parametrize("recompute_h", [False, True])
+def test_bf16_layer_most_experts_empty(recompute_h):
     """60 of 64 experts (the last one among them) get no token: the weight
     gradient stages then run long stretches of tiles with no k-blocks on
     every CTA, which must still come out as zero gradients."""
@@ -55,7 +59,7 @@ def test_bf16_layer_most_experts_empty():
     ids4, gates = I.random_routing(cfg.L, 4, cfg.K, 7)
     used = torch.tensor([0, 9, 30, 41], dtype=torch.int32)
     inp["ids"], inp["gates"] = used[ids4.long()].contiguous(), gates
-    errs, layer = full_compare(cfg, inp)
+    errs, layer = full_compare(cfg, inp, recompute_h=recompute_h)
     empty = [e for e in range(cfg.E) if e not in used.tolist()]
     assert float(layer.dW1[empty].float().abs().max()) == 0.0
     assert float(layer.dW3[empty].float().abs().max()) == 0.0
@@ -101,9 +105,10 @@ def test_empty_layer_zero_grads():
     assert float(layer.dW1.float().abs().sum()) == 0 and float(layer.dW3.float().abs().sum()) == 0
 
 
-@pytest.mark.parametrize("ci", [1, 2, 3])
-def test_workload_sampled(ci):
-    sampled_compare(I.CONFIGS[ci])
+@pytest.mark.parametrize("ci,recompute_h", [(1, False), (2, False), (3, False), (1, True), (2, True), (3, True)])
+def test_workload_sampled(ci, recompute_h):
+    errs, frac = sampled_compare(I.CONFIGS[ci], recompute_h=recompute_h)
+    print(I.CONFIGS[ci].name, "recompute_h" if recompute_h else "", errs, frac)
 
 
 def test_identity_workload_sampled():
