@@ -307,6 +307,21 @@ MOEBLAZE_API moeblaze_status moeblaze_dispatch_meta_check(const moeblaze_shape* 
 MOEBLAZE_API void moeblaze_set_stage_events(void** events, int32_t n);
 MOEBLAZE_API int64_t moeblaze_kernel_launches(void);
 
+/* Failure-path test hook (for tests; not for production runs).
+ *
+ * moeblaze_set_fault_injection: later calls made from the calling thread run
+ * their bf16 expert GEMMs with `wait_limit_ns` as the limit of every bounded
+ * device-side wait (> 0; 0 restores the default of 4 s).  With withhold != 0
+ * the down projection of a later moeblaze_forward (default mode, not
+ * MOEBLAZE_RECOMPUTE_H) issues nothing for the first stage of each CTA's
+ * first tile, so that stage's barrier is never completed: the CTA's MMA wait
+ * runs out after the limit, the CTA records bit 2 (timeout) in the device
+ * error word, lets the copies it has in flight land, frees its tensor memory
+ * and returns; moeblaze_device_error then returns MOEBLAZE_ERR_TIMEOUT.  The
+ * GPU context stays usable and the next dispatch build clears the word.
+ * (0, 0) switches the hook off. */
+MOEBLAZE_API void moeblaze_set_fault_injection(int64_t wait_limit_ns, int32_t withhold);
+
 /* Static description of a status code. */
 MOEBLAZE_API const char* moeblaze_status_string(moeblaze_status st);
 

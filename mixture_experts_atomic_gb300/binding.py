@@ -29,7 +29,7 @@ EXPORTS = [
     "moeblaze_forward_workspace_bytes", "moeblaze_backward_workspace_bytes", "moeblaze_dispatch_build",
     "moeblaze_forward", "moeblaze_backward", "moeblaze_device_error", "moeblaze_status_string",
     "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
-    "moeblaze_dispatch_build_static", "moeblaze_dispatch_meta_check",
+    "moeblaze_dispatch_build_static", "moeblaze_dispatch_meta_check", "moeblaze_set_fault_injection",
     "moeblaze_router_forward", "moeblaze_router_backward", "moeblaze_router_backward_workspace_bytes",
 ]
 
@@ -98,6 +98,8 @@ def lib():
         L.moeblaze_version.restype = ctypes.c_int32
         L.moeblaze_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
         L.moeblaze_set_stage_events.restype = None
+        L.moeblaze_set_fault_injection.argtypes = [ctypes.c_int64, ctypes.c_int32]
+        L.moeblaze_set_fault_injection.restype = None
         L.moeblaze_kernel_launches.argtypes = []
         L.moeblaze_kernel_launches.restype = ctypes.c_int64
         _lib = L
@@ -178,6 +180,10 @@ def moeblaze_dispatch_meta_check(shape, meta_header) -> int:
 
 def moeblaze_set_stage_events(events, n: int) -> None:
     lib().moeblaze_set_stage_events(events, int(n))
+
+
+def moeblaze_set_fault_injection(wait_limit_ns: int, withhold: int) -> None:
+    lib().moeblaze_set_fault_injection(int(wait_limit_ns), int(withhold))
 
 
 def moeblaze_kernel_launches() -> int:

@@ -25,7 +25,14 @@ namespace {
 std::atomic<int64_t> g_launches{0};
 thread_local void** g_events = nullptr;
 thread_local int32_t g_nevents = 0;
+thread_local uint64_t g_wait_ns = 0;
+thread_local int g_withhold = 0;
 }  // namespace
+
+void fault_injection(uint64_t* wait_ns, int* withhold) {
+  *wait_ns = g_wait_ns;
+  *withhold = g_withhold;
+}
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -136,6 +143,11 @@ void moeblaze_set_stage_events(void** events, int32_t n) {
 }
 
 int64_t moeblaze_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void moeblaze_set_fault_injection(int64_t wait_limit_ns, int32_t withhold) {
+  g_wait_ns = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 0;
+  g_withhold = withhold ? 1 : 0;
+}
 
 const char* moeblaze_status_string(moeblaze_status st) {
   switch (st) {

@@ -140,6 +140,9 @@ int sm_count();
 void count_launch(int n = 1);
 // record stage-boundary event i on st if the caller asked for it
 void stage_event(int i, cudaStream_t st);
+// the calling thread's failure-path test settings (moeblaze_set_fault_injection):
+// wait limit in ns (0: the default) and whether the down projection withholds a stage
+void fault_injection(uint64_t* wait_ns, int* withhold);
 
 // ---------------------------------------------------------------- device helpers
 

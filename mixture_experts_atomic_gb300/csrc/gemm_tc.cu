@@ -146,6 +146,9 @@ struct Params {
   int gld;
   float* dg;                   // dH stage: gate gradients (L,K) fp32, or null
   float* rowg;                 // gate of every padded row (0 for padding rows): written by dH, read by DW3
+  uint64_t wait_ns;            // limit of every bounded wait (kTimeoutNs unless a test sets a shorter one)
+  int withhold;                // test of the failure path (DOWN_H): the first stage of each CTA's first
+                               // tile is never issued, so the MMA's wait for it runs out
   unsigned long long* sched;  // tile counter of this launch (zero at launch)
 };
 
@@ -549,18 +552,19 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
   const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
   int32_t* err = p.meta.err;
+  const uint64_t lim = p.wait_ns;
 
   // queue position j lives in slot j % TQ, phase (j / TQ) & 1
   auto q_post = [&](int j, long long id) -> bool {  // thread 0
     const int sl = j % TQ;
-    if (!wait_bounded(bar(40 + sl), (uint32_t)((j / TQ) & 1) ^ 1u, abort_s, err)) return false;
+    if (!wait_bounded(bar(40 + sl), (uint32_t)((j / TQ) & 1) ^ 1u, abort_s, err, lim)) return false;
     tq[sl] = id;
     mbar_arrive(bar(32 + sl));
     return true;
   };
   auto q_take = [&](int j) -> long long {  // one thread per reader; -1 once the CTA gives up
     const int sl = j % TQ;
-    if (!wait_bounded(bar(32 + sl), (uint32_t)(j / TQ) & 1u, abort_s, err)) return -1;
+    if (!wait_bounded(bar(32 + sl), (uint32_t)(j / TQ) & 1u, abort_s, err, lim)) return -1;
     const long long id = tq[sl];
     mbar_arrive(bar(40 + sl));
     return id;
@@ -648,11 +652,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if constexpr (CP) {
             // every lane of the four producer warps is here: lane 0 waits, the warp follows
-            if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+            if (lane == 0) ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err, lim);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           } else {
             // thread 0 runs this loop alone: no warp-collective operations here
-            ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err);
+            ok = wait_bounded(bar(4 + s), ph ^ 1u, abort_s, err, lim);
           }
           if (!ok) break;
           const uint32_t full = bar(s);
@@ -668,7 +672,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               for (int i = 0; i < 4; ++i) wnext[i] = row_token(p, t, t.pad0 + k0 + BK + i * 16 + r16);
             }
           }
-          if (pt == 0) {
+          // test of the failure path: the down projection leaves the first
+          // stage of this CTA's first tile empty; nothing ever completes its
+          // full barrier
+          const bool withheld = MODE == DOWN_H && p.withhold && j == 0 && kb == 0;
+          if (pt == 0 && !withheld) {
             // ---------------- tiled TMA part of the stage
             if constexpr (FUSED) {
               const uint32_t tma_bytes = (uint32_t)A_BYTES + (fused_sw(MODE) ? (uint32_t)A_BYTES : 0u) +
@@ -786,7 +794,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         fence_proxy_async();
         for (int i = inflight; i > 0; --i) mbar_arrive(bar((s + NST - i) % NST));
       }
-      if (!ok && pt == 0) {
+      if ((!ok || p.withhold) && pt == 0) {
         // give the TMA copies already issued a bounded chance to land
         for (int i = 0; i < NST; ++i)
           if (armed & (1u << i))
@@ -818,7 +826,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
             for (int i = 0; i < 2; ++i) g2[i] = p.rowg[t.pad0 + kb * BK + (tt >> 3) + 32 * i];
           }
           bool got = true;
-          if (lane == 0) got = wait_bounded(bar(48 + hs), hph, abort_s, err);
+          if (lane == 0) got = wait_bounded(bar(48 + hs), hph, abort_s, err, lim);
           ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
           if (!ok) break;
           // every lane observes the completed phase itself (acquire) before it
@@ -863,12 +871,12 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         };
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
         const uint32_t idesc = instr_desc(nmma, a_mn_major(MODE), !b_k_major(MODE));
-        ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err);
+        ok = wait_bounded(bar(10 + abuf), aph ^ 1u, abort_s, err, lim);
         if (!ok) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + abuf * 256;
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          ok = wait_bounded(bar(s), ph, abort_s, err);
+          ok = wait_bounded(bar(s), ph, abort_s, err, lim);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sA = smem_base + s * SB;
@@ -892,7 +900,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       }
       // all MMAs issued by this thread retire before TMEM is released
       mma_commit(bar(12));
-      wait_bounded(bar(12), 0, nullptr, nullptr, ok ? kTimeoutNs : kDrainNs);
+      wait_bounded(bar(12), 0, nullptr, nullptr, ok ? lim : kDrainNs);
     }
     __syncwarp();
   } else {
@@ -946,7 +954,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         }
       }
       bool ok = true;
-      if (lane == 0) ok = wait_bounded(bar(8 + abuf), aph, abort_s, err);
+      if (lane == 0) ok = wait_bounded(bar(8 + abuf), aph, abort_s, err, lim);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
@@ -1162,6 +1170,8 @@ Params base_params(const moeblaze_shape& s, const moeblaze_dispatch& disp, const
   p.meta = meta_view(disp.meta, s.E);
   p.L = s.L;
   p.d = s.d; p.h = s.h; p.E = s.E; p.K = s.K;
+  fault_injection(&p.wait_ns, &p.withhold);
+  if (p.wait_ns == 0) p.wait_ns = kTimeoutNs;
   return p;
 }
 
