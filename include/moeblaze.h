@@ -216,8 +216,11 @@ MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const voi
  *   dgates  device (L,K) fp32, overwritten, or NULL: the gate gradients
  *           dg[t,k] = <dY[t], expert_{ids[t,k]}(x[t])> (y is linear in the
  *           gates), for a router's backward; not on the pages, whose backward
- *           holds the router fixed.  Summed in fp32 over h in an unspecified
- *           order.
+ *           holds the router fixed.  Summed in fp32 over h by float atomic
+ *           adds, one per (token, slot) and 256-column tile of h, in the
+ *           order the CTAs finish their tiles, so repeated calls can differ
+ *           in the last bits (the other bf16 outputs are bitwise repeatable
+ *           for K <= 2).
  *   ws      device moeblaze_backward_workspace_bytes(s) bytes of scratch
  */
 MOEBLAZE_API moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x,
