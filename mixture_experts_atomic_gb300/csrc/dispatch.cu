@@ -1,7 +1,8 @@
 // Atomic-free three-step dispatch build (MoEBlaze, awesome-system-papers
 // page, section "Atomic-free 三步 dispatch 构建").
 //
-//   K1 bitmap_kernel   one CTA per chunk of 1024 tokens.  Builds the chunk's
+//   K1 bitmap_kernel   one CTA per chunk of 1024 tokens (CTA 0 also clears
+//                      the device error word).  Builds the chunk's
 //                      token-expert bitmap in shared memory (bit t%32 of word
 //                      [e][t/32]; every (t,e) bit written once: the lanes of a
 //                      warp with the same expert are found by bit-plane
@@ -10,18 +11,20 @@
 //                      (expert-major, each expert's 32 words = one 128-byte
 //                      line) and the per (expert, chunk) popcount.
 //   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
-//                      counts -> chunk bases and n_e.
-//   K2b offsets_kernel expert_token_offsets (the scan of n_e), the padded
-//                      row offsets, the GEMM tile table (split over a few
-//                      CTAs), the experts' descending-load order and the
-//                      (L, E, K) the build was made for.
-//   K3 scatter_kernel  one CTA per chunk.  A shuffle scan over each expert's
-//                      32 popcounts gives every word its first position;
-//                      each token then places its K slots:
+//                      counts -> chunk bases and n_e.  Large layers only:
+//                      below chunks x experts = 32768 each K3 CTA sums the
+//                      counts it needs itself (one launch fewer).
+//   K3 scatter_kernel  one CTA per chunk.  expert_token_offsets from a block
+//                      scan of n_e; a shuffle scan over each expert's 32
+//                      popcounts gives every word its first position; each
+//                      token then places its K slots:
 //                      pos = off[e] + base[e][c] + wordprefix + popc(bits below).
 //                      Writes token_index_map and token_expert_indices
 //                      token-major (one vector per token) and
-//                      expert_token_indices[pos].
+//                      expert_token_indices[pos].  The CTAs also split the
+//                      GEMM metadata: padded row offsets, the tile -> expert
+//                      table, the experts' descending-load order and the
+//                      (L, E, K) the build was made for.
 //
 // No global atomics on the data path (the device error word is the only
 // atomic, and only for invalid routing).
@@ -78,27 +81,15 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
     for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
   }
   for (int i = tid; i < E * kRow; i += kThreads) words[i] = 0u;
-
-  // routing checks: ids in range, pairwise distinct per token (K*(K-1)/2 compares)
-  bool bad = false;
+  // A new build starts with a clean device error word; K3, which runs after
+  // every K1 CTA has finished, records invalid routing in it.
+  if (chunk == 0 && tid == 0) *err = 0;
+  // ids out of [0, E) are left out of the bitmap (K3 reports them)
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
-    if (t >= L) continue;
+  for (int j = 0; j < kPasses; ++j)
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-      if (k >= K) break;
-      const int e = e_k[j][k];
-      if (e < 0 || e >= E) {
-        bad = true;
-        e_k[j][k] = -1;
-      }
-#pragma unroll
-      for (int i = 0; i < k; ++i)
-        if (e_k[j][k] >= 0 && e_k[j][k] == e_k[j][i]) bad = true;
-    }
-  }
-  if (bad) atomicOr(err, kErrBadRouting);
+    for (int k = 0; k < kMaxK; ++k)
+      if (e_k[j][k] >= E) e_k[j][k] = -1;
   __syncthreads();
 
   // Word [e][w] collects the lanes of this warp routed to e.  Within one
@@ -194,114 +185,51 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
   if (threadIdx.x == 0) n_e[e] = total;
 }
 
-// K2b: expert_token_offsets (exclusive scan of n_e) and the GEMM metadata:
-// padded row offsets, tile count, tile -> expert table and the experts in
-// descending order of load.  Every CTA scans the (at most 512) counts; the
-// tile table (binary search in the padded offsets) and the load ranks are
-// split over the CTAs, and CTA 0 writes the offsets.  Computed once instead
-// of in every chunk's CTA.
-__global__ void __launch_bounds__(kThreads) offsets_kernel(const int32_t* __restrict__ n_e, int E,
-                                                           int32_t* __restrict__ D2, MetaView meta, int64_t max_tiles,
-                                                           int64_t L, int K) {
-  __shared__ int32_t off[kMaxE + 1];
-  __shared__ int32_t poff[kMaxE + 1];
-  __shared__ int32_t cnt[kMaxE];
-  __shared__ int wsum[32];
-  __shared__ int total;
-  const int tid = threadIdx.x;
-  constexpr int kEPT = kMaxE / kThreads;
-  int carry = 0, pcarry = 0;
-#pragma unroll
-  for (int q = 0; q < kEPT; ++q) {
-    const int e = tid + q * kThreads;
-    const int n = e < E ? n_e[e] : 0;
-    const int pn = (n + kRowPad - 1) / kRowPad * kRowPad;
-    const int pre = block_excl_scan(n, wsum, &total);
-    const int tot = total;
-    const int ppre = block_excl_scan(pn, wsum, &total);
-    if (e < E) {
-      off[e] = carry + pre;
-      poff[e] = pcarry + ppre;
-    }
-    carry += tot;
-    pcarry += total;
-  }
-  if (tid == 0) {
-    off[E] = carry;
-    poff[E] = pcarry;
-  }
-  __syncthreads();
-  // tile table: tile m of this CTA's range -> the expert whose padded rows hold it
-  const int64_t ntiles = pcarry / kTileM;
-  const int64_t per = (max_tiles + gridDim.x - 1) / gridDim.x;
-  const int64_t m0 = (int64_t)blockIdx.x * per, m1 = min(max_tiles, m0 + per);
-  for (int64_t m = m0 + tid; m < m1; m += kThreads) {
-    int32_t v = -1;
-    if (m < ntiles) {
-      const int64_t row = m * kTileM;
-      int lo = 0, hi = E - 1;  // last e with poff[e] <= row (non-empty segments only own rows)
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (poff[mid] <= row) lo = mid;
-        else hi = mid - 1;
-      }
-      v = lo;
-    }
-    meta.tile_expert[m] = v;
-  }
-  // descending load, equal loads by index: the rank of expert e is the
-  // number of experts j with n_j > n_e, or n_j == n_e and j < e.  One warp
-  // per expert, the experts spread over all CTAs.
-  for (int e = tid; e < E; e += kThreads) cnt[e] = off[e + 1] - off[e];
-  __syncthreads();
-  const int lane = tid & 31, nwarps = kThreads / 32;
-  for (int e = blockIdx.x * nwarps + (tid >> 5); e < E; e += gridDim.x * nwarps) {
-    const int32_t me = cnt[e];
-    int rank = 0;
-    for (int j = lane; j < E; j += 32) {
-      const int32_t nj = cnt[j];
-      rank += (nj > me) || (nj == me && j < e);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (lane == 0) meta.order[rank] = e;
-  }
-  if (blockIdx.x != 0) return;
-  if (tid == 0) {
-    *meta.num_m_tiles = (int32_t)ntiles;
-    *meta.padded_rows = pcarry;
-    // the shape this build was made for, checked by every forward/backward kernel
-    meta.hdr[kHdrL] = (int32_t)L;
-    meta.hdr[kHdrE] = E;
-    meta.hdr[kHdrK] = K;
-  }
-  for (int e = tid; e <= E; e += kThreads) {
-    D2[e] = off[e];
-    meta.pad_off[e] = poff[e];
-  }
-}
-
-// K3: one CTA per chunk.  Every global read (expert offsets, chunk bases,
-// bitmap words, ids) is issued first; the word prefixes of every expert
-// come from a shuffle scan over its 32 words (4 per thread); each (token,
-// slot) then gets pos = off[e] + base[e][c] + wordprefix + popc(bits below).
+// K3: one CTA per chunk.  Every global read (the chunk's counts or bases,
+// bitmap words, ids) is issued first.  Each CTA then derives the expert
+// offsets itself: the per-expert totals n_e come from K2, or, for a small
+// layer without K2 (chunks x experts <= kInlineBaseCounts), from summing the
+// count array, which also gives this chunk's bases; a block scan of n_e gives
+// expert_token_offsets.  The word prefixes of every expert come from a
+// shuffle scan over its 32 words (4 per thread); each (token, slot) then gets
+// pos = off[e] + base[e][c] + wordprefix + popc(bits below).
 // token_expert_indices and token_index_map are written token-major, one
 // vector per token, and expert_token_indices[pos] = token.
+// The GEMM metadata that K2 used to need a launch of its own is split over
+// the CTAs here: a slice of the tile -> expert table (binary search in the
+// padded offsets), a slice of the experts' load ranks, and, in CTA 0,
+// expert_token_offsets, the padded offsets, the counts, the tile count and
+// the (L, E, K) the build was made for.
+constexpr int kInlineBaseCounts = 32768;
+
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
                                                            const uint32_t* __restrict__ bitmap, int64_t C,
-                                                           const int32_t* __restrict__ base,
-                                                           const int32_t* __restrict__ off, int32_t* __restrict__ D1,
-                                                           int32_t* __restrict__ D3, int32_t* __restrict__ D4) {
+                                                           const int32_t* __restrict__ cb, bool scanned,
+                                                           const int32_t* __restrict__ n_e_in,
+                                                           int32_t* __restrict__ D1, int32_t* __restrict__ D2,
+                                                           int32_t* __restrict__ D3, int32_t* __restrict__ D4,
+                                                           MetaView meta, int64_t max_tiles) {
   extern __shared__ int32_t sm[];
   uint32_t* words = reinterpret_cast<uint32_t*>(sm);         // [E][kRow]
   int32_t* ebase = sm + E * kRow;                            // [E]: off[e] + base[e][chunk]
-  uint16_t* wpre = reinterpret_cast<uint16_t*>(ebase + E);   // [E][kRow]: set bits before word w (odd row stride)
-  const int tid = threadIdx.x, lane = tid & 31;
+  int32_t* off = ebase + E;                                  // [E+1]: expert_token_offsets
+  int32_t* poff = off + E + 1;                               // [E+1]: padded row offsets
+  int32_t* ne = poff + E + 1;                                // [E]: tokens per expert
+  int32_t* cbase = ne + E;                                   // [E]: this chunk's base in each expert
+  uint16_t* wpre = reinterpret_cast<uint16_t*>(cbase + E);   // [E][kRow]: set bits before word w
+  __shared__ int wsum[32];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
   const int64_t wpe = C * kChunkWords;
 
   // ---- all global reads first
-  for (int e = tid; e < E; e += kThreads) ebase[e] = off[e] + base[(int64_t)e * C + chunk];
+  if (scanned) {
+    for (int e = tid; e < E; e += kThreads) {
+      ne[e] = n_e_in[e];
+      cbase[e] = cb[(int64_t)e * C + chunk];
+    }
+  }
   int e_k[kPasses][kMaxK];
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
@@ -315,7 +243,55 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
     uint32_t* dst = words + e * kRow + pc * 4;
     dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
   }
+  if (!scanned) {
+    // small layer: a warp per expert sums its chunk counts, before this
+    // chunk (the base) and over all chunks (n_e)
+    for (int e = warp; e < E; e += kThreads / 32) {
+      int before = 0, all = 0;
+      for (int64_t c = lane; c < C; c += 32) {
+        const int v = cb[(int64_t)e * C + c];
+        all += v;
+        if (c < chunk) before += v;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        all += __shfl_xor_sync(0xffffffffu, all, o);
+      }
+      if (lane == 0) {
+        cbase[e] = before;
+        ne[e] = all;
+      }
+    }
+  }
   __syncthreads();
+
+  // ---- expert offsets (exclusive scan of n_e) and padded offsets
+  {
+    constexpr int kEPT = kMaxE / kThreads;
+    int carry = 0, pcarry = 0;
+#pragma unroll
+    for (int q = 0; q < kEPT; ++q) {
+      const int e = tid + q * kThreads;
+      const int n = e < E ? ne[e] : 0;
+      const int pn = (n + kRowPad - 1) / kRowPad * kRowPad;
+      const int pre = block_excl_scan(n, wsum, &total);
+      const int tot = total;
+      const int ppre = block_excl_scan(pn, wsum, &total);
+      if (e < E) {
+        off[e] = carry + pre;
+        poff[e] = pcarry + ppre;
+      }
+      carry += tot;
+      pcarry += total;
+    }
+    if (tid == 0) {
+      off[E] = carry;
+      poff[E] = pcarry;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kThreads) ebase[e] = off[e] + cbase[e];
 
   // ---- word prefixes: thread i covers words 4g..4g+3 of expert i/8 (g = i%8);
   // the 8 threads of an expert are consecutive lanes and scan their counts
@@ -346,6 +322,27 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
     }
   }
   __syncthreads();
+
+  // ---- routing checks: ids in range, pairwise distinct per token (K*(K-1)/2
+  // compares); one atomic per CTA, and only for invalid routing
+  {
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kPasses; ++j) {
+      const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
+      if (t >= L) continue;
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        if (k >= K) break;
+        const int e = e_k[j][k];
+        if (e < 0 || e >= E) bad = true;
+#pragma unroll
+        for (int i = 0; i < k; ++i)
+          if (e == e_k[j][i]) bad = true;
+      }
+    }
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(meta.err, kErrBadRouting);
+  }
 
   // ---- place every (token, slot)
 #pragma unroll
@@ -386,6 +383,56 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
         }
     }
   }
+
+  // ---- GEMM metadata, split over the CTAs
+  // tile -> expert: tile m belongs to the expert whose padded rows hold row
+  // 128 m (non-empty segments only own rows); -1 past the last tile
+  const int64_t ntiles = poff[E] / kTileM;
+  const int64_t per = (max_tiles + gridDim.x - 1) / gridDim.x;
+  const int64_t m0 = (int64_t)blockIdx.x * per, m1 = min(max_tiles, m0 + per);
+  for (int64_t m = m0 + tid; m < m1; m += kThreads) {
+    int32_t v = -1;
+    if (m < ntiles) {
+      const int64_t row = m * kTileM;
+      int lo = 0, hi = E - 1;  // last e with poff[e] <= row
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (poff[mid] <= row) lo = mid;
+        else hi = mid - 1;
+      }
+      v = lo;
+    }
+    meta.tile_expert[m] = v;
+  }
+  // descending load, equal loads by index: the rank of expert e is the number
+  // of experts j with n_j > n_e, or n_j == n_e and j < e.  One warp per expert,
+  // the experts spread over the CTAs.
+  const int nwarps = kThreads / 32;
+  for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
+    const int32_t me = ne[e];
+    int rank = 0;
+    for (int jx = lane; jx < E; jx += 32) {
+      const int32_t nj = ne[jx];
+      rank += (nj > me) || (nj == me && jx < e);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (lane == 0) meta.order[rank] = e;
+  }
+  if (blockIdx.x != 0) return;
+  if (tid == 0) {
+    *meta.num_m_tiles = (int32_t)ntiles;
+    *meta.padded_rows = poff[E];
+    // the shape this build was made for, checked by every forward/backward kernel
+    meta.hdr[kHdrL] = (int32_t)L;
+    meta.hdr[kHdrE] = E;
+    meta.hdr[kHdrK] = K;
+  }
+  for (int e = tid; e <= E; e += kThreads) {
+    D2[e] = off[e];
+    meta.pad_off[e] = poff[e];
+    if (e < E) meta.n_e[e] = ne[e];
+  }
 }
 
 }  // namespace
@@ -423,10 +470,12 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   const int E = s.E, K = s.K;
   const int64_t L = s.L, LK = L * K;
   MetaView meta = meta_view(out.meta, E);
-  MB_CUDA(cudaMemsetAsync(out.meta, 0, 8 * sizeof(int32_t), st));
   const int64_t C = num_chunks(L);
   const int64_t mt = max_m_tiles(LK, E);
   if (L == 0) {
+    // the header (error word, tile count, L = E = K = 0) is cleared here;
+    // with tokens, K1 clears the error word and K3 writes the rest
+    MB_CUDA(cudaMemsetAsync(out.meta, 0, 8 * sizeof(int32_t), st));
     // no tokens: offsets and counts are zero, no tiles
     MB_CUDA(cudaMemsetAsync(out.expert_token_offsets, 0, sizeof(int32_t) * (E + 1), st));
     MB_CUDA(cudaMemsetAsync(meta.n_e, 0, sizeof(int32_t) * (E + (E + 1)), st));
@@ -441,22 +490,19 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   bitmap_kernel<<<(unsigned)C, kThreads, sm1, st>>>(ids, L, E, K, w.bitmap, w.base, C, meta.err);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
-  MB_CUDA(cudaGetLastError());
-  count_launch();
-  {
-    int64_t g = (mt + 1023) / 1024;  // about 4 tile entries (binary searches) per thread
-    if (g > sm_count()) g = sm_count();
-    if (g < 1) g = 1;
-    offsets_kernel<<<(unsigned)g, kThreads, 0, st>>>(meta.n_e, E, out.expert_token_offsets, meta, mt, L, K);
+  // Large layers scan each expert's chunk counts in K2 (one CTA per expert);
+  // small ones let every K3 CTA sum the counts it needs.
+  const bool scanned = C * E > kInlineBaseCounts;
+  if (scanned) {
+    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
+    MB_CUDA(cudaGetLastError());
+    count_launch();
   }
-  MB_CUDA(cudaGetLastError());
-  count_launch();
-  const size_t sm3 = (size_t)E * kRow * 4 + (size_t)E * sizeof(int32_t) + (size_t)E * kRow * 2;
+  const size_t sm3 = (size_t)E * kRow * 4 + (size_t)(5 * E + 2) * sizeof(int32_t) + (size_t)E * kRow * 2;
   if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, out.expert_token_offsets,
-                                                      out.expert_token_indices, out.token_expert_indices,
-                                                      out.token_index_map);
+  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, scanned, meta.n_e,
+                                                      out.expert_token_indices, out.expert_token_offsets,
+                                                      out.token_expert_indices, out.token_index_map, meta, mt);
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
