@@ -118,7 +118,7 @@ typedef struct {
 MOEBLAZE_API size_t moeblaze_dispatch_meta_bytes(const moeblaze_shape* s);
 MOEBLAZE_API size_t moeblaze_dispatch_workspace_bytes(const moeblaze_shape* s);
 /* Activations kept from forward to backward: A = x W1 and (SwiGLU) B = x W2,
- * expert-major with each expert's rows padded to a multiple of 128, in the
+ * expert-major with each expert's rows padded to a multiple of 256, in the
  * layer dtype.  0 for the identity expert. */
 MOEBLAZE_API size_t moeblaze_saved_bytes(const moeblaze_shape* s);
 MOEBLAZE_API size_t moeblaze_forward_workspace_bytes(const moeblaze_shape* s);

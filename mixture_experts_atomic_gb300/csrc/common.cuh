@@ -15,7 +15,7 @@ namespace moeblaze {
 // ---------------------------------------------------------------- constants
 constexpr int kChunkTokens = 1024;       // tokens per dispatch chunk (32 bitmap words)
 constexpr int kChunkWords = kChunkTokens / 32;
-constexpr int kRowPad = 128;             // expert row segments are padded to this (one GEMM M tile)
+constexpr int kRowPad = 256;             // expert row segments are padded to this (a pair of GEMM M tiles)
 constexpr int kTileM = 128;              // rows of one GEMM tile
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 8;

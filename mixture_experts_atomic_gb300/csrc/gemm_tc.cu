@@ -19,8 +19,17 @@
 // The CTAs claim tiles from a per-launch counter (weight-gradient tiles in
 // descending order of expert load), so skewed expert loads balance.
 //
+// Paired stages (down with stored H, dH, dX, when the reduction is at least
+// 64 k-blocks long): the kernel runs as clusters of two CTAs that take two
+// 128-row tiles of one expert at the same n-tile.  Both need the same weight tiles: each CTA loads half of the boxes
+// and multicasts them to both, halving the weight bytes each SM pulls from
+// L2.  A stage is free again once both CTAs' MMAs have consumed it (their
+// commits arrive in both CTAs), and the leader (rank 0) claims the pair tiles
+// and posts them into both CTAs' tile queues.
+//
 // Row space: an expert's routed rows form a segment of a padded row space,
-// [pad_off[e], pad_off[e+1]), 128-row aligned, so every 128-row M tile
+// [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile (and
+// every pair of them, see below)
 // belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
 // routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
 // gather a valid token and are zero where they feed a reduction.
@@ -93,6 +102,17 @@ __host__ __device__ constexpr bool is_fused(int m) {
 }
 __host__ __device__ constexpr bool fused_sw(int m) { return m == DOWN_SWIGLU || m == DW3_SWIGLU; }
 __host__ __device__ constexpr bool is_wgrad(int m) { return m == DW12 || m == DW1 || is_dw3(m); }
+// stages that can run as clusters of two CTAs sharing (multicasting) the
+// weight tiles; the host pairs them when the reduction is long
+__host__ __device__ constexpr bool pairable(int m) { return m == DOWN_H || m == DH_SWIGLU || m == DH_SILU || m == DX; }
+// Pairing pays off on long reductions with many tiles (measured: the
+// Mixtral-like layer's dX 11% and dH 6% faster); on a small layer the
+// pairs' lockstep costs more than the shared loads save.
+constexpr int kPairMinKblocks = 64;
+constexpr int kPairMinTilesPerSm = 16;
+inline bool pair_stage(int kblocks, int64_t tiles) {
+  return kblocks >= kPairMinKblocks && tiles >= (int64_t)kPairMinTilesPerSm * sm_count();
+}
 // Warp roles: producers 0-3, in the fused stages eight transform warps
 // 4-11, then the MMA warp and four epilogue warps.
 __host__ __device__ constexpr int helper_warps(int m) { return is_fused(m) ? 8 : 0; }
@@ -190,14 +210,30 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// the same test with acquire at cluster scope: for barriers that the peer CTA
+// of a cluster arrives on after writing this CTA's shared memory
+__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of `parity` of `bar`; false on expiry or, when
 // `abort_s` is given, as soon as another role of the CTA has given up.
+// CL: acquire at cluster scope.
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int32_t* err,
                                              uint64_t limit_ns = kTimeoutNs) {
-  if (mbar_try(bar, parity)) return true;
+  auto test = [&]() { return CL ? mbar_try_cl(bar, parity) : mbar_try(bar, parity); };
+  if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
+    if (test()) return true;
     if ((it & 63u) == 0) {
       if (abort_s && *abort_s) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -214,6 +250,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// multicast form: the box lands at `dst` and completes `bar` in every CTA of `mask`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the address of this CTA's shared-memory word `addr` in the CTA of `rank`
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -246,6 +312,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// arrive on `bar` at the same offset in every CTA of `mask` once this thread's MMAs retire
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -421,10 +494,14 @@ struct Tile {
   int n_e;      // tokens routed to e
 };
 
-template <int MODE>
-__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt) {
+// Tile `tile` of the launch.  In the paired stages a tile id names a pair of
+// 128-row tiles of one expert (a 256-row slice of its padded segment) at one
+// n-tile, and `rank` picks this CTA's half.
+template <int MODE, bool PAIR>
+__device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt, int rank) {
   Tile t;
   constexpr int TN = tile_n(MODE);
+  constexpr int PM = PAIR ? 2 : 1;
   int nt;
   if constexpr (is_wgrad(MODE)) {
     const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
@@ -437,12 +514,15 @@ __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt
     t.pad0 = p.meta.pad_off[t.e];
     t.kblocks = (p.meta.pad_off[t.e + 1] - t.pad0) / BK;
   } else {
-    constexpr int GM = 16;
+    // groups of 16 m-tiles (8 pairs) walk the n-tiles together, so the weight
+    // tiles they share stay in L2
+    constexpr int GM = 16 / PM;
+    const int nmu = num_mt / PM;
     const int64_t per_g = (int64_t)GM * p.n_tiles;
     const int g = (int)(tile / per_g);
     const int r = (int)(tile % per_g);
-    const int gm = min(GM, num_mt - g * GM);
-    const int mt = g * GM + r % gm;
+    const int gm = min(GM, nmu - g * GM);
+    const int mt = (g * GM + r % gm) * PM + (PM == 2 ? rank : 0);
     nt = r / gm;
     t.e = p.meta.tile_expert[mt];
     t.row0 = mt * BM;
@@ -485,7 +565,7 @@ __host__ __device__ constexpr bool cp_a(int m) {
 }
 __host__ __device__ constexpr bool cp_b(int m) { return is_dw3(m); }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
   // FUSED: transform warps recompute the A operand from the saved tiles
@@ -493,6 +573,12 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
   constexpr int MMA_WARP = mma_warp(MODE);
   constexpr int NST = stages_of(MODE), SB = stage_bytes_of(MODE);
   constexpr int LAG = NST - 2;  // cp.async groups a producer thread keeps in flight
+  // PAIR: clusters of two CTAs share the weight tiles (multicast) and the
+  // tile queue (filled by rank 0)
+  static_assert(!PAIR || pairable(MODE), "stage cannot run paired");
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  const int64_t cta0 = PAIR ? blockIdx.x / 2 : blockIdx.x;      // cluster (pair) index
+  const int64_t ncta = PAIR ? gridDim.x / 2 : gridDim.x;        // clusters (pairs) in the grid
   // A dispatch built for another (L, E, K) lays out its tables differently:
   // record the mismatch and read none of them (every thread reads the same
   // three header words, so the whole CTA leaves here together, before any
@@ -520,7 +606,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       // full: the gathering producer threads (cp.async stages), the transform
       // warps (fused stages), else thread 0's arrive.expect_tx
       mbar_init(bar(s), FUSED || CP ? (CP ? PRODUCER_THREADS : 0) + transform_threads(MODE) : 1);
-      mbar_init(bar(4 + s), 1);
+      // empty: this CTA's MMA commit (and the peer's, when the pair shares the stage's weight tiles)
+      mbar_init(bar(4 + s), PAIR ? 2 : 1);
       mbar_init(bar(48 + s), 1);
     }
     mbar_init(bar(8), 1);
@@ -532,8 +619,9 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       mbar_init(bar(32 + i), 1);
       // readers of a queue slot: the producer warps (thread 0 alone in the
       // TMA-only stages), the transform warps (fused stages), the MMA thread
-      // and the four epilogue warps
-      mbar_init(bar(40 + i), (CP ? PRODUCER_WARPS : 1) + helper_warps(MODE) + 1 + 4);
+      // and the four epilogue warps; in a pair rank 0's slot is also freed by
+      // the peer's readers (rank 1 posts nothing)
+      mbar_init(bar(40 + i), ((CP ? PRODUCER_WARPS : 1) + helper_warps(MODE) + 1 + 4) * (PAIR ? 2 : 1));
     }
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -546,31 +634,39 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast or remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
-  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)num_mt * p.n_tiles;
+  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)(num_mt / (PAIR ? 2 : 1)) * p.n_tiles;
   int32_t* err = p.meta.err;
   const uint64_t lim = p.wait_ns;
 
   // queue position j lives in slot j % TQ, phase (j / TQ) & 1
-  auto q_post = [&](int j, long long id) -> bool {  // thread 0
+  auto q_post = [&](int j, long long id) -> bool {  // thread 0 (of rank 0 in a pair)
     const int sl = j % TQ;
-    if (!wait_bounded(bar(40 + sl), (uint32_t)((j / TQ) & 1) ^ 1u, abort_s, err, lim)) return false;
+    if (!wait_bounded<PAIR>(bar(40 + sl), (uint32_t)((j / TQ) & 1) ^ 1u, abort_s, err, lim)) return false;
     tq[sl] = id;
     mbar_arrive(bar(32 + sl));
+    if constexpr (PAIR) {
+      // the same id in the peer's slot, then its full barrier (release at cluster scope)
+      st_cluster_u64(peer_addr(smem_u32((const void*)(tq + sl)), 1u), (unsigned long long)id);
+      mbar_arrive_cluster(peer_addr(bar(32 + sl), 1u));
+    }
     return true;
   };
   auto q_take = [&](int j) -> long long {  // one thread per reader; -1 once the CTA gives up
     const int sl = j % TQ;
-    if (!wait_bounded(bar(32 + sl), (uint32_t)(j / TQ) & 1u, abort_s, err, lim)) return -1;
+    if (!wait_bounded<PAIR>(bar(32 + sl), (uint32_t)(j / TQ) & 1u, abort_s, err, lim)) return -1;
     const long long id = tq[sl];
-    mbar_arrive(bar(40 + sl));
+    if (PAIR && rank == 1) mbar_arrive_cluster(peer_addr(bar(40 + sl), 0u));  // rank 0 owns the slots
+    else mbar_arrive(bar(40 + sl));
     return id;
   };
-  // tile of queue position j >= 2 (positions 0 and 1 are blockIdx.x and blockIdx.x + gridDim.x)
-  auto claim = [&]() -> long long { return 2ll * gridDim.x + (long long)atomicAdd(p.sched, 1ull); };
+  // tile of queue position j >= 2 (positions 0 and 1 are this CTA's (pair's)
+  // first two: cta0 and cta0 + ncta)
+  auto claim = [&]() -> long long { return 2ll * ncta + (long long)atomicAdd(p.sched, 1ull); };
 
   if (warp < PRODUCER_WARPS) {
     // ================================================================ producer
@@ -615,17 +711,17 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         }
         return id;
       };
-      if (pt == 0 && q_post(0, blockIdx.x)) q_post(1, (long long)blockIdx.x + gridDim.x);
+      if (pt == 0 && rank == 0 && q_post(0, cta0)) q_post(1, (long long)cta0 + ncta);
       long long tile = take(0);
       Tile t;
       if (tile >= 0 && tile < total) {
-        t = decode<MODE>(p, tile, num_mt);
+        t = decode<MODE, PAIR>(p, tile, num_mt, rank);
         load_tile_tokens(t, rtok, wtok);
       }
       ok = tile >= 0;
       for (int j = 0; ok && tile < total; ++j) {
         long long pending = 0;
-        if (pt == 0) pending = claim();  // for position j + 2, posted after this tile's loads are issued
+        if (pt == 0 && rank == 0) pending = claim();  // for position j + 2, posted after this tile's loads are issued
         const long long ntile = take(j + 1);
         if (ntile < 0) {
           ok = false;
@@ -633,7 +729,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         }
         Tile tn;
         if (ntile < total) {
-          tn = decode<MODE>(p, ntile, num_mt);
+          tn = decode<MODE, PAIR>(p, ntile, num_mt, rank);
           load_tile_tokens(tn, rnext, wfirst);
         }
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
@@ -689,6 +785,15 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
             }
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
+            // box j of the weight tile both CTAs of a pair share: the CTA of
+            // rank j % 2 loads it for both (multicast); unpaired, this CTA
+            auto wbox = [&](int jb, uint32_t dst, const CUtensorMap* m, int c0, int c1, uint32_t b) {
+              if constexpr (PAIR) {
+                if ((jb & 1) == rank) tma_load_2d_mc(dst, m, c0, c1, b, (uint16_t)0x3);
+              } else {
+                tma_load_2d(dst, m, c0, c1, b);
+              }
+            };
             if constexpr (MODE == DX || MODE == DOWN_H) {
               tma_load_2d(sA, &p.tmA, k0, t.row0, full);
             } else if constexpr (MODE == DW3_H) {
@@ -706,23 +811,23 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               }
             }
             if constexpr (MODE == UP_SWIGLU) {
-              tma_load_2d(sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
-              tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0, full);
-              tma_load_2d(sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0, full);
-              tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
+              wbox(0, sB, &p.tmB0, t.n0, t.e * p.d + k0, full);
+              wbox(1, sB + 8192, &p.tmB0, t.n0 + 64, t.e * p.d + k0, full);
+              wbox(2, sB + 16384, &p.tmB1, t.n0, t.e * p.d + k0, full);
+              wbox(3, sB + 24576, &p.tmB1, t.n0 + 64, t.e * p.d + k0, full);
             } else if constexpr (MODE == UP_SILU) {
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
+              for (int j = 0; j < t.nw / 64; ++j) wbox(j, sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.d + k0, full);
             } else if constexpr (is_down(MODE)) {
               const uint32_t wb = FUSED ? loaded : full;
-              for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, wb);
+              for (int j = 0; j < t.nw / 64; ++j) wbox(j, sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.e * p.h + k0, wb);
             } else if constexpr (MODE == DH_SWIGLU || MODE == DH_SILU) {
               for (int j = 0; j < t.nw / 128; ++j)
-                tma_load_2d(sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
+                wbox(j, sB + j * 16384, &p.tmB0, k0, t.e * p.h + t.n0 + 128 * j, full);
             } else if constexpr (MODE == DX) {
               const bool second = kb >= p.ksplit;
               const CUtensorMap* m = second ? &p.tmB1 : &p.tmB0;
               const int kc = second ? k0 - p.ksplit * BK : k0;
-              for (int j = 0; j < t.nw / 128; ++j) tma_load_2d(sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j, full);
+              for (int j = 0; j < t.nw / 128; ++j) wbox(j, sB + j * 16384, m, kc, t.e * p.d + t.n0 + 128 * j, full);
             } else if constexpr (MODE == DW12) {
               tma_load_2d(sB, &p.tmB0, t.n0, t.pad0 + k0, full);
               tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0, full);
@@ -774,7 +879,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if (++s == NST) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        if (pt == 0) ok = q_post(j + 2, pending);
+        if (pt == 0 && rank == 0) ok = q_post(j + 2, pending);
         if constexpr (CP) {
           if (warp == 0) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
@@ -818,7 +923,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         if (lane == 0) tile = q_take(j);
         tile = __shfl_sync(0xffffffffu, tile, 0);
         if (tile < 0 || tile >= total) break;
-        const Tile t = decode<MODE>(p, tile, num_mt);
+        const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           float g2[2] = {1.f, 1.f};
           if constexpr (is_dw3(MODE)) {
@@ -851,7 +956,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       bool ok = true;
       long long tile = q_take(0);
       Tile t;
-      if (tile >= 0 && tile < total) t = decode<MODE>(p, tile, num_mt);
+      if (tile >= 0 && tile < total) t = decode<MODE, PAIR>(p, tile, num_mt, rank);
       for (int j = 0; ok; ++j) {
         if (tile < 0) {
           ok = false;
@@ -866,7 +971,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         bool fetched = false;
         auto fetch_next = [&]() {
           ntile = q_take(j + 1);
-          if (ntile >= 0 && ntile < total) tn = decode<MODE>(p, ntile, num_mt);
+          if (ntile >= 0 && ntile < total) tn = decode<MODE, PAIR>(p, ntile, num_mt, rank);
           fetched = true;
         };
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
@@ -887,7 +992,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
             const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
             mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
-          mma_commit(bar(4 + s));
+          if constexpr (PAIR) mma_commit_mc(bar(4 + s), (uint16_t)0x3);  // frees the stage in both CTAs
+          else mma_commit(bar(4 + s));
           if (++s == NST) { s = 0; ph ^= 1u; }
           if (kb == 0) fetch_next();
         }
@@ -915,7 +1021,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       if (lane == 0) tile = q_take(j);
       tile = __shfl_sync(0xffffffffu, tile, 0);
       if (tile < 0 || tile >= total) break;
-      const Tile t = decode<MODE>(p, tile, num_mt);
+      const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
       constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
@@ -1111,6 +1217,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no multicast or remote arrive is still headed for this CTA
   tc_fence_after();
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
@@ -1148,13 +1255,44 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+// Launch one GEMM stage.  `tiles_bound` bounds the number of 128-row tiles;
+// one CTA per SM, never more than there are tiles.  PAIR: clusters of two
+// CTAs on pairs of tiles (see the kernel).
+template <int MODE, bool PAIR = false>
 moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
   if (tiles_bound <= 0) return MOEBLAZE_OK;
-  auto kern = moe_gemm_kernel<MODE>;
+  auto kern = moe_gemm_kernel<MODE, PAIR>;
   MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of(MODE)));
-  const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
-  kern<<<(unsigned)g, num_threads(MODE), smem_bytes_of(MODE), st>>>(p);
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * (sm_count() / 2)));
+    cfg.blockDim = dim3(num_threads(MODE));
+    cfg.dynamicSmemBytes = smem_bytes_of(MODE);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as can be resident at once, never more than pair tiles
+    static int resident[64][16] = {};
+    int dev = 0;
+    MB_CUDA(cudaGetDevice(&dev));
+    int& clusters = resident[dev & 63][MODE & 15];
+    if (clusters == 0) {
+      MB_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
+      if (clusters < 1) return MOEBLAZE_ERR_UNSUPPORTED;
+    }
+    const int64_t pairs = tiles_bound / 2 < clusters ? tiles_bound / 2 : clusters;
+    if (pairs < 1) return MOEBLAZE_OK;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    MB_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
+  } else {
+    const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
+    kern<<<(unsigned)g, num_threads(MODE), smem_bytes_of(MODE), st>>>(p);
+  }
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;
@@ -1245,7 +1383,8 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.acc32 = wsY32;
       p.sched = sched + 1;
       const int64_t nt = mt_bound * p.n_tiles;
-      moeblaze_status r = !rec ? launch<DOWN_H>(p, nt, st)
+      const bool pair = pair_stage(p.kblocks, nt);
+      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, true>(p, nt, st) : launch<DOWN_H>(p, nt, st))
                                : (sw ? launch<DOWN_SWIGLU>(p, nt, st) : launch<DOWN_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
@@ -1293,7 +1432,10 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!rec && !make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       p.ld0 = nb * s.h;
-      moeblaze_status r = sw ? launch<DH_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<DH_SILU>(p, mt_bound * p.n_tiles, st);
+      const int64_t nt = mt_bound * p.n_tiles;
+      const bool pair = pair_stage(p.kblocks, nt);
+      moeblaze_status r = sw ? (pair ? launch<DH_SWIGLU, true>(p, nt, st) : launch<DH_SWIGLU>(p, nt, st))
+                             : (pair ? launch<DH_SILU, true>(p, nt, st) : launch<DH_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
@@ -1308,7 +1450,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsdX32;
       p.sched = sched + 1;
-      moeblaze_status r = launch<DX>(p, mt_bound * p.n_tiles, st);
+      const int64_t nt = mt_bound * p.n_tiles;
+      moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, true>(p, nt, st) : launch<DX>(p, nt, st);
       if (r != MOEBLAZE_OK) return r;
     }
   }

@@ -5,7 +5,7 @@
 // operands staged through shared memory.
 //
 // Row space: every expert's routed rows occupy a segment of the padded row
-// space [pad_off[e], pad_off[e+1]), a multiple of 128 rows; row q of expert e
+// space [pad_off[e], pad_off[e+1]), a multiple of 256 rows; row q of expert e
 // with i = q - pad_off[e] < n_e is routed row p = off[e] + i of token
 // D1[p].  Padding rows compute on a valid token (so every gathered address is
 // in bounds) and are written as zeros where they feed a reduction.

@@ -39,7 +39,7 @@ def check_dispatch(layer: MoELayer, ids_cpu: torch.Tensor, E: int):
     num_mt, n_e, pad, order = layer.meta()
     n_e = n_e.numpy(); pad = pad.numpy(); order = order.numpy()
     assert np.array_equal(n_e, np.diff(D2))
-    padded = (n_e + 127) // 128 * 128
+    padded = (n_e + 255) // 256 * 256   # expert segments padded to a pair of 128-row tiles
     assert np.array_equal(pad, np.concatenate([[0], np.cumsum(padded)]))
     assert num_mt == pad[-1] // 128
     # experts by descending load, equal loads by index

@@ -60,7 +60,7 @@ def test_sizes_and_shape_validation():
     _lib()
     s = B.make_shape(512, 64, 128, 8, 2, B.F32, "swiglu")
     assert B.moeblaze_dispatch_meta_bytes(s) > 0
-    rows = (1024 + 8 * 127 + 127) // 128 * 128   # L*K plus 127 padding rows per expert
+    rows = (1024 + 8 * 255 + 255) // 256 * 256   # L*K plus 255 padding rows per expert
     assert B.moeblaze_saved_bytes(s) == 2 * rows * 128 * 4
     bad = [
         B.make_shape(512, 64, 128, 2, 3, B.F32, "swiglu"),        # K > E
@@ -180,7 +180,7 @@ def test_recompute_flag_sizes_and_validation():
     for act in ("swiglu", "silu"):
         a = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act)
         r = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act, B.RECOMPUTE_H)
-        rows = -(-(70000 * 2 + 127 * 16) // 128) * 128
+        rows = -(-(70000 * 2 + 255 * 16) // 256) * 256
         h_bytes = -(-(rows * 384 * 2) // 256) * 256
         g_bytes = -(-(rows * 4) // 256) * 256
         assert B.moeblaze_forward_workspace_bytes(a) - B.moeblaze_forward_workspace_bytes(r) == h_bytes

@@ -111,6 +111,17 @@ def test_workload_sampled(ci, recompute_h):
     print(I.CONFIGS[ci].name, "recompute_h" if recompute_h else "", errs, frac)
 
 
+@pytest.mark.parametrize("L,E,K,act", [(10000, 3, 2, "swiglu"), (7000, 6, 3, "silu")])
+def test_paired_stages_sampled(L, E, K, act):
+    """d = h = 4096 and enough rows for 16 tiles per SM: the dH, dX and
+    stored-H down projections (64+ k-blocks) run as clusters of two CTAs that
+    share the weight tiles (a shape the small whole-tensor cases do not
+    reach); sampled rows, columns and every expert's weight gradients."""
+    cfg = I.MoEConfig(f"t_paired_{act}", L, 4096, 4096, E, K, act, "bf16", 23, "softmax")
+    errs, frac = sampled_compare(cfg)
+    print(cfg.name, errs, frac)
+
+
 def test_identity_workload_sampled():
     sampled_compare(I.CONFIGS[4], n_tok=64)
 

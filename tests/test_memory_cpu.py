@@ -50,7 +50,7 @@ def test_memory_report_retained_is_saved_plus_indices():
     layer = _host_layer(cfg)
     rep = bench.memory_report(cfg, layer, 0)
     LK = cfg.L * cfg.K
-    rows = -(-(LK + 127 * cfg.E) // 128) * 128
+    rows = -(-(LK + 255 * cfg.E) // 256) * 256
     assert rep["saved_activation_bytes"] == 2 * rows * cfg.h * 2
     assert rep["index_bytes"] == 3 * LK * 4 + (cfg.E + 4) * 4 + B.moeblaze_dispatch_meta_bytes(layer.shape)
     assert rep["retained_fwd_to_bwd_bytes"] == rep["saved_activation_bytes"] + rep["index_bytes"]
