@@ -474,7 +474,8 @@ def run_recompute_leg(args, cfg, inp, dev, flush, pk, tpk):
         flush_l2(flush)
         step()
     n = min(args.steps, 10)
-    names_f, names_b = ["up", "down", "convert_y"], ["dh", "dx", "dw12", "dw3", "convert_dx"]
+    # in this mode the backward runs its dW3 GEMM first (see moeblaze_set_stage_events)
+    names_f, names_b = ["up", "down", "convert_y"], ["dw3", "dh", "dx", "dw12", "convert_dx"]
     per = {k: [] for k in names_f + names_b}
     tot = []
     for _ in range(n):

@@ -78,8 +78,9 @@ typedef struct {
  * otherwise): the down projection and the dW3 GEMM then recompute H and Hg
  * tile by tile from the saved A and B inside their operand pipelines.  The
  * forward and the backward workspace each shrink by padded_rows x h
- * elements (the backward keeps one fp32 gate per padded row instead); those
- * two GEMMs do the extra recompute.  Results agree with the default within
+ * elements (the saved buffer grows by one fp32 gate per padded row); those
+ * two GEMMs do the extra recompute, and the backward runs its dW3 GEMM
+ * first, while the saved A and B are still intact.  Results agree with the default within
  * the bf16 tolerance (SiLU is then evaluated as a/2 (1 + tanh(a/2)) with the
  * hardware tanh approximation). */
 #define MOEBLAZE_RECOMPUTE_H 1
@@ -119,7 +120,8 @@ MOEBLAZE_API size_t moeblaze_dispatch_meta_bytes(const moeblaze_shape* s);
 MOEBLAZE_API size_t moeblaze_dispatch_workspace_bytes(const moeblaze_shape* s);
 /* Activations kept from forward to backward: A = x W1 and (SwiGLU) B = x W2,
  * expert-major with each expert's rows padded to a multiple of 256, in the
- * layer dtype.  0 for the identity expert. */
+ * layer dtype (bf16 with MOEBLAZE_RECOMPUTE_H: followed by one fp32 gate per
+ * padded row).  0 for the identity expert. */
 MOEBLAZE_API size_t moeblaze_saved_bytes(const moeblaze_shape* s);
 MOEBLAZE_API size_t moeblaze_forward_workspace_bytes(const moeblaze_shape* s);
 MOEBLAZE_API size_t moeblaze_backward_workspace_bytes(const moeblaze_shape* s);
@@ -209,7 +211,11 @@ MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const voi
  * branches' input gradients are accumulated in one accumulator, and dX is
  * reduced back into (L, d).
  *   dY      device (L,d) dtype                 x, gates, disp, W*: as forward
- *   saved   as written by moeblaze_forward
+ *   saved   as written by moeblaze_forward.  bf16: consumed - the dH GEMM,
+ *           the last reader of A and B, writes dA and dB over them in place
+ *           (no separate (rows x 2h) gradient buffer), so after the call it
+ *           no longer holds the forward's activations; run the forward again
+ *           before another backward.  fp32: left unchanged.
  *   dX      device (L,d) dtype, overwritten
  *   dW1,dW2 device (E,d,h) dtype, overwritten  dW3 device (E,h,d) dtype, overwritten
  *           (dW2 NULL for SiLU; all three NULL for identity)
@@ -226,7 +232,7 @@ MOEBLAZE_API moeblaze_status moeblaze_forward(const moeblaze_shape* s, const voi
 MOEBLAZE_API moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x,
                                   const float* gates, const moeblaze_dispatch* disp,
                                   const void* W1, const void* W2, const void* W3,
-                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3,
+                                  void* saved, void* dX, void* dW1, void* dW2, void* dW3,
                                   float* dgates, void* ws, size_t ws_bytes, moeblaze_stream stream);
 
 /* ------------------------------------------------------------------ router
@@ -302,7 +308,10 @@ MOEBLAZE_API moeblaze_status moeblaze_dispatch_meta_check(const moeblaze_shape* 
  *             down-projection + combine, [3] after the final conversion;
  *   backward: [0] before the dH GEMM, [1] after it, [2] after the dX GEMM,
  *             [3] after the dW1/dW2 GEMM, [4] after the dW3 GEMM,
- *             [5] after the final conversion.
+ *             [5] after the final conversion; bf16 with MOEBLAZE_RECOMPUTE_H
+ *             the dW3 GEMM runs first: [0] before it, [1] after it, [2]
+ *             after dH, [3] after dX, [4] after dW1/dW2, [5] after the
+ *             conversion.
  * Only the first `n` events are recorded.  NULL switches recording off.
  *
  * moeblaze_kernel_launches: number of CUDA kernels this library has launched

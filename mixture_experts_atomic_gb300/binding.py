@@ -444,12 +444,20 @@ def device_error(shape: Shape, disp: DispatchBuffers, stream=None) -> int:
     return code
 
 
+def padded_rows(shape: Shape) -> int:
+    """Rows of the expert-major row space: L*K plus each expert's padding to
+    a multiple of 256 rows, at most."""
+    r = shape.L * shape.K + shape.E * 255
+    return (r + 255) // 256 * 256
+
+
 def saved_views(shape: Shape, layer: LayerBuffers, dtype):
-    """(A, B) views of the saved checkpoint: (padded_rows, h) each (B None for SiLU)."""
+    """(A, B) views of the saved checkpoint: (padded_rows, h) each (B None for
+    SiLU).  After a bf16 backward they hold dA and dB."""
     es = 4 if dtype == torch.float32 else 2
     h = shape.h
     nb = 2 if shape.act == SWIGLU else 1
-    rows = moeblaze_saved_bytes(shape) // (nb * h * es)
+    rows = padded_rows(shape)
     t = layer.saved[: rows * nb * h * es].view(dtype).view(nb, rows, h)
     return t[0], (t[1] if nb == 2 else None)
 

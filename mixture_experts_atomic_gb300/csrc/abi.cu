@@ -98,9 +98,10 @@ bool recompute_h(const moeblaze_shape* s) {
   return s->dtype == MOEBLAZE_BF16 && s->act != MOEBLAZE_IDENTITY && (s->flags & MOEBLAZE_RECOMPUTE_H);
 }
 
+// saved:            A | B (SwiGLU) (rows x h each); bf16 with recompute: | one fp32 gate per row
 // forward scratch:  H (rows x h; not when recomputed) | y32 (L x d fp32) + tile counters (bf16 only)
-// backward scratch: dAB (rows x nb*h) | Hg (rows x h), or the row gates (rows fp32) when recomputed
-//                   | dX32 (L x d fp32) + tile counters (bf16 only)
+// backward scratch: bf16: Hg (rows x h; not when recomputed) | dX32 (L x d fp32) + tile counters
+//                   (dA, dB overwrite the saved A, B);  fp32: dAB (rows x nb*h) | Hg (rows x h)
 size_t fwd_ws(const moeblaze_shape* s) {
   if (s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
@@ -110,14 +111,13 @@ size_t fwd_ws(const moeblaze_shape* s) {
 }
 size_t hg_bytes(const moeblaze_shape* s) {
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
-  return recompute_h(s) ? align_up((size_t)rows * 4, 256) : align_up((size_t)rows * s->h * elem(s), 256);
+  return recompute_h(s) ? 0 : align_up((size_t)rows * s->h * elem(s), 256);
 }
 size_t bwd_ws(const moeblaze_shape* s) {
   if (s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
-  size_t b = align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256) + hg_bytes(s);
-  if (s->dtype == MOEBLAZE_BF16) b += align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
-  return b;
+  if (s->dtype == MOEBLAZE_BF16) return hg_bytes(s) + align_up((size_t)s->L * s->d * 4, 256) + kSchedBytes;
+  return align_up((size_t)rows * nbranch(s) * s->h * elem(s), 256) + hg_bytes(s);
 }
 
 moeblaze_status zero_weight_grads(const moeblaze_shape* s, void* dW1, void* dW2, void* dW3, cudaStream_t st) {
@@ -175,7 +175,7 @@ size_t moeblaze_dispatch_workspace_bytes(const moeblaze_shape* s) {
 size_t moeblaze_saved_bytes(const moeblaze_shape* s) {
   if (check_shape(s) != MOEBLAZE_OK || s->act == MOEBLAZE_IDENTITY) return 0;
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
-  return (size_t)rows * nbranch(s) * s->h * elem(s);
+  return (size_t)rows * nbranch(s) * s->h * elem(s) + (recompute_h(s) ? (size_t)rows * 4 : 0);
 }
 
 size_t moeblaze_forward_workspace_bytes(const moeblaze_shape* s) {
@@ -253,7 +253,7 @@ moeblaze_status moeblaze_forward(const moeblaze_shape* s, const void* x, const f
 
 moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const void* x, const float* gates,
                                   const moeblaze_dispatch* disp, const void* W1, const void* W2, const void* W3,
-                                  const void* saved, void* dX, void* dW1, void* dW2, void* dW3, float* dgates,
+                                  void* saved, void* dX, void* dW1, void* dW2, void* dW3, float* dgates,
                                   void* ws, size_t ws_bytes, moeblaze_stream stream) {
   moeblaze_status r = check_shape(s);
   if (r != MOEBLAZE_OK) return r;
@@ -277,20 +277,19 @@ moeblaze_status moeblaze_backward(const moeblaze_shape* s, const void* dY, const
   const int64_t rows = max_padded_rows(s->L * s->K, s->E);
   char* w = reinterpret_cast<char*>(ws);
   const size_t es = elem(s);
-  char* dAB = w;
-  char* Hg = w + align_up((size_t)rows * nbranch(s) * s->h * es, 256);  // Hg, or the row gates when recomputed
   if (s->dtype == MOEBLAZE_F32) {
+    char* dAB = w;
+    char* Hg = w + align_up((size_t)rows * nbranch(s) * s->h * es, 256);
     return simt_backward(*s, (const float*)dY, (const float*)x, gates, *disp, (const float*)W1,
                          sw ? (const float*)W2 : nullptr, (const float*)W3, (const float*)saved, (float*)dX,
                          (float*)dW1, sw ? (float*)dW2 : nullptr, (float*)dW3, dgates, (float*)dAB, (float*)Hg, st);
   }
-  char* dX32 = Hg + hg_bytes(s);
-  const bool rec = recompute_h(s);
+  // bf16: Hg (not when recomputed) | dX32; dA, dB go over the saved A, B
+  char* dX32 = w + hg_bytes(s);
   return tc_backward(*s, (const __nv_bfloat16*)dY, (const __nv_bfloat16*)x, gates, *disp, (const __nv_bfloat16*)W1,
-                     sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (const __nv_bfloat16*)saved,
+                     sw ? (const __nv_bfloat16*)W2 : nullptr, (const __nv_bfloat16*)W3, (__nv_bfloat16*)saved,
                      (__nv_bfloat16*)dX, (__nv_bfloat16*)dW1, sw ? (__nv_bfloat16*)dW2 : nullptr, (__nv_bfloat16*)dW3,
-                     dgates, (__nv_bfloat16*)dAB, rec ? nullptr : (__nv_bfloat16*)Hg, rec ? (float*)Hg : nullptr,
-                     (float*)dX32, st);
+                     dgates, recompute_h(s) ? nullptr : (__nv_bfloat16*)w, (float*)dX32, st);
 }
 
 moeblaze_status moeblaze_device_error(const moeblaze_shape* s, const moeblaze_dispatch* disp, int32_t* code,

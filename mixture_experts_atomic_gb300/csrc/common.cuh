@@ -114,17 +114,17 @@ moeblaze_status simt_backward(const moeblaze_shape& s, const float* dY, const fl
                               float* wsdAB, float* wsHg, cudaStream_t st);
 
 // gemm_tc.cu (bf16 tensor-core path).  wsH / wsHg NULL selects the
-// recompute variants (MOEBLAZE_RECOMPUTE_H); wsRowg is used only by them.
+// recompute variants (MOEBLAZE_RECOMPUTE_H), which keep the row gates in
+// `saved`; the backward overwrites the saved A, B with dA, dB.
 moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, const float* gates,
                            const moeblaze_dispatch& disp, const __nv_bfloat16* W1, const __nv_bfloat16* W2,
                            const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved, __nv_bfloat16* wsH,
                            float* wsY32, cudaStream_t st);
 moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, const __nv_bfloat16* x,
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
-                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
+                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsRowg, float* wsdX32,
-                            cudaStream_t st);
+                            float* dgates, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st);
 
 // router.cu
 constexpr int kMaxRouterE = 256;

@@ -161,11 +161,11 @@ struct Params {
   const __nv_bfloat16* i0;
   const __nv_bfloat16* i1;
   float* acc32;
-  int ld0;          // row stride (elements) of o0 for the stages that need it
   const __nv_bfloat16* gsrc;  // gathered tensor (x or dY), rows of gld elements
   int gld;
   float* dg;                   // dH stage: gate gradients (L,K) fp32, or null
-  float* rowg;                 // gate of every padded row (0 for padding rows): written by dH, read by DW3
+  float* rowg;                 // gate of every padded row (0 for padding rows), recompute mode: written by
+                               // the down projection, read by the backward's DW3
   uint64_t wait_ns;            // limit of every bounded wait (kTimeoutNs unless a test sets a shorter one)
   int withhold;                // test of the failure path (DOWN_H): the first stage of each CTA's first
                                // tile is never issued, so the MMA's wait for it runs out
@@ -794,8 +794,12 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
                 tma_load_2d(dst, m, c0, c1, b);
               }
             };
-            if constexpr (MODE == DX || MODE == DOWN_H) {
+            if constexpr (MODE == DOWN_H) {
               tma_load_2d(sA, &p.tmA, k0, t.row0, full);
+            } else if constexpr (MODE == DX) {
+              // [dA | dB] along K: the first ksplit k-blocks from dA, the rest from dB
+              const bool second = kb >= p.ksplit;
+              tma_load_2d(sA, second ? &p.tmX : &p.tmA, second ? k0 - p.ksplit * BK : k0, t.row0, full);
             } else if constexpr (MODE == DW3_H) {
               tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
               tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
@@ -831,8 +835,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
             } else if constexpr (MODE == DW12) {
               tma_load_2d(sB, &p.tmB0, t.n0, t.pad0 + k0, full);
               tma_load_2d(sB + 8192, &p.tmB0, t.n0 + 64, t.pad0 + k0, full);
-              tma_load_2d(sB + 16384, &p.tmB0, p.h + t.n0, t.pad0 + k0, full);
-              tma_load_2d(sB + 24576, &p.tmB0, p.h + t.n0 + 64, t.pad0 + k0, full);
+              tma_load_2d(sB + 16384, &p.tmB1, t.n0, t.pad0 + k0, full);
+              tma_load_2d(sB + 24576, &p.tmB1, t.n0 + 64, t.pad0 + k0, full);
             } else if constexpr (MODE == DW1) {
               for (int j = 0; j < t.nw / 64; ++j) tma_load_2d(sB + j * 8192, &p.tmB0, t.n0 + 64 * j, t.pad0 + k0, full);
             }
@@ -1103,6 +1107,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
             }
           }
         } else if constexpr (is_down(MODE) || MODE == DX) {
+          // MOEBLAZE_RECOMPUTE_H: the forward keeps every padded row's gate
+          // for the backward's dW3 (0 on padding rows); once per row
+          if constexpr (is_down(MODE)) {
+            if (p.rowg && t.n0 == 0) p.rowg[q] = valid ? g : 0.f;
+          }
           float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
           for (int c = 0; c < t.nw / 32; ++c) {
             MB_TMEM_LD32(tbase + 32 * c, ra);
@@ -1161,15 +1170,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               }
             }
             staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
-            if constexpr (SW) staged_store(ring, &p.tmO0, p.h + t.n0 + 32 * c, wrow0, dB, valid, lane);
+            if constexpr (SW) staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, dB, valid, lane);
             // Hg for the dW3 GEMM (not with MOEBLAZE_RECOMPUTE_H)
             if (p.o1) staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
           }
           if (valid && p.dg) atomicAdd(p.dg + (int64_t)tok * p.K + kslot, dgp);
-          // with MOEBLAZE_RECOMPUTE_H: the row's gate for the dW3 stage, which
-          // recomputes Hg = g SiLU(A) B from the saved A and B (0 on padding
-          // rows); once per row
-          if (p.rowg && t.n0 == 0) p.rowg[q] = valid ? g : 0.f;
         }
       } else {
         // weight gradients: rows of dW_e, plain bf16 stores
@@ -1298,6 +1303,13 @@ moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
   return MOEBLAZE_OK;
 }
 
+// MOEBLAZE_RECOMPUTE_H: the saved buffer is A | B (SwiGLU) | one fp32 gate per padded row
+float* saved_row_gates(const __nv_bfloat16* saved, const moeblaze_shape& s) {
+  const int64_t rows = max_padded_rows(s.L * s.K, s.E);
+  const int nb = s.act == MOEBLAZE_SWIGLU ? 2 : 1;
+  return reinterpret_cast<float*>(const_cast<__nv_bfloat16*>(saved) + (int64_t)nb * rows * s.h);
+}
+
 Params base_params(const moeblaze_shape& s, const moeblaze_dispatch& disp, const float* gates) {
   Params p;
   memset(&p, 0, sizeof(p));
@@ -1339,7 +1351,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
                            const __nv_bfloat16* W3, __nv_bfloat16* y, __nv_bfloat16* saved, __nv_bfloat16* wsH,
                            float* wsY32, cudaStream_t st) {
   const bool sw = s.act == MOEBLAZE_SWIGLU;
-  const bool rec = wsH == nullptr;  // MOEBLAZE_RECOMPUTE_H: no H temporary
+  const bool rec = wsH == nullptr;  // MOEBLAZE_RECOMPUTE_H: no H temporary; the row gates are kept in saved
   const int64_t LK = s.L * s.K;
   const int64_t rows = max_padded_rows(LK, s.E);
   const int64_t mt_bound = rows / BM;
@@ -1381,6 +1393,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.ksplit = p.kblocks;
       p.n_tiles = (s.d + 255) / 256;
       p.acc32 = wsY32;
+      p.rowg = rec ? saved_row_gates(saved, s) : nullptr;
       p.sched = sched + 1;
       const int64_t nt = mt_bound * p.n_tiles;
       const bool pair = pair_stage(p.kblocks, nt);
@@ -1397,85 +1410,33 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
 
 moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, const __nv_bfloat16* x,
                             const float* gates, const moeblaze_dispatch& disp, const __nv_bfloat16* W1,
-                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, const __nv_bfloat16* saved,
+                            const __nv_bfloat16* W2, const __nv_bfloat16* W3, __nv_bfloat16* saved,
                             __nv_bfloat16* dX, __nv_bfloat16* dW1, __nv_bfloat16* dW2, __nv_bfloat16* dW3,
-                            float* dgates, __nv_bfloat16* wsdAB, __nv_bfloat16* wsHg, float* wsRowg, float* wsdX32,
-                            cudaStream_t st) {
-  const bool rec = wsHg == nullptr;  // MOEBLAZE_RECOMPUTE_H: row gates instead of an Hg temporary
+                            float* dgates, __nv_bfloat16* wsHg, float* wsdX32, cudaStream_t st) {
+  // The saved A and B are read for the last time by the dH GEMM, which reads
+  // and writes the same (row, column) positions, so its dA and dB overwrite
+  // them in place and the dX and dW1|dW2 GEMMs read them from there.
+  // Default: dH also stores Hg (scratch) for the dW3 GEMM, which runs last.
+  // MOEBLAZE_RECOMPUTE_H (wsHg NULL): dW3 runs first, recomputing
+  // Hg = g SiLU(A) B from the saved A, B and the row gates the forward kept.
+  const bool rec = wsHg == nullptr;
   const bool sw = s.act == MOEBLAZE_SWIGLU;
-  const int nb = sw ? 2 : 1;
   const int64_t LK = s.L * s.K;
   const int64_t rows = max_padded_rows(LK, s.E);
   const int64_t mt_bound = rows / BM;
-  const __nv_bfloat16* A = saved;
-  const __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;
+  __nv_bfloat16* A = saved;                                  // A, then dA
+  __nv_bfloat16* B = sw ? saved + rows * s.h : nullptr;      // B, then dB
   // dX32 and, behind it, the tile counters of the four launches start at zero
   const size_t dx32_bytes = (sizeof(float) * s.L * s.d + 255) / 256 * 256;
   unsigned long long* sched = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(wsdX32) + dx32_bytes);
   MB_CUDA(cudaMemsetAsync(wsdX32, 0, dx32_bytes + kSchedBytes, st));
-  stage_event(0, st);
-  if (s.L > 0) {
-    {  // dH = dY W3^T with the SwiGLU backward epilogue
-      Params p = base_params(s, disp, gates);
-      p.gsrc = dY;
-      p.gld = s.d;
-      if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 128)) return MOEBLAZE_ERR_CUDA;
-      p.N = s.h;
-      p.kblocks = s.d / BK;
-      p.ksplit = p.kblocks;
-      p.n_tiles = (s.h + 255) / 256;
-      p.o0 = wsdAB; p.o1 = wsHg; p.i0 = A; p.i1 = B;
-      p.rowg = rec ? wsRowg : nullptr;
-      p.dg = dgates;
-      p.sched = sched + 0;
-      const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
-      if (!make_map(&p.tmO0, wsdAB, (uint64_t)nb * s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      if (!rec && !make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      p.ld0 = nb * s.h;
-      const int64_t nt = mt_bound * p.n_tiles;
-      const bool pair = pair_stage(p.kblocks, nt);
-      moeblaze_status r = sw ? (pair ? launch<DH_SWIGLU, true>(p, nt, st) : launch<DH_SWIGLU>(p, nt, st))
-                             : (pair ? launch<DH_SILU, true>(p, nt, st) : launch<DH_SILU>(p, nt, st));
-      if (r != MOEBLAZE_OK) return r;
-    }
-    stage_event(1, st);
-    {  // dX = dA W1^T + dB W2^T, reduced into dX32
-      Params p = base_params(s, disp, gates);
-      if (!make_map(&p.tmA, wsdAB, (uint64_t)nb * s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
-      if (!make_map(&p.tmB0, W1, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
-      if (sw && !make_map(&p.tmB1, W2, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
-      p.N = s.d;
-      p.kblocks = nb * s.h / BK;
-      p.ksplit = s.h / BK;
-      p.n_tiles = (s.d + 255) / 256;
-      p.acc32 = wsdX32;
-      p.sched = sched + 1;
-      const int64_t nt = mt_bound * p.n_tiles;
-      moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, true>(p, nt, st) : launch<DX>(p, nt, st);
-      if (r != MOEBLAZE_OK) return r;
-    }
-  }
-  stage_event(2, st);
-  {  // dW1 (and dW2) = X_e^T [dA | dB]
-    Params p = base_params(s, disp, gates);
-    p.gsrc = x;
-    p.gld = s.d;
-    if (!make_map(&p.tmB0, wsdAB, (uint64_t)nb * s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
-    p.N = s.h;
-    p.m_tiles_w = s.d / BM;
-    p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
-    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
-    p.o0 = dW1; p.o1 = dW2;
-    p.sched = sched + 2;
-    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
-    if (r != MOEBLAZE_OK) return r;
-  }
-  stage_event(3, st);
-  {  // dW3 = Hg^T dY, Hg stored by dH or recomputed from the saved tiles (Hg = g SiLU(A) B)
+  int ev = 0;
+  stage_event(ev++, st);
+  auto dw3 = [&]() -> moeblaze_status {  // dW3 = Hg^T dY
     Params p = base_params(s, disp, gates);
     if (!make_map(&p.tmA, rec ? A : wsHg, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
     if (rec && sw && !make_map(&p.tmX, B, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
-    p.rowg = rec ? wsRowg : nullptr;
+    p.rowg = rec ? saved_row_gates(saved, s) : nullptr;
     p.gsrc = dY;
     p.gld = s.d;
     p.N = s.d;
@@ -1486,11 +1447,75 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.sched = sched + 3;
     moeblaze_status r = !rec ? launch<DW3_H>(p, p.total_w, st)
                              : (sw ? launch<DW3_SWIGLU>(p, p.total_w, st) : launch<DW3_SILU>(p, p.total_w, st));
+    if (r == MOEBLAZE_OK) stage_event(ev++, st);
+    return r;
+  };
+  if (rec) {
+    moeblaze_status r = dw3();
     if (r != MOEBLAZE_OK) return r;
   }
-  stage_event(4, st);
+  {  // dH = dY W3^T with the SwiGLU backward epilogue; dA, dB over A, B
+    Params p = base_params(s, disp, gates);
+    p.gsrc = dY;
+    p.gld = s.d;
+    if (!make_map(&p.tmB0, W3, s.d, (uint64_t)s.E * s.h, 64, 128)) return MOEBLAZE_ERR_CUDA;
+    p.N = s.h;
+    p.kblocks = s.d / BK;
+    p.ksplit = p.kblocks;
+    p.n_tiles = (s.h + 255) / 256;
+    p.o1 = wsHg; p.i0 = A; p.i1 = B;
+    p.dg = dgates;
+    p.sched = sched + 0;
+    const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+    if (sw && !make_map(&p.tmO2, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+    if (!rec && !make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
+    const int64_t nt = mt_bound * p.n_tiles;
+    const bool pair = pair_stage(p.kblocks, nt);
+    moeblaze_status r = sw ? (pair ? launch<DH_SWIGLU, true>(p, nt, st) : launch<DH_SWIGLU>(p, nt, st))
+                           : (pair ? launch<DH_SILU, true>(p, nt, st) : launch<DH_SILU>(p, nt, st));
+    if (r != MOEBLAZE_OK) return r;
+  }
+  stage_event(ev++, st);
+  {  // dX = dA W1^T + dB W2^T, reduced into dX32
+    Params p = base_params(s, disp, gates);
+    if (!make_map(&p.tmA, A, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+    if (sw && !make_map(&p.tmX, B, s.h, rows, 64, 128)) return MOEBLAZE_ERR_CUDA;
+    if (!make_map(&p.tmB0, W1, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
+    if (sw && !make_map(&p.tmB1, W2, s.h, (uint64_t)s.E * s.d, 64, 128)) return MOEBLAZE_ERR_CUDA;
+    p.N = s.d;
+    p.kblocks = (sw ? 2 : 1) * s.h / BK;
+    p.ksplit = s.h / BK;
+    p.n_tiles = (s.d + 255) / 256;
+    p.acc32 = wsdX32;
+    p.sched = sched + 1;
+    const int64_t nt = mt_bound * p.n_tiles;
+    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, true>(p, nt, st) : launch<DX>(p, nt, st);
+    if (r != MOEBLAZE_OK) return r;
+  }
+  stage_event(ev++, st);
+  {  // dW1 (and dW2) = X_e^T [dA | dB]
+    Params p = base_params(s, disp, gates);
+    p.gsrc = x;
+    p.gld = s.d;
+    if (!make_map(&p.tmB0, A, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    if (sw && !make_map(&p.tmB1, B, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
+    p.N = s.h;
+    p.m_tiles_w = s.d / BM;
+    p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
+    p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
+    p.o0 = dW1; p.o1 = dW2;
+    p.sched = sched + 2;
+    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
+    if (r != MOEBLAZE_OK) return r;
+  }
+  stage_event(ev++, st);
+  if (!rec) {
+    moeblaze_status r = dw3();
+    if (r != MOEBLAZE_OK) return r;
+  }
   moeblaze_status r = convert(wsdX32, dX, s.L * s.d, st);
-  stage_event(5, st);
+  stage_event(ev++, st);
   return r;
 }
 

@@ -47,19 +47,27 @@ def check_dispatch(layer: MoELayer, ids_cpu: torch.Tensor, E: int):
     return D1, D2, D3, D4
 
 
-def run_layer(cfg, inp_dev, recompute_h=False) -> MoELayer:
+def run_layer(cfg, inp_dev, recompute_h=False, keep_saved=False):
+    """One step; with keep_saved also a copy of the saved A (B) taken after
+    the forward (the bf16 backward overwrites them with dA, dB)."""
     layer = MoELayer.for_config(cfg, "cuda", recompute_h=recompute_h)
-    layer.step(inp_dev)
+    W = (inp_dev.get("W1"), inp_dev.get("W2"), inp_dev.get("W3"))
+    layer.dispatch(inp_dev["ids"])
+    layer.forward(inp_dev["x"], inp_dev["gates"], *W)
+    saved = None
+    if keep_saved:
+        saved = tuple(None if v is None else v.clone() for v in layer.saved())
+    layer.backward(inp_dev["dY"], inp_dev["x"], inp_dev["gates"], *W)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
-    return layer
+    return (layer, saved) if keep_saved else layer
 
 
 def full_compare(cfg, inp_cpu, tol=None, check_saved=True, recompute_h=False):
     """Whole-tensor comparison of every output with the oracle."""
     tol = TOL[cfg.dtype] if tol is None else tol
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
-    layer = run_layer(cfg, dev, recompute_h)
+    layer, saved = run_layer(cfg, dev, recompute_h, keep_saved=True)
     D1, D2, D3, D4 = check_dispatch(layer, inp_cpu["ids"], cfg.E)
     a = inp_cpu
     y, keep = O.forward(a["ids"], a["gates"], a["x"], a["W1"], a["W2"], a["W3"], cfg.act, E=cfg.E, keep=True)
@@ -72,7 +80,7 @@ def full_compare(cfg, inp_cpu, tol=None, check_saved=True, recompute_h=False):
         if cfg.act == "swiglu":
             errs["dW2"] = O.rel_err(layer.dW2, dW2)
         if check_saved:
-            A, Bv = layer.saved()
+            A, Bv = saved
             _, _, pad, _ = layer.meta()
             ra, rb = [], []
             ga, gb = [], []

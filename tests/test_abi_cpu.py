@@ -173,19 +173,19 @@ def test_dispatch_meta_check_compares_the_recorded_shape():
 
 def test_recompute_flag_sizes_and_validation():
     """MOEBLAZE_RECOMPUTE_H drops H (padded_rows x h) from the forward
-    scratch and swaps Hg for one fp32 gate per padded row in the backward
-    scratch of the bf16 expert layers; fp32 and identity layers ignore it;
-    unknown flag bits are refused."""
+    scratch and Hg from the backward scratch of the bf16 expert layers, and
+    keeps one fp32 gate per padded row in the saved buffer instead; fp32 and
+    identity layers ignore it; unknown flag bits are refused."""
     _lib()
     for act in ("swiglu", "silu"):
         a = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act)
         r = B.make_shape(70000, 256, 384, 16, 2, B.BF16, act, B.RECOMPUTE_H)
         rows = -(-(70000 * 2 + 255 * 16) // 256) * 256
+        assert rows == B.padded_rows(a)
         h_bytes = -(-(rows * 384 * 2) // 256) * 256
-        g_bytes = -(-(rows * 4) // 256) * 256
         assert B.moeblaze_forward_workspace_bytes(a) - B.moeblaze_forward_workspace_bytes(r) == h_bytes
-        assert B.moeblaze_backward_workspace_bytes(a) - B.moeblaze_backward_workspace_bytes(r) == h_bytes - g_bytes
-        assert B.moeblaze_saved_bytes(a) == B.moeblaze_saved_bytes(r)
+        assert B.moeblaze_backward_workspace_bytes(a) - B.moeblaze_backward_workspace_bytes(r) == h_bytes
+        assert B.moeblaze_saved_bytes(r) - B.moeblaze_saved_bytes(a) == rows * 4
     for dt, act in ((B.F32, "swiglu"), (B.BF16, "identity")):
         a = B.make_shape(700, 64, 128, 8, 2, dt, act)
         r = B.make_shape(700, 64, 128, 8, 2, dt, act, B.RECOMPUTE_H)
@@ -194,3 +194,17 @@ def test_recompute_flag_sizes_and_validation():
     bad = B.make_shape(700, 128, 128, 8, 2, B.BF16, "swiglu", 2)
     assert B.moeblaze_saved_bytes(bad) == 0
     assert B.moeblaze_dispatch_build(bad, FAKE, _disp(), FAKE, 1 << 30, 0, None) == B.ERR_INVALID_ARG
+
+
+def test_bf16_backward_scratch_has_no_gradient_buffer():
+    """The bf16 backward writes dA and dB over the saved A and B: its scratch
+    is Hg (rows x h) and the fp32 dX accumulator (L x d) plus 256 bytes of
+    tile counters; the fp32 layer keeps its own dA|dB buffer."""
+    _lib()
+    L, d, h, E, K = 5000, 256, 384, 8, 2
+    s = B.make_shape(L, d, h, E, K, B.BF16, "swiglu")
+    rows = B.padded_rows(s)
+    up = lambda n: -(-n // 256) * 256
+    assert B.moeblaze_backward_workspace_bytes(s) == up(rows * h * 2) + up(L * d * 4) + 256
+    f = B.make_shape(L, d, h, E, K, B.F32, "swiglu")
+    assert B.moeblaze_backward_workspace_bytes(f) == up(rows * 2 * h * 4) + up(rows * h * 4)
