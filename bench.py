@@ -109,10 +109,21 @@ def dispatch_bytes(cfg):
     """Algorithmic bytes of the dispatch build (the per-token figure of the
     method's dispatch): ids read (4LK), D1, D3, D4 written (12LK), the
     offsets, and the bit-packed L x E bitmap written once and read twice
-    (3LE/8; these kernels fuse the count into the bitmap pass and read it
-    once, so they move LE/8 fewer)."""
+    (3LE/8).  These kernels keep each chunk's bitmap on chip, so they move
+    none of the bitmap bytes; dispatch_kernel_bytes counts what they move."""
     LK = cfg.L * cfg.K
     return 4 * LK + 12 * LK + 4 * (cfg.E + 1) + 3 * (cfg.L * cfg.E // 8)
+
+
+def dispatch_kernel_bytes(cfg):
+    """Bytes the three dispatch kernels read and write: the ids (4LK), D3
+    (4LK) and the packed (in-chunk rank, expert) slots (4LK) in K1; those
+    slots again (4LK), D1 and D4 (8LK) in K3; and the per-(expert, chunk)
+    counts: written, scanned in place (large layers) and read per chunk with
+    the expert totals (about 16 E C)."""
+    LK = cfg.L * cfg.K
+    C = (cfg.L + 1023) // 1024
+    return 24 * LK + 16 * cfg.E * C + 4 * (cfg.E + 1)
 
 
 def materialising_bytes(cfg):
@@ -553,9 +564,11 @@ def run_routing_stress(cfg, dev, warmup, iters, pk, src, flush, combine=True):
     per_build = (B.moeblaze_kernel_launches() - n0) / (warmup + iters)
     assert B.device_error(shape, disp) == 0
     nb = dispatch_bytes(cfg)
+    kb = dispatch_kernel_bytes(cfg)
     ach = nb / (ms * 1e-3) / 1e9
     out = {"dispatch_build": {
         "workload": cfg.name, "ms": ms, "algorithmic_bytes": nb, "GB_per_s": ach, "launches_per_build": per_build,
+        "kernel_bytes": kb, "kernel_GB_per_s": kb / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / pk["hbm_gbs"], "peak_source": src}}}
     if combine:
@@ -676,10 +689,12 @@ def run_dispatch_only(args, local_rank):
     ms = time_calls(lambda: B.dispatch_build(shape, ids, disp), flush, args.warmup, args.steps)
     assert B.device_error(shape, disp) == 0
     nb = dispatch_bytes(cfg)
+    kb = dispatch_kernel_bytes(cfg)
     pk, src = peaks()
     ach = nb / (ms * 1e-3) / 1e9
     return {"metric": "dispatch build HBM GB/s", "config": {"workload": cfg.name, "L": cfg.L, "E": cfg.E, "K": cfg.K},
-            "ms": ms, "algorithmic_bytes": nb, "steps": args.steps, "warmup": args.warmup,
+            "ms": ms, "algorithmic_bytes": nb, "kernel_bytes": kb, "kernel_GB_per_s": kb / (ms * 1e-3) / 1e9,
+            "steps": args.steps, "warmup": args.warmup,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / pk["hbm_gbs"], "peak_source": src}}
 

@@ -130,11 +130,14 @@ MOEBLAZE_API size_t moeblaze_backward_workspace_bytes(const moeblaze_shape* s);
  * Atomic-free three-step dispatch build (MoEBlaze, awesome-system-papers
  * page, section "Atomic-free 三步 dispatch 构建"):
  *   1. a dense token-expert bitmap (bit-packed, one 32-bit word per expert
- *      per 32 tokens), each (token, expert) bit written once;
- *   2. per-expert counts by population count and warp reduction, prefix
- *      sums into expert_token_offsets;
- *   3. a tile scan of the bitmap giving each (token, slot) its final
- *      position, then parallel writes of the three (L,K)-sized maps.
+ *      per 32 tokens), each (token, expert) bit written once; it is built
+ *      per chunk of 1024 tokens in on-chip memory and never stored to HBM;
+ *   2. per-(expert, chunk) counts by population count, and from the same
+ *      bitmap the in-chunk rank of every (token, slot) (set bits before it
+ *      in its expert's row); prefix sums over chunks and experts into
+ *      expert_token_offsets;
+ *   3. each (token, slot)'s final position = expert offset + chunk base +
+ *      in-chunk rank, then parallel writes of the three (L,K)-sized maps.
  * topk_ids: device int32 (L,K) row-major, the router's top-K expert ids.
  * out: the five device buffers above.  ws: device scratch of
  * moeblaze_dispatch_workspace_bytes(s) bytes (contents on entry ignored).
@@ -157,12 +160,12 @@ MOEBLAZE_API moeblaze_status moeblaze_dispatch_build(const moeblaze_shape* s, co
  * fixed, fully claimed pool, or code on a path where a new device
  * allocation is not allowed.  It runs the same three-step build as
  * moeblaze_dispatch_build and writes the same outputs into `out`, but keeps
- * its scratch (the bitmap and the per-chunk counts) in a fixed array that
+ * its scratch (the in-chunk positions and the per-chunk counts) in a fixed array that
  * lives inside the library: MOEBLAZE_STATIC_SCRATCH_BYTES bytes on every GPU
  * that loads the library, held until the process exits.
  *   - A shape whose scratch would exceed MOEBLAZE_STATIC_SCRATCH_BYTES
  *     (moeblaze_dispatch_workspace_bytes(s) > the limit; roughly
- *     E * ceil(L / 1024) * 132 bytes) is rejected with
+ *     4 * L * K + 4 * E * ceil(L / 1024) bytes) is rejected with
  *     MOEBLAZE_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address on the
  *     current device (a one-time set-up per device); make that first call

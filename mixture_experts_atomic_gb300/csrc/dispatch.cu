@@ -7,24 +7,27 @@
 //                      [e][t/32]; every (t,e) bit written once: the lanes of a
 //                      warp with the same expert are found by bit-plane
 //                      ballots and only the lowest one writes, so no two
-//                      lanes touch one word), writes it transposed
-//                      (expert-major, each expert's 32 words = one 128-byte
-//                      line) and the per (expert, chunk) popcount.
+//                      lanes touch one word).  While the bitmap is on chip it
+//                      derives, per expert, the prefix of set bits before
+//                      every word (a shuffle scan over the expert's 32
+//                      popcounts), the per (expert, chunk) count, and the
+//                      in-chunk rank of every (token, slot):
+//                      wordprefix + popc(bits below).  It writes the counts
+//                      and the ranks (u16, token-major); the bitmap itself
+//                      never goes to HBM.
 //   K2 scan_kernel     one CTA per expert: the exclusive scan of its chunk
 //                      counts -> chunk bases and n_e.  Large layers only:
 //                      below chunks x experts = 32768 each K3 CTA sums the
 //                      counts it needs itself (one launch fewer).
-//   K3 scatter_kernel  one CTA per chunk.  expert_token_offsets from a block
-//                      scan of n_e; a shuffle scan over each expert's 32
-//                      popcounts gives every word its first position; each
-//                      token then places its K slots:
-//                      pos = off[e] + base[e][c] + wordprefix + popc(bits below).
-//                      Writes token_index_map and token_expert_indices
-//                      token-major (one vector per token) and
-//                      expert_token_indices[pos].  The CTAs also split the
-//                      GEMM metadata: padded row offsets, the tile -> expert
-//                      table, the experts' descending-load order and the
-//                      (L, E, K) the build was made for.
+//   K3 scatter_kernel  one CTA per chunk, streaming: expert_token_offsets
+//                      from a block scan of n_e; every (token, slot) gets
+//                      pos = off[e] + base[e][c] + rank.  Writes
+//                      token_index_map and token_expert_indices token-major
+//                      (one vector per token) and expert_token_indices[pos].
+//                      The CTAs also split the GEMM metadata: padded row
+//                      offsets, the tile -> expert table, the experts'
+//                      descending-load order and the (L, E, K) the build was
+//                      made for.
 //
 // No global atomics on the data path (the device error word is the only
 // atomic, and only for invalid routing).
@@ -41,18 +44,17 @@ namespace {
 // looked up per device with cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_scratch[MOEBLAZE_STATIC_SCRATCH_BYTES];
 
-// dispatch workspace: bitmap [E][C*32] u32 | cnt/base [E][C] i32
+// dispatch workspace: (in-chunk rank << 16 | expert) [L][K] i32 | cnt/base [E][C] i32
 struct DispatchWs {
-  uint32_t* bitmap;
+  int32_t* packed;
   int32_t* base;
 };
 
 DispatchWs carve(void* ws, const moeblaze_shape& s) {
-  int64_t C = num_chunks(s.L);
   DispatchWs w;
-  w.bitmap = reinterpret_cast<uint32_t*>(ws);
-  size_t bm = align_up((size_t)s.E * C * kChunkWords * sizeof(uint32_t), 256);
-  w.base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + bm);
+  w.packed = reinterpret_cast<int32_t*>(ws);
+  const size_t rb = align_up((size_t)s.L * s.K * sizeof(int32_t), 256);
+  w.base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + rb);
   return w;
 }
 
@@ -60,27 +62,79 @@ constexpr int kThreads = 256;                       // 8 warps; warp w owns word
 constexpr int kPasses = kChunkTokens / kThreads;    // tokens per thread (4)
 constexpr int kRow = kChunkWords + 1;               // padded shared row: conflict-free column walks
 
-// K1: one CTA per chunk of 1024 tokens.  All ids are loaded up front; the
-// chunk's bitmap is built in shared memory (word [e][w] holds the tokens
-// 32w..32w+31 of the chunk routed to e), stored expert-major, and the
-// per-(expert, chunk) popcounts are written expert-major for the scan.
+// The K int32 values of token t's row (-1 for slots past K or tokens past
+// L); KM >= K.  Rows are 4K bytes, so K = 4 and K = 2 rows are one vector.
+template <int KM>
+__device__ __forceinline__ void load_slots(const int32_t* __restrict__ src0, int64_t t, int64_t L, int K, int* v) {
+#pragma unroll
+  for (int k = 0; k < KM; ++k) v[k] = -1;
+  if (t >= L) return;
+  const int32_t* src = src0 + t * K;
+  if constexpr (KM == 4) {
+    if (K == 4) {
+      const int4 u = *reinterpret_cast<const int4*>(src);
+      v[0] = u.x, v[1] = u.y, v[2] = u.z, v[3] = u.w;
+      return;
+    }
+  }
+  if (K == 2) {
+    const int2 u = *reinterpret_cast<const int2*>(src);
+    v[0] = u.x, v[1] = u.y;
+  } else {
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      if (k < K) v[k] = src[k];
+  }
+}
+
+template <int KM>
+__device__ __forceinline__ void store_slots(int32_t* __restrict__ dst0, int64_t t, int K, const int* v) {
+  int32_t* dst = dst0 + t * K;
+  if constexpr (KM == 4) {
+    if (K == 4) {
+      *reinterpret_cast<int4*>(dst) = make_int4(v[0], v[1], v[2], v[3]);
+      return;
+    }
+  }
+  if (K == 2) {
+    *reinterpret_cast<int2*>(dst) = make_int2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      if (k < K) dst[k] = v[k];
+  }
+}
+
+// K1: one CTA per chunk of 1024 tokens.  All ids are loaded up front and
+// copied to token_expert_indices; the chunk's bitmap is built in shared
+// memory (word [e][w] holds the tokens 32w..32w+31 of the chunk routed to
+// e); the per-(expert, chunk) popcounts are written expert-major for the
+// scan, and every (token, slot) gets (in-chunk rank << 16 | expert),
+// token-major, for the scatter (-1 for an id out of [0, E)).
+template <int KM>
 __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
-                                                          uint32_t* __restrict__ bitmap, int32_t* __restrict__ cnt,
-                                                          int64_t C, int32_t* err) {
+                                                          int32_t* __restrict__ D3, int32_t* __restrict__ packed,
+                                                          int32_t* __restrict__ cnt, int64_t C, int32_t* err) {
   extern __shared__ uint32_t words[];  // [E][kRow]: a padded row keeps [e][w] and [e'][w] in different banks
+  uint16_t* wpre = reinterpret_cast<uint16_t*>(words + E * kRow);  // [E][kRow]: set bits before word w
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
-  const int64_t wpe = C * kChunkWords;
   const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest expert id
 
-  int e_k[kPasses][kMaxK];
+  int e_k[kPasses][KM];
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) load_slots<KM>(ids, chunk * kChunkTokens + (warp + 8 * j) * 32 + lane, L, K, e_k[j]);
+  // token_expert_indices is the ids as given
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
     const int64_t t = chunk * kChunkTokens + (warp + 8 * j) * 32 + lane;
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
+    if (t < L) store_slots<KM>(D3, t, K, e_k[j]);
   }
-  for (int i = tid; i < E * kRow; i += kThreads) words[i] = 0u;
+  {
+    const int nw = E * kRow;  // cleared 4 words at a time, then the 0-3 left over
+    for (int i = tid; i < nw / 4; i += kThreads) reinterpret_cast<uint4*>(words)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < (nw & 3)) words[(nw & ~3) + tid] = 0u;
+  }
   // A new build starts with a clean device error word; K3, which runs after
   // every K1 CTA has finished, records invalid routing in it.
   if (chunk == 0 && tid == 0) *err = 0;
@@ -88,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
 #pragma unroll
   for (int j = 0; j < kPasses; ++j)
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k)
+    for (int k = 0; k < KM; ++k)
       if (e_k[j][k] >= E) e_k[j][k] = -1;
   __syncthreads();
 
@@ -102,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   for (int j = 0; j < kPasses; ++j) {
     const int w = warp + 8 * j;
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
+    for (int k = 0; k < KM; ++k) {
       if (k >= K) break;  // K is the same for every lane
       const int e = e_k[j][k];
       unsigned grp = __ballot_sync(0xffffffffu, e >= 0);
@@ -117,24 +171,57 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   }
   __syncthreads();
 
-  // expert-major store, 4 words (16 bytes) per thread, and the per-(expert,
-  // chunk) popcount: the 8 threads of one expert are 8 consecutive lanes and
-  // add their counts with shuffles (counts stored [E][C] for the scan)
+  // Word prefixes and the per-(expert, chunk) count: thread i covers words
+  // 4g..4g+3 of expert i/8 (g = i%8); the 8 threads of an expert are
+  // consecutive lanes and scan their popcounts with shuffles (counts stored
+  // [E][C] for the scan)
   for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
     const int i = i0 + tid;
     const bool v = i < E * 8;
-    const int e = i >> 3, pc = i & 7;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    const int e = i >> 3, g = i & 7;
+    int c[4] = {0, 0, 0, 0};
     if (v) {
-      const uint32_t* src = words + e * kRow + pc * 4;
-      u = make_uint4(src[0], src[1], src[2], src[3]);
-      reinterpret_cast<uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc] = u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[q] = __popc(words[e * kRow + 4 * g + q]);
     }
-    int c = __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
-    c += __shfl_xor_sync(0xffffffffu, c, 1);
-    c += __shfl_xor_sync(0xffffffffu, c, 2);
-    c += __shfl_xor_sync(0xffffffffu, c, 4);
-    if (v && pc == 0) cnt[(int64_t)e * C + chunk] = c;
+    const int mine = c[0] + c[1] + c[2] + c[3];
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((lane & 7) >= o) incl += u;
+    }
+    if (v) {
+      int r = incl - mine;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wpre[e * kRow + 4 * g + q] = (uint16_t)r;
+        r += c[q];
+      }
+      if (g == 7) cnt[(int64_t)e * C + chunk] = incl;
+    }
+  }
+  __syncthreads();
+
+  // (in-chunk rank << 16 | expert) of every (token, slot): the rank counts
+  // the set bits of its expert before its own
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int w = warp + 8 * j;
+    const int64_t t = chunk * kChunkTokens + w * 32 + lane;
+    if (t >= L) continue;
+    int pk[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      const int e = e_k[j][k];
+      pk[k] = -1;
+      if (k < K && e >= 0) {
+        const uint32_t r = (uint32_t)wpre[e * kRow + w] + (uint32_t)__popc(words[e * kRow + w] & below);
+        pk[k] = (int)((r << 16) | (uint32_t)e);
+      }
+    }
+    store_slots<KM>(packed, t, K, pk);
   }
 }
 
@@ -185,43 +272,34 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
   if (threadIdx.x == 0) n_e[e] = total;
 }
 
-// K3: one CTA per chunk.  Every global read (the chunk's counts or bases,
-// bitmap words, ids) is issued first.  Each CTA then derives the expert
-// offsets itself: the per-expert totals n_e come from K2, or, for a small
-// layer without K2 (chunks x experts <= kInlineBaseCounts), from summing the
-// count array, which also gives this chunk's bases; a block scan of n_e gives
-// expert_token_offsets.  The word prefixes of every expert come from a
-// shuffle scan over its 32 words (4 per thread); each (token, slot) then gets
-// pos = off[e] + base[e][c] + wordprefix + popc(bits below).
-// token_expert_indices and token_index_map are written token-major, one
-// vector per token, and expert_token_indices[pos] = token.
-// The GEMM metadata that K2 used to need a launch of its own is split over
-// the CTAs here: a slice of the tile -> expert table (binary search in the
-// padded offsets), a slice of the experts' load ranks, and, in CTA 0,
-// expert_token_offsets, the padded offsets, the counts, the tile count and
-// the (L, E, K) the build was made for.
+// K3: one CTA per chunk, streaming.  Every global read (the chunk's counts
+// or bases, the packed (rank, expert) slots) is issued first.  Each CTA then
+// derives the expert offsets itself: the per-expert totals n_e come from K2,
+// or, for a small layer without K2 (chunks x experts <= kInlineBaseCounts),
+// from summing the count array, which also gives this chunk's bases; one
+// warp scans n_e (and the padded counts, in the same pass) into
+// expert_token_offsets and the padded offsets.  Each (token, slot) then gets
+// pos = off[e] + base[e][c] + rank; token_index_map is written token-major,
+// one vector per token, and expert_token_indices[pos] = token.
+// The GEMM metadata is split over the CTAs here: a slice of the tile ->
+// expert table (binary search in the padded offsets), a slice of the experts'
+// load ranks, and, in CTA 0, expert_token_offsets, the padded offsets, the
+// counts, the tile count and the (L, E, K) the build was made for.
 constexpr int kInlineBaseCounts = 32768;
 
-__global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ ids, int64_t L, int E, int K,
-                                                           const uint32_t* __restrict__ bitmap, int64_t C,
-                                                           const int32_t* __restrict__ cb, bool scanned,
+template <int KM>
+__global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int64_t L, int E, int K, const int32_t* __restrict__ packed,
+                                                           int64_t C, const int32_t* __restrict__ cb, bool scanned,
                                                            const int32_t* __restrict__ n_e_in,
                                                            int32_t* __restrict__ D1, int32_t* __restrict__ D2,
-                                                           int32_t* __restrict__ D3, int32_t* __restrict__ D4,
-                                                           MetaView meta, int64_t max_tiles) {
+                                                           int32_t* __restrict__ D4, MetaView meta, int64_t max_tiles) {
   extern __shared__ int32_t sm[];
-  uint32_t* words = reinterpret_cast<uint32_t*>(sm);         // [E][kRow]
-  int32_t* ebase = sm + E * kRow;                            // [E]: off[e] + base[e][chunk]
-  int32_t* off = ebase + E;                                  // [E+1]: expert_token_offsets
-  int32_t* poff = off + E + 1;                               // [E+1]: padded row offsets
-  int32_t* ne = poff + E + 1;                                // [E]: tokens per expert
-  int32_t* cbase = ne + E;                                   // [E]: this chunk's base in each expert
-  uint16_t* wpre = reinterpret_cast<uint16_t*>(cbase + E);   // [E][kRow]: set bits before word w
-  __shared__ int wsum[32];
-  __shared__ int total;
+  int32_t* off = sm;               // [E+1]: expert_token_offsets
+  int32_t* poff = off + E + 1;     // [E+1]: padded row offsets
+  int32_t* ne = poff + E + 1;      // [E]: tokens per expert
+  int32_t* cbase = ne + E;         // [E]: this chunk's base in each expert
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
-  const int64_t wpe = C * kChunkWords;
 
   // ---- all global reads first
   if (scanned) {
@@ -230,19 +308,9 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
       cbase[e] = cb[(int64_t)e * C + chunk];
     }
   }
-  int e_k[kPasses][kMaxK];
+  int p_k[kPasses][KM];
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) e_k[j][k] = (k < K && t < L) ? ids[t * K + k] : -1;
-  }
-  for (int i = tid; i < E * kChunkWords / 4; i += kThreads) {
-    const int e = i / (kChunkWords / 4), pc = i % (kChunkWords / 4);
-    const uint4 u = reinterpret_cast<const uint4*>(bitmap + (int64_t)e * wpe + chunk * kChunkWords)[pc];
-    uint32_t* dst = words + e * kRow + pc * 4;
-    dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
-  }
+  for (int j = 0; j < kPasses; ++j) load_slots<KM>(packed, chunk * kChunkTokens + tid + kThreads * j, L, K, p_k[j]);
   if (!scanned) {
     // small layer: a warp per expert sums its chunk counts, before this
     // chunk (the base) and over all chunks (n_e)
@@ -264,124 +332,83 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
       }
     }
   }
+  // routing checks while the loads land: every slot of a token in [0, E)
+  // (K1 marks the others -1) and pairwise distinct
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
+    if (t >= L) continue;
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k >= K) break;
+      const int e = p_k[j][k] & 0xffff;
+      if (p_k[j][k] < 0) bad = true;
+#pragma unroll
+      for (int i = 0; i < k; ++i)
+        if (p_k[j][i] >= 0 && e == (p_k[j][i] & 0xffff)) bad = true;
+    }
+  }
   __syncthreads();
 
-  // ---- expert offsets (exclusive scan of n_e) and padded offsets
-  {
-    constexpr int kEPT = kMaxE / kThreads;
-    int carry = 0, pcarry = 0;
-#pragma unroll
-    for (int q = 0; q < kEPT; ++q) {
-      const int e = tid + q * kThreads;
-      const int n = e < E ? ne[e] : 0;
-      const int pn = (n + kRowPad - 1) / kRowPad * kRowPad;
-      const int pre = block_excl_scan(n, wsum, &total);
-      const int tot = total;
-      const int ppre = block_excl_scan(pn, wsum, &total);
+  // ---- expert offsets (exclusive scan of n_e) and padded offsets: warp 0,
+  // lane l owning experts [l*per, (l+1)*per), the two counts packed in one
+  // 64-bit word (neither half's running sum reaches 2^32)
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    unsigned long long mine = 0ull;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
       if (e < E) {
-        off[e] = carry + pre;
-        poff[e] = pcarry + ppre;
-      }
-      carry += tot;
-      pcarry += total;
-    }
-    if (tid == 0) {
-      off[E] = carry;
-      poff[E] = pcarry;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kThreads) ebase[e] = off[e] + cbase[e];
-
-  // ---- word prefixes: thread i covers words 4g..4g+3 of expert i/8 (g = i%8);
-  // the 8 threads of an expert are consecutive lanes and scan their counts
-  // with shuffles
-  for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
-    const int i = i0 + tid;
-    const bool v = i < E * 8;
-    const int e = i >> 3, g = i & 7;
-    int c[4] = {0, 0, 0, 0};
-    if (v) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = __popc(words[e * kRow + 4 * g + q]);
-    }
-    const int mine = c[0] + c[1] + c[2] + c[3];
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if ((lane & 7) >= o) incl += u;
-    }
-    if (v) {
-      int r = incl - mine;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        wpre[e * kRow + 4 * g + q] = (uint16_t)r;
-        r += c[q];
+        const unsigned n = (unsigned)ne[e];
+        mine += ((unsigned long long)((n + kRowPad - 1) / kRowPad * kRowPad) << 32) | n;
       }
     }
-  }
-  __syncthreads();
-
-  // ---- routing checks: ids in range, pairwise distinct per token (K*(K-1)/2
-  // compares); one atomic per CTA, and only for invalid routing
-  {
-    bool bad = false;
+    unsigned long long incl = mine;
 #pragma unroll
-    for (int j = 0; j < kPasses; ++j) {
-      const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
-      if (t >= L) continue;
-#pragma unroll
-      for (int k = 0; k < kMaxK; ++k) {
-        if (k >= K) break;
-        const int e = e_k[j][k];
-        if (e < 0 || e >= E) bad = true;
-#pragma unroll
-        for (int i = 0; i < k; ++i)
-          if (e == e_k[j][i]) bad = true;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    unsigned long long run = incl - mine;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        off[e] = (int32_t)(run & 0xffffffffull);
+        poff[e] = (int32_t)(run >> 32);
+        const unsigned n = (unsigned)ne[e];
+        run += ((unsigned long long)((n + kRowPad - 1) / kRowPad * kRowPad) << 32) | n;
       }
     }
-    if (__syncthreads_or(bad) && tid == 0) atomicOr(meta.err, kErrBadRouting);
+    if (lane == 31) {
+      off[E] = (int32_t)(incl & 0xffffffffull);
+      poff[E] = (int32_t)(incl >> 32);
+    }
   }
+  // one atomic per CTA, and only for invalid routing; the barrier also
+  // publishes the offsets
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(meta.err, kErrBadRouting);
 
   // ---- place every (token, slot)
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
-    const int tl = tid + kThreads * j;
-    const int64_t t = chunk * kChunkTokens + tl;
+    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
     if (t >= L) continue;
-    const int w = tl >> 5, b = tl & 31;
-    const uint32_t below = (1u << b) - 1u;
-    int d3[kMaxK], d4[kMaxK];
+    int d4[KM];
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-      d3[k] = e_k[j][k];
+    for (int k = 0; k < KM; ++k) {
       d4[k] = -1;
-      if (k < K) {
-        const int e = e_k[j][k];
-        if (e >= 0 && e < E) {
-          const int pos = ebase[e] + wpre[e * kRow + w] + __popc(words[e * kRow + w] & below);
+      if (k < K && p_k[j][k] >= 0) {
+        const int e = p_k[j][k] & 0xffff;
+        if (e < E) {
+          const int pos = off[e] + cbase[e] + (p_k[j][k] >> 16);
           D1[pos] = (int32_t)t;
           d4[k] = pos;
         }
       }
     }
-    int32_t* o3 = D3 + t * K;
-    int32_t* o4 = D4 + t * K;
-    if (K == 4) {
-      *reinterpret_cast<int4*>(o3) = make_int4(d3[0], d3[1], d3[2], d3[3]);
-      *reinterpret_cast<int4*>(o4) = make_int4(d4[0], d4[1], d4[2], d4[3]);
-    } else if (K == 2) {
-      *reinterpret_cast<int2*>(o3) = make_int2(d3[0], d3[1]);
-      *reinterpret_cast<int2*>(o4) = make_int2(d4[0], d4[1]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < kMaxK; ++k)
-        if (k < K) {
-          o3[k] = d3[k];
-          o4[k] = d4[k];
-        }
-    }
+    store_slots<KM>(D4, t, K, d4);
   }
 
   // ---- GEMM metadata, split over the CTAs
@@ -437,6 +464,40 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
 
 }  // namespace
 
+namespace {
+
+// K1, K2 (large layers) and K3 for ids of at most KM slots per token.
+template <int KM>
+moeblaze_status run_build(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
+                          const DispatchWs& w, const MetaView& meta, int64_t C, int64_t mt, cudaStream_t st) {
+  const int E = s.E, K = s.K;
+  const int64_t L = s.L;
+  const size_t sm1 = (size_t)E * kRow * (sizeof(uint32_t) + sizeof(uint16_t));
+  if (sm1 > 48 * 1024)
+    MB_CUDA(cudaFuncSetAttribute(bitmap_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
+  bitmap_kernel<KM><<<(unsigned)C, kThreads, sm1, st>>>(ids, L, E, K, out.token_expert_indices, w.packed, w.base, C,
+                                                        meta.err);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  // Large layers scan each expert's chunk counts in K2 (one CTA per expert);
+  // small ones let every K3 CTA sum the counts it needs.
+  const bool scanned = C * E > kInlineBaseCounts;
+  if (scanned) {
+    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
+    MB_CUDA(cudaGetLastError());
+    count_launch();
+  }
+  const size_t sm3 = (size_t)(4 * E + 2) * sizeof(int32_t);
+  scatter_kernel<KM><<<(unsigned)C, kThreads, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
+                                                          out.expert_token_indices, out.expert_token_offsets,
+                                                          out.token_index_map, meta, mt);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  return MOEBLAZE_OK;
+}
+
+}  // namespace
+
 moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
                                        cudaStream_t st) {
   constexpr int kMaxDev = 64;
@@ -460,9 +521,8 @@ moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* i
 }
 
 size_t dispatch_ws_bytes(const moeblaze_shape& s) {
-  int64_t C = num_chunks(s.L);
-  return align_up((size_t)s.E * C * kChunkWords * sizeof(uint32_t), 256) +
-         align_up((size_t)C * s.E * sizeof(int32_t), 256) + 256;
+  const int64_t C = num_chunks(s.L);
+  return align_up((size_t)s.L * s.K * sizeof(int32_t), 256) + align_up((size_t)C * s.E * sizeof(int32_t), 256) + 256;
 }
 
 moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
@@ -485,27 +545,9 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
     return MOEBLAZE_OK;
   }
   DispatchWs w = carve(ws, s);
-  const size_t sm1 = (size_t)E * kRow * sizeof(uint32_t);
-  if (sm1 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
-  bitmap_kernel<<<(unsigned)C, kThreads, sm1, st>>>(ids, L, E, K, w.bitmap, w.base, C, meta.err);
-  MB_CUDA(cudaGetLastError());
-  count_launch();
-  // Large layers scan each expert's chunk counts in K2 (one CTA per expert);
-  // small ones let every K3 CTA sum the counts it needs.
-  const bool scanned = C * E > kInlineBaseCounts;
-  if (scanned) {
-    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
-    MB_CUDA(cudaGetLastError());
-    count_launch();
-  }
-  const size_t sm3 = (size_t)E * kRow * 4 + (size_t)(5 * E + 2) * sizeof(int32_t) + (size_t)E * kRow * 2;
-  if (sm3 > 48 * 1024) MB_CUDA(cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<<<(unsigned)C, kThreads, sm3, st>>>(ids, L, E, K, w.bitmap, C, w.base, scanned, meta.n_e,
-                                                      out.expert_token_indices, out.expert_token_offsets,
-                                                      out.token_expert_indices, out.token_index_map, meta, mt);
-  MB_CUDA(cudaGetLastError());
-  count_launch();
-  return MOEBLAZE_OK;
+  if (K <= 2) return run_build<2>(s, ids, out, w, meta, C, mt, st);
+  if (K <= 4) return run_build<4>(s, ids, out, w, meta, C, mt, st);
+  return run_build<kMaxK>(s, ids, out, w, meta, C, mt, st);
 }
 
 }  // namespace moeblaze

@@ -20,7 +20,7 @@ from mixture_experts_atomic_gb300 import inputs as I
 
 def test_static_scratch_limit_is_checked_on_the_host():
     B.lib()
-    # the 2M-token, 256-expert dispatch needs ~69 MB of scratch: over the limit
+    # the 2M-token, 256-expert dispatch needs ~36 MB of scratch: over the limit
     big = B.make_shape(2097152, 128, 0, 256, 4, B.BF16, "identity")
     assert B.moeblaze_dispatch_workspace_bytes(big) > B.STATIC_SCRATCH_BYTES
     fake = 0x100000
