@@ -284,6 +284,33 @@ MOEBLAZE_API moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, c
                                                       const float* dgates, float* dWr, float* dbias, void* dx,
                                                       void* ws, size_t ws_bytes, moeblaze_stream stream);
 
+/* The router fused with the first step of the dispatch build (MoEBlaze,
+ * awesome-system-papers page: the token-choice top-K routing ahead of the
+ * section "Atomic-free 三步 dispatch 构建").  One call gives what
+ * moeblaze_router_forward followed by moeblaze_dispatch_build on its ids
+ * gives: topk_ids and gates as moeblaze_router_forward writes them, and
+ * `out` as moeblaze_dispatch_build writes it.
+ *   - bf16 x and E <= 64: one kernel computes the logits on the tensor cores
+ *     (Wr split into three bf16 parts, hi + mid + lo, whose products with x
+ *     are exact and summed in fp32: the logits carry fp32 precision, though
+ *     not the same rounding as moeblaze_router_forward's, so near-equal
+ *     logits may be ordered differently), selects the top K, and builds the
+ *     dispatch bitmap of each 1024-token chunk in on-chip memory while the
+ *     ids are still in registers; the rest of the dispatch build follows.
+ *     The ids are not read back from HBM for the bitmap.
+ *   - any other router shape (fp32 x, E > 64): moeblaze_router_forward, then
+ *     moeblaze_dispatch_build's kernels, in the same call.
+ * Shape: as for moeblaze_dispatch_build and moeblaze_router_forward (both
+ * sets of limits apply).  Arguments as for those two calls; ws: device
+ * scratch of moeblaze_router_dispatch_workspace_bytes(s) bytes (contents on
+ * entry ignored; 0 for an unsupported shape).  The ids it produces are
+ * always valid routing. */
+MOEBLAZE_API size_t moeblaze_router_dispatch_workspace_bytes(const moeblaze_shape* s);
+MOEBLAZE_API moeblaze_status moeblaze_router_dispatch_build(const moeblaze_shape* s, const void* x, const float* Wr,
+                                                            const float* bias, int32_t* topk_ids, float* gates,
+                                                            const moeblaze_dispatch* out, void* ws, size_t ws_bytes,
+                                                            moeblaze_stream stream);
+
 /* Synchronise `stream` and read the device error word of `disp->meta`:
  * *code = 0 when every kernel since the last dispatch_build on this meta
  * finished normally; otherwise a bitwise OR of 1 (bad routing), 2 (a

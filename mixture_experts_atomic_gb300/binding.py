@@ -31,6 +31,7 @@ EXPORTS = [
     "moeblaze_version", "moeblaze_set_stage_events", "moeblaze_kernel_launches",
     "moeblaze_dispatch_build_static", "moeblaze_dispatch_meta_check", "moeblaze_set_fault_injection",
     "moeblaze_router_forward", "moeblaze_router_backward", "moeblaze_router_backward_workspace_bytes",
+    "moeblaze_router_dispatch_workspace_bytes", "moeblaze_router_dispatch_build",
 ]
 
 # fixed scratch of moeblaze_dispatch_build_static (MOEBLAZE_STATIC_SCRATCH_BYTES)
@@ -88,6 +89,10 @@ def lib():
         L.moeblaze_router_backward_workspace_bytes.restype = sz
         L.moeblaze_router_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, sz, P]
         L.moeblaze_router_backward.restype = ctypes.c_int
+        L.moeblaze_router_dispatch_workspace_bytes.argtypes = [SP]
+        L.moeblaze_router_dispatch_workspace_bytes.restype = sz
+        L.moeblaze_router_dispatch_build.argtypes = [SP, P, P, P, P, P, DP, P, sz, P]
+        L.moeblaze_router_dispatch_build.restype = ctypes.c_int
         L.moeblaze_device_error.argtypes = [SP, DP, ctypes.POINTER(ctypes.c_int32), P]
         L.moeblaze_device_error.restype = ctypes.c_int
         L.moeblaze_dispatch_meta_check.argtypes = [SP, P]
@@ -164,6 +169,15 @@ def moeblaze_router_backward_workspace_bytes(shape: Shape) -> int:
 def moeblaze_router_backward(shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws, ws_bytes, stream) -> int:
     return lib().moeblaze_router_backward(ctypes.byref(shape), x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws,
                                           ws_bytes, stream)
+
+
+def moeblaze_router_dispatch_workspace_bytes(shape: Shape) -> int:
+    return lib().moeblaze_router_dispatch_workspace_bytes(ctypes.byref(shape))
+
+
+def moeblaze_router_dispatch_build(shape, x, Wr, bias, topk_ids, gates, disp, ws, ws_bytes, stream) -> int:
+    return lib().moeblaze_router_dispatch_build(ctypes.byref(shape), x, Wr, bias, topk_ids, gates, ctypes.byref(disp),
+                                                ws, ws_bytes, stream)
 
 
 def moeblaze_device_error(shape, disp, stream):
@@ -412,6 +426,31 @@ def router_forward(shape: Shape, x, Wr, bias, topk_ids, gates, stream=None):
           (gates, "gates", (shape.L, shape.K), torch.float32, False))
     st = moeblaze_router_forward(shape, _ptr(x), _ptr(Wr), _ptr(bias), _ptr(topk_ids), _ptr(gates), _stream(stream))
     _check(st, "moeblaze_router_forward")
+
+
+def router_dispatch_build(shape: Shape, x, Wr, bias, topk_ids, gates, bufs: Optional["DispatchBuffers"] = None,
+                          ws=None, stream=None) -> "DispatchBuffers":
+    """The router fused with the dispatch build's first step: fills topk_ids
+    (L,K) int32, gates (L,K) fp32 and the dispatch buffers in one call.  `ws`
+    is a device byte tensor of moeblaze_router_dispatch_workspace_bytes(shape)
+    bytes (allocated here when None)."""
+    _args((x, "x", (shape.L, shape.d), _TORCH_DTYPE[shape.dtype], False),
+          (Wr, "Wr", (shape.d, shape.E), torch.float32, False), (bias, "bias", (shape.E,), torch.float32, True),
+          (topk_ids, "topk_ids", (shape.L, shape.K), torch.int32, False),
+          (gates, "gates", (shape.L, shape.K), torch.float32, False))
+    if bufs is None:
+        bufs = alloc_dispatch(shape, Wr.device)
+    _check_dispatch_bufs(shape, bufs)
+    n = moeblaze_router_dispatch_workspace_bytes(shape)
+    if n == 0:
+        raise MoEBlazeError(ERR_UNSUPPORTED, "moeblaze_router_dispatch_workspace_bytes")
+    if ws is None:
+        ws = _bytes(n, Wr.device)
+    _bytes_arg(ws, "ws", n)
+    st = moeblaze_router_dispatch_build(shape, _ptr(x), _ptr(Wr), _ptr(bias), _ptr(topk_ids), _ptr(gates),
+                                        bufs.struct(), _ptr(ws), n, _stream(stream))
+    _check(st, "moeblaze_router_dispatch_build")
+    return bufs
 
 
 def router_backward(shape: Shape, x, Wr, topk_ids, gates, dgates, dWr, dbias, dx, ws=None, stream=None):

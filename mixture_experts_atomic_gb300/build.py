@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoeblaze.so")
-SOURCES = ["abi.cu", "dispatch.cu", "identity.cu", "simt.cu", "gemm_tc.cu", "router.cu"]
+SOURCES = ["abi.cu", "dispatch.cu", "identity.cu", "simt.cu", "gemm_tc.cu", "router.cu", "router_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -42,7 +42,7 @@ def _newer(src_files, target) -> bool:
 
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    headers = [os.path.join(SRC, "common.cuh"), os.path.join(ROOT, "include", "moeblaze.h")]
+    headers = [os.path.join(SRC, "common.cuh"), os.path.join(SRC, "tc_ptx.cuh"), os.path.join(ROOT, "include", "moeblaze.h")]
     objs = []
     jobs = []
     for s in SOURCES:

@@ -330,6 +330,31 @@ moeblaze_status moeblaze_router_forward(const moeblaze_shape* s, const void* x, 
   return launch_router_forward(*s, x, Wr, bias, topk_ids, gates, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t moeblaze_router_dispatch_workspace_bytes(const moeblaze_shape* s) {
+  if (check_shape(s) != MOEBLAZE_OK || check_router_shape(s) != MOEBLAZE_OK) return 0;
+  return router_dispatch_fused(*s) ? router_dispatch_ws_bytes(*s) : dispatch_ws_bytes(*s);
+}
+
+moeblaze_status moeblaze_router_dispatch_build(const moeblaze_shape* s, const void* x, const float* Wr,
+                                               const float* bias, int32_t* topk_ids, float* gates,
+                                               const moeblaze_dispatch* out, void* ws, size_t ws_bytes,
+                                               moeblaze_stream stream) {
+  moeblaze_status r = check_shape(s);
+  if (r != MOEBLAZE_OK) return r;
+  if ((r = check_router_shape(s)) != MOEBLAZE_OK) return r;
+  if ((r = check_dispatch(out)) != MOEBLAZE_OK) return r;
+  if (!ok_ptr4(Wr) || (bias && !ok_ptr4(bias))) return MOEBLAZE_ERR_INVALID_ARG;
+  if (s->L > 0 && (!ok_ptr(x) || !ok_ptr4(topk_ids) || !ok_ptr4(gates))) return MOEBLAZE_ERR_INVALID_ARG;
+  if (ws_bytes < moeblaze_router_dispatch_workspace_bytes(s)) return MOEBLAZE_ERR_WORKSPACE;
+  if (!ok_ptr(ws)) return MOEBLAZE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (router_dispatch_fused(*s)) return launch_router_dispatch(*s, x, Wr, bias, topk_ids, gates, *out, ws, st);
+  // shapes the fused kernel does not take (fp32 x, more than 64 experts, no
+  // tokens): the router, then the dispatch build on its ids
+  if (s->L > 0 && (r = launch_router_forward(*s, x, Wr, bias, topk_ids, gates, st)) != MOEBLAZE_OK) return r;
+  return launch_dispatch(*s, topk_ids, *out, ws, st);
+}
+
 moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, const void* x, const float* Wr,
                                          const int32_t* topk_ids, const float* gates, const float* dgates,
                                          float* dWr, float* dbias, void* dx, void* ws, size_t ws_bytes,

@@ -97,6 +97,11 @@ size_t dispatch_ws_bytes(const moeblaze_shape& s);
 // the dispatch build on the library's fixed scratch array (see dispatch.cu)
 moeblaze_status launch_dispatch_static(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
                                        cudaStream_t st);
+// the dispatch scratch's packed (in-chunk rank << 16 | expert) slots [L][K]
+// and per-(expert, chunk) counts [E][C], for a kernel that does K1's work
+void dispatch_ws_parts(const moeblaze_shape& s, void* ws, int32_t** packed, int32_t** cnt);
+// K2 (large layers) and K3 on a scratch whose slots and counts are written
+moeblaze_status launch_dispatch_tail(const moeblaze_shape& s, const moeblaze_dispatch& out, void* ws, cudaStream_t st);
 
 // identity.cu
 moeblaze_status launch_identity_combine(const moeblaze_shape& s, const void* src, const moeblaze_dispatch& disp,
@@ -134,6 +139,13 @@ moeblaze_status launch_router_forward(const moeblaze_shape& s, const void* x, co
 moeblaze_status launch_router_backward(const moeblaze_shape& s, const void* x, const float* Wr, const int32_t* ids,
                                        const float* gates, const float* dgates, float* dWr, float* dbias, void* dx,
                                        void* ws, cudaStream_t st);
+
+// router_tc.cu: the router fused with the dispatch's first step (bf16 x, E <= 64)
+bool router_dispatch_fused(const moeblaze_shape& s);
+size_t router_dispatch_ws_bytes(const moeblaze_shape& s);
+moeblaze_status launch_router_dispatch(const moeblaze_shape& s, const void* x, const float* Wr, const float* bias,
+                                       int32_t* ids, float* gates, const moeblaze_dispatch& out, void* ws,
+                                       cudaStream_t st);
 
 // shared helpers (abi.cu)
 int sm_count();

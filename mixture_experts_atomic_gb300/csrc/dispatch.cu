@@ -20,10 +20,12 @@
 //                      below chunks x experts = 32768 each K3 CTA sums the
 //                      counts it needs itself (one launch fewer).
 //   K3 scatter_kernel  one CTA per chunk, streaming: expert_token_offsets
-//                      from a block scan of n_e; every (token, slot) gets
+//                      from a warp scan of n_e; every (token, slot) gets
 //                      pos = off[e] + base[e][c] + rank.  Writes
-//                      token_index_map and token_expert_indices token-major
-//                      (one vector per token) and expert_token_indices[pos].
+//                      token_index_map token-major (one vector per token);
+//                      the chunk's tokens are staged in shared memory in
+//                      expert_token_indices order, so each expert's run of
+//                      that array is written by consecutive threads.
 //                      The CTAs also split the GEMM metadata: padded row
 //                      offsets, the tile -> expert table, the experts'
 //                      descending-load order and the (L, E, K) the build was
@@ -61,6 +63,8 @@ DispatchWs carve(void* ws, const moeblaze_shape& s) {
 constexpr int kThreads = 256;                       // 8 warps; warp w owns words w, w+8, w+16, w+24
 constexpr int kPasses = kChunkTokens / kThreads;    // tokens per thread (4)
 constexpr int kRow = kChunkWords + 1;               // padded shared row: conflict-free column walks
+constexpr int kMaxIdBits = 9;                       // bits of an expert id below kMaxE
+static_assert(kMaxE <= (1 << kMaxIdBits), "expert ids must fit in kMaxIdBits bits");
 
 // The K int32 values of token t's row (-1 for slots past K or tokens past
 // L); KM >= K.  Rows are 4K bytes, so K = 4 and K = 2 rows are one vector.
@@ -160,10 +164,13 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
       if (k >= K) break;  // K is the same for every lane
       const int e = e_k[j][k];
       unsigned grp = __ballot_sync(0xffffffffu, e >= 0);
-      for (int b = 0; b < nbits; ++b) {
-        const bool bit = (e >> b) & 1;
-        const unsigned plane = __ballot_sync(0xffffffffu, bit);
-        grp &= bit ? plane : ~plane;
+      const unsigned ue = (unsigned)e;
+#pragma unroll
+      for (int b = 0; b < kMaxIdBits; ++b) {
+        if (b >= nbits) break;  // the same in every lane
+        const unsigned bit = (ue >> b) & 1u;
+        const unsigned plane = __ballot_sync(0xffffffffu, bit != 0u);
+        grp &= plane ^ (bit - 1u);  // the plane where the bit is set, its complement where it is not
       }
       if (e >= 0 && lane == __ffs(grp) - 1) words[e * kRow + w] |= grp;
       __syncwarp();
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
 constexpr int kInlineBaseCounts = 32768;
 
 template <int KM>
-__global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int64_t L, int E, int K, const int32_t* __restrict__ packed,
+__global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L, int E, int K, const int32_t* __restrict__ packed,
                                                            int64_t C, const int32_t* __restrict__ cb, bool scanned,
                                                            const int32_t* __restrict__ n_e_in,
                                                            int32_t* __restrict__ D1, int32_t* __restrict__ D2,
@@ -298,14 +305,23 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int6
   int32_t* poff = off + E + 1;     // [E+1]: padded row offsets
   int32_t* ne = poff + E + 1;      // [E]: tokens per expert
   int32_t* cbase = ne + E;         // [E]: this chunk's base in each expert
+  int32_t* ccnt = cbase + E;       // [E]: this chunk's tokens in each expert
+  int32_t* ebase = ccnt + E;       // [E]: off[e] + cbase[e], the expert's first position from this chunk
+  int32_t* delta = ebase + E;      // [E]: ebase[e] - (the expert's first entry in the chunk's staging)
+  int32_t* stage_t = delta + E;    // [kChunkTokens * KM]: the chunk's tokens in expert_token_indices order
+  uint16_t* stage_e = reinterpret_cast<uint16_t*>(stage_t + kChunkTokens * KM);  // their experts
+  __shared__ int nstage;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
 
   // ---- all global reads first
   if (scanned) {
     for (int e = tid; e < E; e += kThreads) {
-      ne[e] = n_e_in[e];
-      cbase[e] = cb[(int64_t)e * C + chunk];
+      const int n = n_e_in[e];
+      const int b = cb[(int64_t)e * C + chunk];
+      ne[e] = n;
+      cbase[e] = b;
+      ccnt[e] = (chunk + 1 < C ? cb[(int64_t)e * C + chunk + 1] : n) - b;
     }
   }
   int p_k[kPasses][KM];
@@ -315,20 +331,23 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int6
     // small layer: a warp per expert sums its chunk counts, before this
     // chunk (the base) and over all chunks (n_e)
     for (int e = warp; e < E; e += kThreads / 32) {
-      int before = 0, all = 0;
+      int before = 0, all = 0, mine = 0;
       for (int64_t c = lane; c < C; c += 32) {
         const int v = cb[(int64_t)e * C + c];
         all += v;
         if (c < chunk) before += v;
+        if (c == chunk) mine = v;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         before += __shfl_xor_sync(0xffffffffu, before, o);
         all += __shfl_xor_sync(0xffffffffu, all, o);
+        mine += __shfl_xor_sync(0xffffffffu, mine, o);
       }
       if (lane == 0) {
         cbase[e] = before;
         ne[e] = all;
+        ccnt[e] = mine;
       }
     }
   }
@@ -355,42 +374,59 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int6
   // lane l owning experts [l*per, (l+1)*per), the two counts packed in one
   // 64-bit word (neither half's running sum reaches 2^32)
   if (warp == 0) {
+    // ... and the chunk's own counts into its staging offsets
     const int per = (E + 31) / 32;
     const int e0 = lane * per;
     unsigned long long mine = 0ull;
+    int cmine = 0;
     for (int i = 0; i < per; ++i) {
       const int e = e0 + i;
       if (e < E) {
         const unsigned n = (unsigned)ne[e];
         mine += ((unsigned long long)((n + kRowPad - 1) / kRowPad * kRowPad) << 32) | n;
+        cmine += ccnt[e];
       }
     }
     unsigned long long incl = mine;
+    int cincl = cmine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
+      const int cu = __shfl_up_sync(0xffffffffu, cincl, o);
+      if (lane >= o) {
+        incl += u;
+        cincl += cu;
+      }
     }
     unsigned long long run = incl - mine;
+    int crun = cincl - cmine;
     for (int i = 0; i < per; ++i) {
       const int e = e0 + i;
       if (e < E) {
-        off[e] = (int32_t)(run & 0xffffffffull);
+        const int o0 = (int32_t)(run & 0xffffffffull);
+        off[e] = o0;
         poff[e] = (int32_t)(run >> 32);
+        ebase[e] = o0 + cbase[e];
+        delta[e] = o0 + cbase[e] - crun;
         const unsigned n = (unsigned)ne[e];
         run += ((unsigned long long)((n + kRowPad - 1) / kRowPad * kRowPad) << 32) | n;
+        crun += ccnt[e];
       }
     }
     if (lane == 31) {
       off[E] = (int32_t)(incl & 0xffffffffull);
       poff[E] = (int32_t)(incl >> 32);
+      nstage = cincl;
     }
   }
   // one atomic per CTA, and only for invalid routing; the barrier also
   // publishes the offsets
-  if (__syncthreads_or(bad) && tid == 0) atomicOr(meta.err, kErrBadRouting);
+  const bool any_bad = __syncthreads_or(bad) != 0;
+  if (any_bad && tid == 0) atomicOr(meta.err, kErrBadRouting);
 
-  // ---- place every (token, slot)
+  // ---- place every (token, slot): token_index_map directly, the token into
+  // the chunk's staging at its position minus delta[e] (the chunk's slots of
+  // one expert are consecutive there, as in expert_token_indices)
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
     const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
@@ -402,14 +438,24 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int6
       if (k < K && p_k[j][k] >= 0) {
         const int e = p_k[j][k] & 0xffff;
         if (e < E) {
-          const int pos = off[e] + cbase[e] + (p_k[j][k] >> 16);
-          D1[pos] = (int32_t)t;
+          const int pos = ebase[e] + (p_k[j][k] >> 16);
+          const int si = pos - delta[e];
+          stage_t[si] = (int32_t)t;
+          stage_e[si] = (uint16_t)e;
           d4[k] = pos;
         }
       }
     }
     store_slots<KM>(D4, t, K, d4);
   }
+  __syncthreads();
+  // expert_token_indices: the chunk's runs, one per expert, each contiguous
+  // in the output, written by consecutive threads.  A token with a repeated
+  // id leaves a staging entry unwritten, so a chunk with invalid routing
+  // skips this (its part of the output is unspecified; nothing is written
+  // outside the buffer).
+  if (!any_bad)
+    for (int j = tid; j < nstage; j += kThreads) D1[delta[stage_e[j]] + j] = stage_t[j];
 
   // ---- GEMM metadata, split over the CTAs
   // tile -> expert: tile m belongs to the expert whose padded rows hold row
@@ -466,7 +512,34 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 6 : 1) scatter_kernel(int6
 
 namespace {
 
-// K1, K2 (large layers) and K3 for ids of at most KM slots per token.
+// K2 (large layers) and K3 for ids of at most KM slots per token, once K1
+// (or the router kernel that does K1's work) has written the packed slots
+// and the per-(expert, chunk) counts.
+template <int KM>
+moeblaze_status run_tail(const moeblaze_shape& s, const moeblaze_dispatch& out, const DispatchWs& w,
+                         const MetaView& meta, int64_t C, int64_t mt, cudaStream_t st) {
+  const int E = s.E, K = s.K;
+  const int64_t L = s.L;
+  // Large layers scan each expert's chunk counts in K2 (one CTA per expert);
+  // small ones let every K3 CTA sum the counts it needs.
+  const bool scanned = C * E > kInlineBaseCounts;
+  if (scanned) {
+    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
+    MB_CUDA(cudaGetLastError());
+    count_launch();
+  }
+  const size_t sm3 = (size_t)(7 * E + 2) * sizeof(int32_t) + (size_t)kChunkTokens * KM * (sizeof(int32_t) + sizeof(uint16_t));
+  if (sm3 > 48 * 1024)
+    MB_CUDA(cudaFuncSetAttribute(scatter_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
+  scatter_kernel<KM><<<(unsigned)C, kThreads, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
+                                                          out.expert_token_indices, out.expert_token_offsets,
+                                                          out.token_index_map, meta, mt);
+  MB_CUDA(cudaGetLastError());
+  count_launch();
+  return MOEBLAZE_OK;
+}
+
+// K1, then the tail
 template <int KM>
 moeblaze_status run_build(const moeblaze_shape& s, const int32_t* ids, const moeblaze_dispatch& out,
                           const DispatchWs& w, const MetaView& meta, int64_t C, int64_t mt, cudaStream_t st) {
@@ -479,21 +552,7 @@ moeblaze_status run_build(const moeblaze_shape& s, const int32_t* ids, const moe
                                                         meta.err);
   MB_CUDA(cudaGetLastError());
   count_launch();
-  // Large layers scan each expert's chunk counts in K2 (one CTA per expert);
-  // small ones let every K3 CTA sum the counts it needs.
-  const bool scanned = C * E > kInlineBaseCounts;
-  if (scanned) {
-    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
-    MB_CUDA(cudaGetLastError());
-    count_launch();
-  }
-  const size_t sm3 = (size_t)(4 * E + 2) * sizeof(int32_t);
-  scatter_kernel<KM><<<(unsigned)C, kThreads, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
-                                                          out.expert_token_indices, out.expert_token_offsets,
-                                                          out.token_index_map, meta, mt);
-  MB_CUDA(cudaGetLastError());
-  count_launch();
-  return MOEBLAZE_OK;
+  return run_tail<KM>(s, out, w, meta, C, mt, st);
 }
 
 }  // namespace
@@ -548,6 +607,23 @@ moeblaze_status launch_dispatch(const moeblaze_shape& s, const int32_t* ids, con
   if (K <= 2) return run_build<2>(s, ids, out, w, meta, C, mt, st);
   if (K <= 4) return run_build<4>(s, ids, out, w, meta, C, mt, st);
   return run_build<kMaxK>(s, ids, out, w, meta, C, mt, st);
+}
+
+void dispatch_ws_parts(const moeblaze_shape& s, void* ws, int32_t** packed, int32_t** cnt) {
+  const DispatchWs w = carve(ws, s);
+  *packed = w.packed;
+  *cnt = w.base;
+}
+
+moeblaze_status launch_dispatch_tail(const moeblaze_shape& s, const moeblaze_dispatch& out, void* ws, cudaStream_t st) {
+  const int K = s.K;
+  const MetaView meta = meta_view(out.meta, s.E);
+  const int64_t C = num_chunks(s.L);
+  const int64_t mt = max_m_tiles(s.L * K, s.E);
+  const DispatchWs w = carve(ws, s);
+  if (K <= 2) return run_tail<2>(s, out, w, meta, C, mt, st);
+  if (K <= 4) return run_tail<4>(s, out, w, meta, C, mt, st);
+  return run_tail<kMaxK>(s, out, w, meta, C, mt, st);
 }
 
 }  // namespace moeblaze
