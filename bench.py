@@ -593,8 +593,9 @@ def fp32_alu_tflops(pk):
 
 def run_router(cfg, inp, dev, flush, pk, iters=10):
     """The workload's softmax router (the step before the dispatch) and its
-    backward, timed outside the layer step with CUDA events, L2 flushed
-    before each call.  Algorithmic bytes: forward x read, ids and gates
+    backward, and the router followed by the dispatch build (two calls, and
+    the fused call), timed outside the layer step with CUDA events, L2
+    flushed before each call.  Algorithmic bytes: forward x read, ids and gates
     written, Wr read; backward x read, dx written, ids/gates/dgates read, Wr
     read, dWr written.  FLOPs 2LdE (forward) and 4LdE (backward)."""
     from mixture_experts_atomic_gb300 import binding as B
@@ -606,11 +607,22 @@ def run_router(cfg, inp, dev, flush, pk, iters=10):
     dg = torch.randn(cfg.L, cfg.K, device=dev)
     dWr, db, dx = torch.empty_like(Wr), torch.empty(cfg.E, device=dev), torch.empty_like(x)
     ws = torch.empty(B.moeblaze_router_backward_workspace_bytes(sh), dtype=torch.uint8, device=dev)
+    disp = B.alloc_dispatch(sh, dev)
+    rd_ws = torch.empty(B.moeblaze_router_dispatch_workspace_bytes(sh), dtype=torch.uint8, device=dev)
     calls = {"forward": lambda: B.router_forward(sh, x, Wr, b, ids, gates),
-             "backward": lambda: B.router_backward(sh, x, Wr, ids, gates, dg, dWr, db, dx, ws)}
+             "backward": lambda: B.router_backward(sh, x, Wr, ids, gates, dg, dWr, db, dx, ws),
+             # the router and the dispatch build: two calls, and the fused call
+             "forward_then_dispatch": lambda: (B.router_forward(sh, x, Wr, b, ids, gates),
+                                               B.dispatch_build(sh, ids, disp)),
+             "fused_router_dispatch": lambda: B.router_dispatch_build(sh, x, Wr, b, ids, gates, disp, rd_ws)}
     s_x = cfg.L * cfg.d * cfg.elem_bytes
+    # router + dispatch: x read, ids and gates written, D1, D3, D4 written (the
+    # bytes the pair must move; the dispatch's bitmap is not counted)
+    rd = s_x + 8 * cfg.L * cfg.K + 4 * cfg.d * cfg.E + 12 * cfg.L * cfg.K
     work = {"forward": (s_x + 8 * cfg.L * cfg.K + 4 * cfg.d * cfg.E, 2 * cfg.L * cfg.d * cfg.E),
-            "backward": (2 * s_x + 12 * cfg.L * cfg.K + 8 * cfg.d * cfg.E, 4 * cfg.L * cfg.d * cfg.E)}
+            "backward": (2 * s_x + 12 * cfg.L * cfg.K + 8 * cfg.d * cfg.E, 4 * cfg.L * cfg.d * cfg.E),
+            "forward_then_dispatch": (rd, 2 * cfg.L * cfg.d * cfg.E),
+            "fused_router_dispatch": (rd, 2 * cfg.L * cfg.d * cfg.E)}
     alu = fp32_alu_tflops(pk)
     ridge = alu * 1e12 / (pk["hbm_gbs"] * 1e9)  # FLOP per byte where the two bounds meet
     out = {"fp32_alu_peak_tflops": alu}
@@ -632,6 +644,10 @@ def run_router(cfg, inp, dev, flush, pk, iters=10):
             ach = flops / (ms * 1e-3) / 1e12
             roof = {"bound": "alu", "achieved": ach, "peak": alu, "unit": "TFLOP/s", "frac": ach / alu}
         else:
+            ach = nbytes / (ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
+        if name == "fused_router_dispatch" and cfg.dtype == "bf16" and cfg.E <= 64 and cfg.L >= 128:
+            # the fused kernel (bf16 x, E <= 64, L >= 128) runs the logits on the tensor cores: its bound is HBM
             ach = nbytes / (ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
         out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "flops": flops, "roofline": roof}

@@ -290,7 +290,7 @@ MOEBLAZE_API moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, c
  * moeblaze_router_forward followed by moeblaze_dispatch_build on its ids
  * gives: topk_ids and gates as moeblaze_router_forward writes them, and
  * `out` as moeblaze_dispatch_build writes it.
- *   - bf16 x and E <= 64: one kernel computes the logits on the tensor cores
+ *   - bf16 x, E <= 64 and L >= 128: one kernel computes the logits on the tensor cores
  *     (Wr split into three bf16 parts, hi + mid + lo, whose products with x
  *     are exact and summed in fp32: the logits carry fp32 precision, though
  *     not the same rounding as moeblaze_router_forward's, so near-equal
@@ -298,7 +298,7 @@ MOEBLAZE_API moeblaze_status moeblaze_router_backward(const moeblaze_shape* s, c
  *     dispatch bitmap of each 1024-token chunk in on-chip memory while the
  *     ids are still in registers; the rest of the dispatch build follows.
  *     The ids are not read back from HBM for the bitmap.
- *   - any other router shape (fp32 x, E > 64): moeblaze_router_forward, then
+ *   - any other router shape (fp32 x, E > 64, L < 128): moeblaze_router_forward, then
  *     moeblaze_dispatch_build's kernels, in the same call.
  * Shape: as for moeblaze_dispatch_build and moeblaze_router_forward (both
  * sets of limits apply).  Arguments as for those two calls; ws: device

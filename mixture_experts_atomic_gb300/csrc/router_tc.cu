@@ -373,8 +373,10 @@ size_t router_dispatch_ws_bytes(const moeblaze_shape& s) {
   return dispatch_ws_bytes(s) + align_up((size_t)tc::rt_n(EP) * s.d * sizeof(__nv_bfloat16), 256);
 }
 
+// the fused kernel takes bf16 x, up to 64 experts and at least one full
+// 128-token tile (the x tile's TMA box)
 bool router_dispatch_fused(const moeblaze_shape& s) {
-  return s.dtype == MOEBLAZE_BF16 && s.E <= tc::kRtMaxEP && s.L > 0;
+  return s.dtype == MOEBLAZE_BF16 && s.E <= tc::kRtMaxEP && s.L >= tc::kRtTokens;
 }
 
 moeblaze_status launch_router_dispatch(const moeblaze_shape& s, const void* x, const float* Wr, const float* bias,
