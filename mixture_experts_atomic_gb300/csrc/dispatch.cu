@@ -20,7 +20,7 @@
 //                      below chunks x experts = 32768 each K3 CTA sums the
 //                      counts it needs itself (one launch fewer).
 //   K3 scatter_kernel  one CTA per chunk, streaming: expert_token_offsets
-//                      from a warp scan of n_e; every (token, slot) gets
+//                      from a block scan of n_e; every (token, slot) gets
 //                      pos = off[e] + base[e][c] + rank.  Writes
 //                      token_index_map token-major (one vector per token);
 //                      the chunk's tokens are staged in shared memory in
@@ -155,13 +155,16 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   // bit of the id, keeping the lanes whose bit agrees with its own (and a
   // first ballot dropping lanes with no valid id).  This is the mask
   // match_any would give, from ballots, which cost less to issue.  Only the
-  // group's lowest lane writes; distinct groups write distinct words.
+  // group's lowest lane writes; distinct groups write distinct words.  The
+  // kPasses token groups of one slot write different words, so they run
+  // without ordering between them; two slots may write the same word, so a
+  // warp barrier separates the slots.
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    const int w = warp + 8 * j;
+  for (int k = 0; k < KM; ++k) {
+    if (k >= K) break;  // K is the same for every lane
 #pragma unroll
-    for (int k = 0; k < KM; ++k) {
-      if (k >= K) break;  // K is the same for every lane
+    for (int j = 0; j < kPasses; ++j) {
+      const int w = warp + 8 * j;
       const int e = e_k[j][k];
       unsigned grp = __ballot_sync(0xffffffffu, e >= 0);
       const unsigned ue = (unsigned)e;
@@ -173,8 +176,8 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
         grp &= plane ^ (bit - 1u);  // the plane where the bit is set, its complement where it is not
       }
       if (e >= 0 && lane == __ffs(grp) - 1) words[e * kRow + w] |= grp;
-      __syncwarp();
     }
+    __syncwarp();
   }
   __syncthreads();
 
@@ -283,9 +286,10 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
 // or bases, the packed (rank, expert) slots) is issued first.  Each CTA then
 // derives the expert offsets itself: the per-expert totals n_e come from K2,
 // or, for a small layer without K2 (chunks x experts <= kInlineBaseCounts),
-// from summing the count array, which also gives this chunk's bases; one
-// warp scans n_e (and the padded counts, in the same pass) into
-// expert_token_offsets and the padded offsets.  Each (token, slot) then gets
+// from summing the count array, which also gives this chunk's bases; a block
+// scan of n_e (and of the padded counts and of this chunk's counts, in the
+// same pass) gives expert_token_offsets, the padded offsets and the chunk's
+// staging offsets.  Each (token, slot) then gets
 // pos = off[e] + base[e][c] + rank; token_index_map is written token-major,
 // one vector per token, and expert_token_indices[pos] = token.
 // The GEMM metadata is split over the CTAs here: a slice of the tile ->
@@ -293,9 +297,11 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cn
 // load ranks, and, in CTA 0, expert_token_offsets, the padded offsets, the
 // counts, the tile count and the (L, E, K) the build was made for.
 constexpr int kInlineBaseCounts = 32768;
+constexpr int kT3 = 256;                      // K3 threads: four tokens each
+constexpr int kP3 = kChunkTokens / kT3;
 
 template <int KM>
-__global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L, int E, int K, const int32_t* __restrict__ packed,
+__global__ void __launch_bounds__(kT3, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L, int E, int K, const int32_t* __restrict__ packed,
                                                            int64_t C, const int32_t* __restrict__ cb, bool scanned,
                                                            const int32_t* __restrict__ n_e_in,
                                                            int32_t* __restrict__ D1, int32_t* __restrict__ D2,
@@ -311,12 +317,14 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   int32_t* stage_t = delta + E;    // [kChunkTokens * KM]: the chunk's tokens in expert_token_indices order
   uint16_t* stage_e = reinterpret_cast<uint16_t*>(stage_t + kChunkTokens * KM);  // their experts
   __shared__ int nstage;
+  __shared__ unsigned long long wtot[kT3 / 32];
+  __shared__ int wctot[kT3 / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk = blockIdx.x;
 
   // ---- all global reads first
   if (scanned) {
-    for (int e = tid; e < E; e += kThreads) {
+    for (int e = tid; e < E; e += kT3) {
       const int n = n_e_in[e];
       const int b = cb[(int64_t)e * C + chunk];
       ne[e] = n;
@@ -324,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
       ccnt[e] = (chunk + 1 < C ? cb[(int64_t)e * C + chunk + 1] : n) - b;
     }
   }
-  int p_k[kPasses][KM];
+  int p_k[kP3][KM];
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) load_slots<KM>(packed, chunk * kChunkTokens + tid + kThreads * j, L, K, p_k[j]);
+  for (int j = 0; j < kP3; ++j) load_slots<KM>(packed, chunk * kChunkTokens + tid + kT3 * j, L, K, p_k[j]);
   if (!scanned) {
     // small layer: a warp per expert sums its chunk counts, before this
     // chunk (the base) and over all chunks (n_e)
-    for (int e = warp; e < E; e += kThreads / 32) {
+    for (int e = warp; e < E; e += kT3 / 32) {
       int before = 0, all = 0, mine = 0;
       for (int64_t c = lane; c < C; c += 32) {
         const int v = cb[(int64_t)e * C + c];
@@ -355,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   // (K1 marks the others -1) and pairwise distinct
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
+  for (int j = 0; j < kP3; ++j) {
+    const int64_t t = chunk * kChunkTokens + tid + kT3 * j;
     if (t >= L) continue;
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
@@ -370,13 +378,14 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   }
   __syncthreads();
 
-  // ---- expert offsets (exclusive scan of n_e) and padded offsets: warp 0,
-  // lane l owning experts [l*per, (l+1)*per), the two counts packed in one
-  // 64-bit word (neither half's running sum reaches 2^32)
-  if (warp == 0) {
-    // ... and the chunk's own counts into its staging offsets
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
+  // ---- expert offsets (exclusive scan of n_e), padded offsets and the
+  // chunk's staging offsets (scan of its own counts): thread i owns experts
+  // [i*per, (i+1)*per); a warp scan, then the warps' totals.  n_e and its
+  // padded value are packed in one 64-bit word (neither half's running sum
+  // reaches 2^32).
+  {
+    const int per = (E + kT3 - 1) / kT3;
+    const int e0 = tid * per;
     unsigned long long mine = 0ull;
     int cmine = 0;
     for (int i = 0; i < per; ++i) {
@@ -398,8 +407,17 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
         cincl += cu;
       }
     }
+    if (lane == 31) {
+      wtot[warp] = incl;
+      wctot[warp] = cincl;
+    }
+    __syncthreads();
     unsigned long long run = incl - mine;
     int crun = cincl - cmine;
+    for (int w2 = 0; w2 < warp; ++w2) {
+      run += wtot[w2];
+      crun += wctot[w2];
+    }
     for (int i = 0; i < per; ++i) {
       const int e = e0 + i;
       if (e < E) {
@@ -413,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
         crun += ccnt[e];
       }
     }
-    if (lane == 31) {
-      off[E] = (int32_t)(incl & 0xffffffffull);
-      poff[E] = (int32_t)(incl >> 32);
-      nstage = cincl;
+    if (tid == kT3 - 1) {
+      off[E] = (int32_t)(run & 0xffffffffull);
+      poff[E] = (int32_t)(run >> 32);
+      nstage = crun;
     }
   }
   // one atomic per CTA, and only for invalid routing; the barrier also
@@ -428,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   // the chunk's staging at its position minus delta[e] (the chunk's slots of
   // one expert are consecutive there, as in expert_token_indices)
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    const int64_t t = chunk * kChunkTokens + tid + kThreads * j;
+  for (int j = 0; j < kP3; ++j) {
+    const int64_t t = chunk * kChunkTokens + tid + kT3 * j;
     if (t >= L) continue;
     int d4[KM];
 #pragma unroll
@@ -455,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   // skips this (its part of the output is unspecified; nothing is written
   // outside the buffer).
   if (!any_bad)
-    for (int j = tid; j < nstage; j += kThreads) D1[delta[stage_e[j]] + j] = stage_t[j];
+    for (int j = tid; j < nstage; j += kT3) D1[delta[stage_e[j]] + j] = stage_t[j];
 
   // ---- GEMM metadata, split over the CTAs
   // tile -> expert: tile m belongs to the expert whose padded rows hold row
@@ -463,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   const int64_t ntiles = poff[E] / kTileM;
   const int64_t per = (max_tiles + gridDim.x - 1) / gridDim.x;
   const int64_t m0 = (int64_t)blockIdx.x * per, m1 = min(max_tiles, m0 + per);
-  for (int64_t m = m0 + tid; m < m1; m += kThreads) {
+  for (int64_t m = m0 + tid; m < m1; m += kT3) {
     int32_t v = -1;
     if (m < ntiles) {
       const int64_t row = m * kTileM;
@@ -480,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
   // descending load, equal loads by index: the rank of expert e is the number
   // of experts j with n_j > n_e, or n_j == n_e and j < e.  One warp per expert,
   // the experts spread over the CTAs.
-  const int nwarps = kThreads / 32;
+  const int nwarps = kT3 / 32;
   for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
     const int32_t me = ne[e];
     int rank = 0;
@@ -501,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, KM <= 4 ? 5 : 1) scatter_kernel(int6
     meta.hdr[kHdrE] = E;
     meta.hdr[kHdrK] = K;
   }
-  for (int e = tid; e <= E; e += kThreads) {
+  for (int e = tid; e <= E; e += kT3) {
     D2[e] = off[e];
     meta.pad_off[e] = poff[e];
     if (e < E) meta.n_e[e] = ne[e];
@@ -531,7 +549,7 @@ moeblaze_status run_tail(const moeblaze_shape& s, const moeblaze_dispatch& out, 
   const size_t sm3 = (size_t)(7 * E + 2) * sizeof(int32_t) + (size_t)kChunkTokens * KM * (sizeof(int32_t) + sizeof(uint16_t));
   if (sm3 > 48 * 1024)
     MB_CUDA(cudaFuncSetAttribute(scatter_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<KM><<<(unsigned)C, kThreads, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
+  scatter_kernel<KM><<<(unsigned)C, kT3, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
                                                           out.expert_token_indices, out.expert_token_offsets,
                                                           out.token_index_map, meta, mt);
   MB_CUDA(cudaGetLastError());
