@@ -325,8 +325,14 @@ __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt
     const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
     const int rank = (int)(tile / per_e);
     const int r = (int)(tile % per_e);
-    const int mt = r % p.m_tiles_w;
-    nt = r / p.m_tiles_w;
+    // groups of GW m-tiles walk the n-tiles together: the CTAs running at
+    // once then share fewer, more reused A and B slices in L2
+    constexpr int GW = 16;
+    const int g = r / (GW * p.n_tiles);
+    const int gw = min(GW, p.m_tiles_w - g * GW);
+    const int rr = r - g * GW * p.n_tiles;
+    const int mt = g * GW + rr % gw;
+    nt = rr / gw;
     t.e = p.meta.order[rank];
     t.row0 = mt * BM;
     t.pad0 = p.meta.pad_off[t.e];
