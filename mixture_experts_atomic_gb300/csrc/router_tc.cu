@@ -18,7 +18,7 @@
 //
 // Grid: one CTA per 128 tokens, clusters of 8 CTAs = one 1024-token dispatch
 // chunk.  Warp 4 streams the CTA's x tile and the split weights by TMA
-// through a 4-stage ring, warp 5 allocates TMEM and issues
+// through a 4-stage ring (2 stages for 64 experts), warp 5 allocates TMEM and issues
 // tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = 3 EP rounded up to 16),
 // warps 0-3 (one token per thread, TMEM lanes 32w..32w+31) read the
 // accumulator row, add the three parts and the bias, select the top K
@@ -40,7 +40,6 @@ namespace tc {
 namespace {
 
 constexpr int kRtTokens = 128;                      // tokens per CTA (one M tile)
-constexpr int kRtStages = 4;
 constexpr int kRtThreads = 192;                     // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kRtCluster = kChunkTokens / kRtTokens;  // CTAs of one dispatch chunk (8)
 constexpr int kRtA = kRtTokens * 64 * 2;            // one x k-block: 16 KB
@@ -51,8 +50,11 @@ __host__ __device__ constexpr int rt_cols(int ep) {
   return rt_n(ep) <= 32 ? 32 : rt_n(ep) <= 64 ? 64 : rt_n(ep) <= 128 ? 128 : 256;
 }
 __host__ __device__ constexpr int rt_stage(int ep) { return kRtA + rt_n(ep) * 128; }
+// ring depth: 4 stages, 2 for 64 experts, whose 40 KB stages would otherwise
+// leave room for one CTA per SM (a cluster of 8 then needs 8 free SMs of a GPC)
+__host__ __device__ constexpr int rt_stages(int ep) { return ep >= 64 ? 2 : 4; }
 // ring | barriers, TMEM address, abort flag | bitmap words [EP][4] | popcounts [EP] | bases [EP] | 1 KB alignment slack
-__host__ __device__ constexpr int rt_smem(int ep) { return kRtStages * rt_stage(ep) + 256 + ep * 4 * 4 + 2 * ep * 4 + 1024; }
+__host__ __device__ constexpr int rt_smem(int ep) { return rt_stages(ep) * rt_stage(ep) + 256 + ep * 4 * 4 + 2 * ep * 4 + 1024; }
 
 struct RtParams {
   CUtensorMap tmX;  // x (L x d bf16), boxes of 64 columns x 128 rows
@@ -97,7 +99,7 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
 
 template <int EP>
 __global__ void __launch_bounds__(kRtThreads, 1) router_k1_kernel(const __grid_constant__ RtParams p) {
-  constexpr int N = rt_n(EP), TCOLS = rt_cols(EP), SB = rt_stage(EP);
+  constexpr int N = rt_n(EP), TCOLS = rt_cols(EP), SB = rt_stage(EP), kRtStages = rt_stages(EP);
   constexpr int NLD = (3 * EP + 31) / 32;  // 32-column TMEM loads that cover the three parts
   extern __shared__ uint8_t rt_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_raw) + 1023) & ~uintptr_t(1023));
