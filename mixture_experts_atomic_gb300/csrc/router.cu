@@ -517,21 +517,44 @@ __global__ void __launch_bounds__(kRThreads) router_dwr_kernel(const T* __restri
   if (blockIdx.x == 0 && tid < E) part_b[(int64_t)blockIdx.y * E + tid] = bacc;
 }
 
-// dWr for few experts (EP <= 16): a thread owns 8 consecutive rows of Wr
-// (columns j of x) for all EP experts and reads its 16-byte piece of each
-// token row of x straight from global memory (coalesced across the CTA);
-// the chunk's dlogits are expanded to a dense 64 x EP tile in shared memory
-// and read as broadcasts.  part[s][j][e] as in router_dwr_kernel.
+// The router backward for few experts (EP <= 16) in one pass over x: a
+// thread owns 8 consecutive columns j of x (rows of Wr) for all EP experts.
+// Per 64-token chunk the first 64 threads form the chunk's dlogits (the
+// softmax over the selected logits: dl_k = g_k (dg_k - sum_i g_i dg_i)),
+// as a dense 64 x EP tile and per slot; every thread then, token by token,
+// writes dx[t, j..j+7] = sum_k dl_k Wr[j.., e_k] (the CTA's rows of Wr
+// staged transposed in shared memory, so a thread's 8 values of one expert
+// are 32 contiguous bytes) and adds x[t, j..j+7] dl[t, :] to its partial
+// dWr.  Each thread keeps its next kBwAhead pieces of x in flight by
+// cp.async into a ring of its own in shared memory.  part[s][j][e] = sum over the split's tokens, summed in a fixed order
+// by router_reduce_kernel.
+constexpr int kBwThreads = 128;
+constexpr int kBwCols = kBwThreads * 8;  // columns of x (rows of Wr) per CTA
+constexpr int kBwAhead = 8;              // tokens of x each thread has in flight (cp.async)
 template <typename T, int EP>
-__global__ void __launch_bounds__(256) router_dwr_small_kernel(const T* __restrict__ x,
-                                                               const int32_t* __restrict__ ids,
-                                                               const float* __restrict__ dl, int64_t L, int d, int E,
-                                                               int K, int64_t split, float* __restrict__ part,
-                                                               float* __restrict__ part_b) {
+constexpr size_t bwd_small_smem() {
+  return (size_t)EP * kBwCols * sizeof(float) + (size_t)kBwAhead * kBwThreads * 8 * sizeof(T);
+}
+
+template <typename T, int EP>
+__global__ void __launch_bounds__(kBwThreads) router_bwd_small_kernel(
+    const T* __restrict__ x, const float* __restrict__ Wr, const int32_t* __restrict__ ids,
+    const float* __restrict__ gates, const float* __restrict__ dgates, int64_t L, int d, int E, int K, int64_t split,
+    T* __restrict__ dx, float* __restrict__ part, float* __restrict__ part_b) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  float* wt = reinterpret_cast<float*>(rsm);  // [EP][kBwCols]: Wr^T, this CTA's columns
+  T* xs = reinterpret_cast<T*>(wt + EP * kBwCols);  // [kBwAhead][kBwThreads][8]: each thread's own x pieces
   __shared__ __align__(16) float dd[kRT][EP];
+  __shared__ float dls[kRT][kMaxK];
+  __shared__ int ids_s[kRT][kMaxK];
   const int tid = threadIdx.x;
-  const int j = (blockIdx.x * blockDim.x + tid) * 8;  // first of this thread's 8 columns
+  const int col0 = blockIdx.x * kBwCols;
+  const int j = col0 + tid * 8;
   const bool jv = j < d;
+  for (int i = tid; i < EP * kBwCols; i += kBwThreads) {
+    const int e = i / kBwCols, c = i % kBwCols;
+    wt[i] = (e < E && col0 + c < d) ? Wr[(int64_t)(col0 + c) * E + e] : 0.f;
+  }
   const int64_t ts = (int64_t)blockIdx.y * split;
   const int64_t tend = min(L, ts + split);
   float acc[8][EP];
@@ -541,14 +564,29 @@ __global__ void __launch_bounds__(256) router_dwr_small_kernel(const T* __restri
     for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
   float bacc = 0.f;
   for (int64_t c0 = ts; c0 < tend; c0 += kRT) {
-    __syncthreads();  // every thread is done with the previous chunk's tile
-    for (int i = tid; i < kRT * EP; i += blockDim.x) (&dd[0][0])[i] = 0.f;
-    __syncthreads();
-    if (tid < kRT && c0 + tid < tend) {
+    __syncthreads();  // every thread is done with the previous chunk's dlogits
+    if (tid < kRT) {
       const int64_t t = c0 + tid;
-      for (int k = 0; k < K; ++k) {
-        const int e = ids[t * K + k];
-        if ((unsigned)e < (unsigned)E) dd[tid][e] = dl[t * K + k];
+      const bool tv = t < tend;
+      float g[kMaxK], dg[kMaxK], sdot = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        g[k] = (k < K && tv) ? gates[t * K + k] : 0.f;
+        dg[k] = (k < K && tv) ? dgates[t * K + k] : 0.f;
+        const int e = (k < K && tv) ? ids[t * K + k] : 0;
+        ids_s[tid][k] = ((unsigned)e < (unsigned)E) ? e : 0;
+        sdot = fmaf(g[k], dg[k], sdot);
+      }
+#pragma unroll
+      for (int e = 0; e < EP; ++e) dd[tid][e] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        const float v = g[k] * (dg[k] - sdot);
+        dls[tid][k] = k < K ? v : 0.f;
+        if (k < K && tv) {
+          const int e = ids[t * K + k];
+          if ((unsigned)e < (unsigned)E) dd[tid][e] = v;
+        }
       }
     }
     __syncthreads();
@@ -556,10 +594,43 @@ __global__ void __launch_bounds__(256) router_dwr_small_kernel(const T* __restri
     if (blockIdx.x == 0 && tid < EP)
       for (int t = 0; t < n; ++t) bacc += dd[t][tid];
     if (!jv) continue;
-#pragma unroll 4
+    // the thread's 8 columns of token c0 + tt into its own ring slot tt % kBwAhead
+    auto fetch = [&](int tt) {
+      const T* src = x + (c0 + tt) * d + j;
+      const uint32_t dst = saddr(xs + ((tt % kBwAhead) * kBwThreads + tid) * 8);
+#pragma unroll
+      for (int q = 0; q < (int)(8 * sizeof(T) / 16); ++q) cp16(dst + 16 * q, src + q * (16 / sizeof(T)), true);
+    };
+#pragma unroll
+    for (int tt = 0; tt < kBwAhead; ++tt) {
+      if (tt < n) fetch(tt);
+      cp_commit();
+    }
     for (int t = 0; t < n; ++t) {
+      cp_wait<kBwAhead - 1>();  // token t's copy (groups complete in order) has landed
       float xv[8];
-      load8(x + (c0 + t) * d + j, xv);
+      load8(xs + ((t % kBwAhead) * kBwThreads + tid) * 8, xv);
+      if (t + kBwAhead < n) fetch(t + kBwAhead);
+      cp_commit();
+      if (dx) {
+        float out[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) out[u] = 0.f;
+        for (int k = 0; k < K; ++k) {
+          const float dv = dls[t][k];
+          const float4* wr = reinterpret_cast<const float4*>(wt + ids_s[t][k] * kBwCols + tid * 8);
+          const float4 w0 = wr[0], w1 = wr[1];
+          out[0] = fmaf(dv, w0.x, out[0]);
+          out[1] = fmaf(dv, w0.y, out[1]);
+          out[2] = fmaf(dv, w0.z, out[2]);
+          out[3] = fmaf(dv, w0.w, out[3]);
+          out[4] = fmaf(dv, w1.x, out[4]);
+          out[5] = fmaf(dv, w1.y, out[5]);
+          out[6] = fmaf(dv, w1.z, out[6]);
+          out[7] = fmaf(dv, w1.w, out[7]);
+        }
+        store8(dx + (c0 + t) * d + j, out);
+      }
       const float4* dr = reinterpret_cast<const float4*>(&dd[t][0]);
 #pragma unroll
       for (int e4 = 0; e4 < EP / 4; ++e4) {
@@ -610,7 +681,7 @@ int padded_experts(int E) {
 // column blocks of the dWr kernel: 64 rows of Wr per CTA, or for few
 // experts 8 rows per thread of a 256-thread CTA
 int64_t router_col_blocks(const moeblaze_shape& s) {
-  return padded_experts(s.E) <= 16 ? (s.d + 2047) / 2048 : s.d / kRT;
+  return padded_experts(s.E) <= 16 ? (s.d + kBwCols - 1) / kBwCols : s.d / kRT;
 }
 
 // token splits of the weight-gradient sums: enough CTAs to fill the GPU a
@@ -676,32 +747,38 @@ moeblaze_status bwd_ep(const moeblaze_shape& s, const void* x, const float* Wr, 
   float* dl = reinterpret_cast<float*>(w);
   float* part = reinterpret_cast<float*>(w + align_up(sizeof(float) * s.L * s.K, 256));
   float* part_b = part + (size_t)S * s.d * s.E;
-  const unsigned tiles = (unsigned)((s.L + kRT - 1) / kRT);
-  {
-    auto kern = router_dx_kernel<T, EP>;
-    const size_t sm = dx_smem<EP>();
-    MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-    kern<<<tiles, kRThreads, sm, st>>>(Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, dl, static_cast<T*>(dx));
-    MB_CUDA(cudaGetLastError());
-  }
   if constexpr (EP <= 16) {
-    router_dwr_small_kernel<T, EP><<<dim3((unsigned)router_col_blocks(s), (unsigned)S), 256, 0, st>>>(
-        static_cast<const T*>(x), ids, dl, s.L, s.d, s.E, s.K, split, part, part_b);
+    auto kern = router_bwd_small_kernel<T, EP>;
+    const size_t sm = bwd_small_smem<T, EP>();  // plus 6 KB of static shared memory: always above the default limit
+    MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<dim3((unsigned)router_col_blocks(s), (unsigned)S), kBwThreads, sm, st>>>(
+        static_cast<const T*>(x), Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, split, static_cast<T*>(dx), part,
+        part_b);
     MB_CUDA(cudaGetLastError());
+    count_launch();
   } else {
+    const unsigned tiles = (unsigned)((s.L + kRT - 1) / kRT);
+    {
+      auto kern = router_dx_kernel<T, EP>;
+      const size_t sm = dx_smem<EP>();
+      MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+      kern<<<tiles, kRThreads, sm, st>>>(Wr, ids, gates, dgates, s.L, s.d, s.E, s.K, dl, static_cast<T*>(dx));
+      MB_CUDA(cudaGetLastError());
+    }
     auto kern = router_dwr_kernel<T, EP>;
     const size_t sm = dwr_smem<T, EP>();
     MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
     kern<<<dim3((unsigned)(s.d / kRT), (unsigned)S), kRThreads, sm, st>>>(static_cast<const T*>(x), ids, dl, s.L, s.d,
                                                                           s.E, s.K, split, part, part_b);
     MB_CUDA(cudaGetLastError());
+    count_launch(2);
   }
   const int64_t n = (int64_t)s.d * s.E;
   int64_t blocks = (n + s.E + 255) / 256;
   if (blocks > 8 * (int64_t)sm_count()) blocks = 8 * (int64_t)sm_count();
   router_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(part, part_b, n, s.E, (int)S, dWr, dbias);
   MB_CUDA(cudaGetLastError());
-  count_launch(3);
+  count_launch();
   return MOEBLAZE_OK;
 }
 
