@@ -119,6 +119,8 @@ def test_router_forward_on_the_softmax_workloads(ci):
     (700, 128, 256, 8, "bf16"),
     (5000, 1024, 8, 2, "bf16"),
     (40, 64, 3, 3, "f32"),
+    (2100, 1536, 12, 3, "f32"),   # <= 16 experts, one-pass kernel: fp32 x, 1.5 column blocks of 1024
+    (1500, 2560, 16, 4, "bf16"),  # 16 experts, 2.5 column blocks
 ])
 def test_router_backward_matches_oracle(L, d, E, K, dtype):
     x, Wr, b = _problem(L, d, E, K, dtype, seed=7 * L + E)
