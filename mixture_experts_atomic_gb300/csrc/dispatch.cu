@@ -60,6 +60,13 @@ DispatchWs carve(void* ws, const moeblaze_shape& s) {
   return w;
 }
 
+// Programmatic dependent launch: K2 and K3 are launched while the kernel
+// before them is still running (its last CTAs have started), so their launch
+// and CTA start-up overlap its tail; each waits for the previous kernel's
+// completion and memory before it reads anything that kernel wrote.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr int kThreads = 256;                       // 8 warps; warp w owns words w, w+8, w+16, w+24
 constexpr int kPasses = kChunkTokens / kThreads;    // tokens per thread (4)
 constexpr int kRow = kChunkWords + 1;               // padded shared row: conflict-free column walks
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   extern __shared__ uint32_t words[];  // [E][kRow]: a padded row keeps [e][w] and [e'][w] in different banks
   uint16_t* wpre = reinterpret_cast<uint16_t*>(words + E * kRow);  // [E][kRow]: set bits before word w
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  allow_dependents();  // K2 / K3 may start their CTAs once every K1 CTA has started
   const int64_t chunk = blockIdx.x;
   const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest expert id
 
@@ -262,15 +270,46 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   return r;
 }
 
+constexpr int kMaxScanVec = 4;  // K2: counts a thread keeps in registers, in 4-wide vectors
+
 // K2: one CTA per expert: exclusive scan of its chunk counts (in place) and
 // its total n_e.  Each thread sums a contiguous run of chunks.
 __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ cnt, int64_t C, int32_t* __restrict__ n_e) {
   __shared__ int wsum[32];
   __shared__ int total;
+  allow_dependents();
+  wait_previous();  // K1's counts
   const int e = blockIdx.x;
   int32_t* row = cnt + (int64_t)e * C;
   const int64_t per = (C + kThreads - 1) / kThreads;
   const int64_t c0 = threadIdx.x * per, c1 = (c0 + per < C) ? c0 + per : C;
+  if (C % 4 == 0 && per % 4 == 0 && per <= 4 * kMaxScanVec) {  // the same in every thread
+    // 16-byte aligned runs (every row starts at e*C, a multiple of 4): one
+    // vector load and one vector store per 4 counts, kept in registers
+    int4 v[kMaxScanVec];
+    int s = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxScanVec; ++q) {
+      const int64_t c = c0 + 4 * q;
+      v[q] = (4 * q < per && c < c1) ? *reinterpret_cast<const int4*>(row + c) : make_int4(0, 0, 0, 0);
+      s += v[q].x + v[q].y + v[q].z + v[q].w;
+    }
+    int run = block_excl_scan(s, wsum, &total);
+#pragma unroll
+    for (int q = 0; q < kMaxScanVec; ++q) {
+      const int64_t c = c0 + 4 * q;
+      if (4 * q < per && c < c1) {
+        int4 o;
+        o.x = run; run += v[q].x;
+        o.y = run; run += v[q].y;
+        o.z = run; run += v[q].z;
+        o.w = run; run += v[q].w;
+        *reinterpret_cast<int4*>(row + c) = o;
+      }
+    }
+    if (threadIdx.x == 0) n_e[e] = total;
+    return;
+  }
   int s = 0;
   for (int64_t c = c0; c < c1; ++c) s += row[c];
   int run = block_excl_scan(s, wsum, &total);
@@ -320,6 +359,7 @@ __global__ void __launch_bounds__(kT3, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L
   __shared__ unsigned long long wtot[kT3 / 32];
   __shared__ int wctot[kT3 / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  wait_previous();  // K1's slots and counts, K2's bases
   const int64_t chunk = blockIdx.x;
 
   // ---- all global reads first
@@ -530,6 +570,24 @@ __global__ void __launch_bounds__(kT3, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L
 
 namespace {
 
+// Launch `kern` on `st` as a programmatic dependent of the kernel before it
+// (the kernel calls wait_previous() before reading that kernel's output).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 // K2 (large layers) and K3 for ids of at most KM slots per token, once K1
 // (or the router kernel that does K1's work) has written the packed slots
 // and the per-(expert, chunk) counts.
@@ -542,16 +600,16 @@ moeblaze_status run_tail(const moeblaze_shape& s, const moeblaze_dispatch& out, 
   // small ones let every K3 CTA sum the counts it needs.
   const bool scanned = C * E > kInlineBaseCounts;
   if (scanned) {
-    scan_kernel<<<E, kThreads, 0, st>>>(w.base, C, meta.n_e);
+    MB_CUDA(launch_dependent(scan_kernel, dim3(E), dim3(kThreads), 0, st, w.base, C, meta.n_e));
     MB_CUDA(cudaGetLastError());
     count_launch();
   }
   const size_t sm3 = (size_t)(7 * E + 2) * sizeof(int32_t) + (size_t)kChunkTokens * KM * (sizeof(int32_t) + sizeof(uint16_t));
   if (sm3 > 48 * 1024)
     MB_CUDA(cudaFuncSetAttribute(scatter_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
-  scatter_kernel<KM><<<(unsigned)C, kT3, sm3, st>>>(L, E, K, w.packed, C, w.base, scanned, meta.n_e,
-                                                          out.expert_token_indices, out.expert_token_offsets,
-                                                          out.token_index_map, meta, mt);
+  MB_CUDA(launch_dependent(scatter_kernel<KM>, dim3((unsigned)C), dim3(kT3), sm3, st, L, E, K, (const int32_t*)w.packed,
+                           C, (const int32_t*)w.base, scanned, (const int32_t*)meta.n_e, out.expert_token_indices,
+                           out.expert_token_offsets, out.token_index_map, meta, mt));
   MB_CUDA(cudaGetLastError());
   count_launch();
   return MOEBLAZE_OK;

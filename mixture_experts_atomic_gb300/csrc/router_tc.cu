@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_k1_kernel(const __grid_c
   const uint32_t done = smem_u32(bars + 2 * kRtStages);
   const uint64_t lim = p.wait_ns;
 
+  // the dispatch's next kernels are launched as programmatic dependents: they
+  // may start their CTAs once every CTA of this one has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0 && tid == 0) *p.err = 0;  // a new build starts with a clean error word
   if (tid == 0) {
     for (int s = 0; s < kRtStages; ++s) {

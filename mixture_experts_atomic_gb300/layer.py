@@ -40,6 +40,20 @@ class MoELayer:
         B.dispatch_build(self.shape, ids, self.disp, validate=validate)
         return B.index_views(self.shape, self.disp)
 
+    def route(self, x: torch.Tensor, Wr: torch.Tensor, bias: Optional[torch.Tensor] = None):
+        """The softmax top-K router fused with the dispatch build
+        (moeblaze_router_dispatch_build): fills this layer's dispatch and
+        returns (topk_ids, gates), which forward and backward then take."""
+        if not hasattr(self, "_route_bufs"):
+            dev = Wr.device
+            self._route_bufs = (torch.empty((self.L, self.K), dtype=torch.int32, device=dev),
+                                torch.empty((self.L, self.K), dtype=torch.float32, device=dev),
+                                torch.empty(B.moeblaze_router_dispatch_workspace_bytes(self.shape), dtype=torch.uint8,
+                                            device=dev))
+        ids, gates, ws = self._route_bufs
+        B.router_dispatch_build(self.shape, x, Wr, bias, ids, gates, self.disp, ws)
+        return ids, gates
+
     def forward(self, x, gates, W1=None, W2=None, W3=None) -> torch.Tensor:
         B.forward(self.shape, x, gates, self.disp, W1, W2, W3, self.y, self.bufs)
         return self.y

@@ -26,6 +26,9 @@ def _layer(L, E, K, dtype=torch.bfloat16, d=128, h=128, act="swiglu"):
     (1, 1, 1, 0, None), (5, 4, 2, 1, None), (1000, 8, 2, 2, None), (1024, 8, 2, 3, None),
     (1025, 16, 4, 4, None), (3000, 64, 6, 5, 3), (4096, 512, 8, 6, None), (2048, 3, 3, 7, None),
     (777, 256, 4, 8, 200), (70000, 32, 2, 9, 0),
+    # chunk counts scanned by their own kernel (chunks x experts > 32768):
+    (66000, 512, 4, 10, None),   # 65 chunks per expert, scalar runs
+    (921000, 64, 2, 11, 5),      # 900 chunks: 4-wide vector runs, the last threads past the end
 ])
 def test_dispatch_matches_oracle(L, E, K, seed, one):
     ids, _ = I.random_routing(L, E, K, seed, one_expert=one)

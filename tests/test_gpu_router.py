@@ -156,11 +156,13 @@ def test_router_empty_batch():
     assert float(dWr.abs().sum()) == 0 and float(db.abs().sum()) == 0
 
 
-def test_router_then_layer_training_step():
+@pytest.mark.parametrize("fused", [False, True])
+def test_router_then_layer_training_step(fused):
     """router -> dispatch -> layer forward/backward (with gate gradients) ->
     router backward on the GPU, against the same composition of oracle
     functions.  The inputs keep every token's selection unique by a wide
-    margin, so both sides route identically."""
+    margin, so both sides route identically.  fused: the router and the
+    dispatch in one call (MoELayer.route)."""
     L, d, h, E, K = 768, 256, 384, 8, 2
     cfg = I.MoEConfig("t_router_step", L, d, h, E, K, "swiglu", "bf16", 21, "softmax")
     inp = I.make_inputs(cfg, "cpu")
@@ -173,12 +175,17 @@ def test_router_then_layer_training_step():
     ids = torch.empty((L, K), dtype=torch.int32, device="cuda")
     gates = torch.empty((L, K), dtype=torch.float32, device="cuda")
     x = inp["x"].cuda()
-    B.router_forward(shape, x, Wr.cuda(), b.cuda(), ids, gates)
     from mixture_experts_atomic_gb300.layer import MoELayer
     layer = MoELayer.for_config(cfg, "cuda")
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
-    dev["ids"], dev["gates"] = ids, gates
-    layer.step(dev)
+    if fused:
+        ids, gates = layer.route(x, Wr.cuda(), b.cuda())
+        layer.forward(x, gates, dev["W1"], dev["W2"], dev["W3"])
+        layer.backward(dev["dY"], x, gates, dev["W1"], dev["W2"], dev["W3"])
+    else:
+        B.router_forward(shape, x, Wr.cuda(), b.cuda(), ids, gates)
+        dev["ids"], dev["gates"] = ids, gates
+        layer.step(dev)
     dWr = torch.empty((d, E), device="cuda")
     db = torch.empty((E,), device="cuda")
     dxr = torch.empty((L, d), dtype=torch.bfloat16, device="cuda")
