@@ -189,34 +189,51 @@ __global__ void __launch_bounds__(kThreads) bitmap_kernel(const int32_t* __restr
   }
   __syncthreads();
 
-  // Word prefixes and the per-(expert, chunk) count: thread i covers words
-  // 4g..4g+3 of expert i/8 (g = i%8); the 8 threads of an expert are
-  // consecutive lanes and scan their popcounts with shuffles (counts stored
-  // [E][C] for the scan)
-  for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
-    const int i = i0 + tid;
-    const bool v = i < E * 8;
-    const int e = i >> 3, g = i & 7;
-    int c[4] = {0, 0, 0, 0};
-    if (v) {
+  // Word prefixes and the per-(expert, chunk) count (counts stored [E][C]
+  // for the scan).
+  if (E * 8 <= 2 * kThreads) {
+    // few experts: thread i covers words 4g..4g+3 of expert i/8 (g = i%8);
+    // the 8 threads of an expert are consecutive lanes and scan their
+    // popcounts with shuffles
+    for (int i0 = 0; i0 < E * 8; i0 += kThreads) {
+      const int i = i0 + tid;
+      const bool v = i < E * 8;
+      const int e = i >> 3, g = i & 7;
+      int c[4] = {0, 0, 0, 0};
+      if (v) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = __popc(words[e * kRow + 4 * g + q]);
-    }
-    const int mine = c[0] + c[1] + c[2] + c[3];
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if ((lane & 7) >= o) incl += u;
-    }
-    if (v) {
-      int r = incl - mine;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        wpre[e * kRow + 4 * g + q] = (uint16_t)r;
-        r += c[q];
+        for (int q = 0; q < 4; ++q) c[q] = __popc(words[e * kRow + 4 * g + q]);
       }
-      if (g == 7) cnt[(int64_t)e * C + chunk] = incl;
+      const int mine = c[0] + c[1] + c[2] + c[3];
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((lane & 7) >= o) incl += u;
+      }
+      if (v) {
+        int r = incl - mine;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          wpre[e * kRow + 4 * g + q] = (uint16_t)r;
+          r += c[q];
+        }
+        if (g == 7) cnt[(int64_t)e * C + chunk] = incl;
+      }
+    }
+  } else {
+    // many experts: a thread walks one expert's 32 words (the padded rows
+    // put the threads of a warp in different banks) with a running popcount
+    for (int e = tid; e < E; e += kThreads) {
+      const uint32_t* row = words + e * kRow;
+      uint16_t* prow = wpre + e * kRow;
+      int run = 0;
+#pragma unroll
+      for (int w = 0; w < kChunkWords; ++w) {
+        prow[w] = (uint16_t)run;
+        run += __popc(row[w]);
+      }
+      cnt[(int64_t)e * C + chunk] = run;
     }
   }
   __syncthreads();
