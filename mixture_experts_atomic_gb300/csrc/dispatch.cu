@@ -416,23 +416,6 @@ __global__ void __launch_bounds__(kT3, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L
       }
     }
   }
-  // routing checks while the loads land: every slot of a token in [0, E)
-  // (K1 marks the others -1) and pairwise distinct
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < kP3; ++j) {
-    const int64_t t = chunk * kChunkTokens + tid + kT3 * j;
-    if (t >= L) continue;
-#pragma unroll
-    for (int k = 0; k < KM; ++k) {
-      if (k >= K) break;
-      const int e = p_k[j][k] & 0xffff;
-      if (p_k[j][k] < 0) bad = true;
-#pragma unroll
-      for (int i = 0; i < k; ++i)
-        if (p_k[j][i] >= 0 && e == (p_k[j][i] & 0xffff)) bad = true;
-    }
-  }
   __syncthreads();
 
   // ---- expert offsets (exclusive scan of n_e), padded offsets and the
@@ -494,9 +477,14 @@ __global__ void __launch_bounds__(kT3, KM <= 4 ? 5 : 1) scatter_kernel(int64_t L
       nstage = crun;
     }
   }
-  // one atomic per CTA, and only for invalid routing; the barrier also
-  // publishes the offsets
-  const bool any_bad = __syncthreads_or(bad) != 0;
+  __syncthreads();  // publishes the offsets and nstage
+  // Routing check, one comparison per chunk: with every id in [0, E) and no
+  // id repeated within a token, the chunk's bitmap holds one bit per slot,
+  // so its counts add up to tokens x K; an id out of range (K1 left it out)
+  // or a repeated one (two slots, one bit) leaves the sum short.  One atomic
+  // per CTA, and only for invalid routing.
+  const int64_t ntok = min((int64_t)kChunkTokens, L - chunk * kChunkTokens);
+  const bool any_bad = (int64_t)nstage != ntok * K;
   if (any_bad && tid == 0) atomicOr(meta.err, kErrBadRouting);
 
   // ---- place every (token, slot): token_index_map directly, the token into
