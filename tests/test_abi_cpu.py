@@ -208,3 +208,34 @@ def test_bf16_backward_scratch_has_no_gradient_buffer():
     assert B.moeblaze_backward_workspace_bytes(s) == up(rows * h * 2) + up(L * d * 4) + 256
     f = B.make_shape(L, d, h, E, K, B.F32, "swiglu")
     assert B.moeblaze_backward_workspace_bytes(f) == up(rows * 2 * h * 4) + up(rows * h * 4)
+
+
+def test_router_dispatch_validation_codes():
+    """moeblaze_router_dispatch_build: both the dispatch's and the router's
+    shape rules apply, and its scratch holds the dispatch's plus, on the
+    fused path (bf16 x, <= 64 experts, >= 128 tokens), the split router
+    weights (3 x 8 rows of d bf16, rounded up to 16 rows, for <= 8 experts)."""
+    _lib()
+    ok = B.make_shape(4096, 1024, 1024, 8, 2, B.BF16, "silu")
+    n = B.moeblaze_router_dispatch_workspace_bytes(ok)
+    split = 32 * 1024 * 2
+    assert n == B.moeblaze_dispatch_workspace_bytes(ok) + split
+    # the unfused shapes need only the dispatch's scratch
+    for sh in (B.make_shape(4096, 1024, 1024, 8, 2, B.F32, "silu"),      # fp32 x
+               B.make_shape(4096, 1024, 1024, 100, 2, B.BF16, "silu"),   # more than 64 experts
+               B.make_shape(100, 1024, 1024, 8, 2, B.BF16, "silu")):     # fewer than 128 tokens
+        assert B.moeblaze_router_dispatch_workspace_bytes(sh) == B.moeblaze_dispatch_workspace_bytes(sh)
+    # router limits (E > 256) and dispatch limits (bf16 d % 128) both refuse
+    assert B.moeblaze_router_dispatch_workspace_bytes(B.make_shape(4096, 1024, 1024, 300, 2, B.BF16, "silu")) == 0
+    assert B.moeblaze_router_dispatch_workspace_bytes(B.make_shape(4096, 192, 1024, 8, 2, B.BF16, "silu")) == 0
+    call = lambda sh, x=FAKE, Wr=FAKE, ids=FAKE, g=FAKE, d=None, ws=FAKE, nb=n: B.moeblaze_router_dispatch_build(
+        sh, x, Wr, None, ids, g, _disp() if d is None else d, ws, nb, None)
+    assert call(ok, nb=n - 1) == B.ERR_WORKSPACE
+    assert call(ok, Wr=None) == B.ERR_INVALID_ARG
+    assert call(ok, x=MISALIGNED) == B.ERR_INVALID_ARG
+    assert call(ok, ids=None) == B.ERR_INVALID_ARG
+    assert call(ok, ws=None) == B.ERR_INVALID_ARG
+    d = _disp()
+    d.meta = None
+    assert call(ok, d=d) == B.ERR_INVALID_ARG
+    assert call(B.make_shape(16, 128, 128, 2, 3, B.BF16, "silu")) == B.ERR_INVALID_ARG  # K > E
