@@ -270,11 +270,13 @@ __global__ void __launch_bounds__(512) router_fwd_gemv_kernel(const T* __restric
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t t0 = warp * TPW; t0 < L; t0 += nwarps * TPW) {
-    float acc[TPW][EP];
+    // pairs of experts per packed fp32x2 FMA for up to 8 experts (each half
+    // is an ordinary fp32 FMA, round to nearest, so the logits are the same)
+    float2 acc2[TPW][EP / 2];
 #pragma unroll
     for (int q = 0; q < TPW; ++q)
 #pragma unroll
-      for (int e = 0; e < EP; ++e) acc[q][e] = 0.f;
+      for (int e = 0; e < EP / 2; ++e) acc2[q][e] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int c0 = lane * 8; c0 < d; c0 += 256) {
       float xv[TPW][8];
@@ -293,16 +295,31 @@ __global__ void __launch_bounds__(512) router_fwd_gemv_kernel(const T* __restric
 #pragma unroll
         for (int e4 = 0; e4 < EP / 4; ++e4) {
           const float4 w = wr[e4];
+          const float2 wa = make_float2(w.x, w.y), wb = make_float2(w.z, w.w);
 #pragma unroll
           for (int q = 0; q < TPW; ++q) {
-            acc[q][4 * e4 + 0] = fmaf(xv[q][u], w.x, acc[q][4 * e4 + 0]);
-            acc[q][4 * e4 + 1] = fmaf(xv[q][u], w.y, acc[q][4 * e4 + 1]);
-            acc[q][4 * e4 + 2] = fmaf(xv[q][u], w.z, acc[q][4 * e4 + 2]);
-            acc[q][4 * e4 + 3] = fmaf(xv[q][u], w.w, acc[q][4 * e4 + 3]);
+            const float2 x2 = make_float2(xv[q][u], xv[q][u]);
+            if constexpr (EP <= 8) {
+              acc2[q][2 * e4 + 0] = __ffma2_rn(x2, wa, acc2[q][2 * e4 + 0]);
+              acc2[q][2 * e4 + 1] = __ffma2_rn(x2, wb, acc2[q][2 * e4 + 1]);
+            } else {  // 16 experts: scalar FMAs keep the registers within the 512-thread budget
+              acc2[q][2 * e4 + 0].x = fmaf(x2.x, wa.x, acc2[q][2 * e4 + 0].x);
+              acc2[q][2 * e4 + 0].y = fmaf(x2.x, wa.y, acc2[q][2 * e4 + 0].y);
+              acc2[q][2 * e4 + 1].x = fmaf(x2.x, wb.x, acc2[q][2 * e4 + 1].x);
+              acc2[q][2 * e4 + 1].y = fmaf(x2.x, wb.y, acc2[q][2 * e4 + 1].y);
+            }
           }
         }
       }
     }
+    float acc[TPW][EP];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+      for (int e = 0; e < EP / 2; ++e) {
+        acc[q][2 * e] = acc2[q][e].x;
+        acc[q][2 * e + 1] = acc2[q][e].y;
+      }
 #pragma unroll
     for (int q = 0; q < TPW; ++q)
 #pragma unroll
