@@ -762,8 +762,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-recompute-leg", action="store_true",
                     help="skip timing the step again with MOEBLAZE_RECOMPUTE_H (no H / Hg temporaries)")
-    ap.add_argument("--only", choices=["dispatch"], default=None,
-                    help="time only the dispatch build of the workload (allocates only its routing and index buffers)")
+    ap.add_argument("--only", choices=["dispatch", "router"], default=None,
+                    help="time only the dispatch build of the workload (allocates only its routing and index buffers), "
+                         "or only its router legs (x, the router's weights and outputs, the index buffers)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -778,6 +779,16 @@ def main():
     if args.only == "dispatch":
         if rank == 0:
             print(json.dumps(run_dispatch_only(args, local_rank)), flush=True)
+        return
+    if args.only == "router":
+        if rank == 0:
+            cfg = I.CONFIGS[args.config]
+            torch.cuda.set_device(local_rank)
+            dev = torch.device("cuda", local_rank)
+            flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+            pk, _ = peaks()
+            out = run_router(cfg, {"x": I.make_x(cfg, dev)}, dev, flush, pk, iters=args.steps)
+            print(json.dumps({"metric": "router legs", "config": {"workload": cfg.name}, "router": out}), flush=True)
         return
     if args.impl == "reference":
         if rank != 0:
