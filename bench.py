@@ -458,6 +458,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if cfg.router in ("softmax", "softmax_bias"):
         out["router"] = run_router(cfg, inp, dev, flush, pk)
+    if not args.no_graph_leg:
+        out["graph_step"] = run_graph_leg(args, layer, inp, flush, statistics.mean(step_ms))
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, cfg, layer, inp, dev, world)
     del layer
@@ -531,6 +533,18 @@ def identity_roofline(cfg, t_ms, pk, src):
             "traffic": traffic_per_launch(cfg.name, "identity_forward", IDENTITY_SRC),
             "peak_source": src, "algorithmic_bytes": nbytes, "ms": t_ms,
             "routed_row_bytes": rb, "routed_row_GB_per_s": rb / (t_ms * 1e-3) / 1e9}
+
+
+def run_graph_leg(args, layer, inp, flush, eager_ms):
+    """The same step captured once as a CUDA graph (layer.GraphStep) and
+    replayed: what one graph launch saves over a host call per kernel."""
+    from mixture_experts_atomic_gb300.layer import GraphStep
+    g = GraphStep(layer, inp)
+    ms = time_calls(g.replay, flush, args.warmup, min(args.steps, 10))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0, "device error in the graph leg"
+    del g
+    return {"ms": ms, "eager_ms": eager_ms, "saved_ms": eager_ms - ms}
 
 
 def time_calls(fn, flush, warmup, iters):
@@ -760,6 +774,8 @@ def main():
     ap.add_argument("--clock-log", default=None,
                     help="keep the raw nvidia-smi clock samples of the timed region at this path ({rank} is replaced)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph-leg", action="store_true",
+                    help="skip timing the step replayed as a captured CUDA graph")
     ap.add_argument("--no-recompute-leg", action="store_true",
                     help="skip timing the step again with MOEBLAZE_RECOMPUTE_H (no H / Hg temporaries)")
     ap.add_argument("--only", choices=["dispatch", "router"], default=None,

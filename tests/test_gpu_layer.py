@@ -183,3 +183,32 @@ def test_malformed_arguments_are_refused_before_launch():
     layer.step(inp)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
+
+
+@pytest.mark.parametrize("act,dtype", [("swiglu", "bf16"), ("silu", "bf16"), ("swiglu", "f32"), ("identity", "bf16")])
+def test_graph_step_matches_eager_step(act, dtype):
+    """The whole step captured as one CUDA graph (GraphStep) and replayed on
+    refilled inputs gives the same bits as eager steps (K = 2: every
+    reduction is order-independent)."""
+    from mixture_experts_atomic_gb300.layer import GraphStep, MoELayer
+    h = 0 if act == "identity" else 384
+    cfg = I.MoEConfig("t_graph", 1000, 256, h, 5, 2, act, dtype, 33, "softmax")
+    base = {k: (v.cuda() if v is not None else None) for k, v in I.make_inputs(cfg, "cpu").items()}
+    eager = MoELayer.for_config(cfg, "cuda", with_dgates=False)
+    layer = MoELayer.for_config(cfg, "cuda", with_dgates=False)
+    inp = {k: (v.clone() if v is not None else None) for k, v in base.items()}
+    g = GraphStep(layer, inp)
+    for i in range(2):
+        ids, gates = I.random_routing(cfg.L, cfg.E, cfg.K, 60 + i)
+        gen = torch.Generator().manual_seed(70 + i)
+        x = torch.randn(cfg.L, cfg.d, generator=gen).to(base["x"].dtype).cuda()
+        new = dict(base, ids=ids.cuda(), gates=gates.cuda(), x=x)
+        for k in ("ids", "gates", "x"):
+            inp[k].copy_(new[k])
+        g.replay()
+        eager.step(new)
+        torch.cuda.synchronize()
+        assert layer.device_error() == 0 and eager.device_error() == 0
+        assert torch.equal(layer.y, eager.y) and torch.equal(layer.dX, eager.dX)
+        if act != "identity":
+            assert torch.equal(layer.dW1, eager.dW1) and torch.equal(layer.dW3, eager.dW3)
