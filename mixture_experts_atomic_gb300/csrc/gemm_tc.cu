@@ -70,7 +70,6 @@ constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
 constexpr int PRODUCER_WARPS = 4;
 constexpr int PRODUCER_THREADS = PRODUCER_WARPS * 32;
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
@@ -119,14 +118,39 @@ __host__ __device__ constexpr int mma_warp(int m) { return PRODUCER_WARPS + help
 __host__ __device__ constexpr int num_threads(int m) { return (mma_warp(m) + 1 + 4) * 32; }
 // threads that recompute the A operand of a fused stage
 __host__ __device__ constexpr int transform_threads(int m) { return helper_warps(m) * 32; }
-// The ring: 4 stages of A (16 KB) + B operand (32 KB); the fused SwiGLU
-// stages add the saved-B tile (16 KB) to every stage and keep 3 of them.
-// The fused stages need no epilogue staging area.
-__host__ __device__ constexpr int stages_of(int m) { return fused_sw(m) ? 3 : STAGES; }
-__host__ __device__ constexpr int stage_bytes_of(int m) { return STAGE_BYTES + (fused_sw(m) ? A_BYTES : 0); }
-__host__ __device__ constexpr int smem_bytes_of(int m) {
-  return stages_of(m) * stage_bytes_of(m) + (is_fused(m) ? 0 : EPI_STAGE_BYTES) + 1024 + BAR_BYTES;
+// Launch variants of a stage: one CTA a tile, clusters of two CTAs sharing
+// the weight tiles (row stages), or wide weight-gradient tiles.
+enum Variant : int { SINGLE = 0, PAIRED = 1, WIDE = 2 };
+// Wide weight-gradient tiles: 256 output rows a CTA, as two M=128 MMAs that
+// share every B tile, into one 512-column accumulator (no second buffer: the
+// epilogue runs once per reduction, which is long when this is chosen).  A
+// k-block then brings 64 KB for 8.4 MFLOP instead of 48 KB for 4.2.
+__host__ __device__ constexpr bool widenable(int m) { return m == DW12 || m == DW1 || m == DW3_H; }
+// Measured: from 4,096 routed rows per expert (64 k-blocks a tile) the wide
+// tiles are 20-23% faster on dW1 (dW1 || dW2) and dW3 than 128-row tiles.
+constexpr int64_t kWideMinRows = 4096;  // routed rows per expert (on average) from which wide tiles are used
+// out_rows: rows of the weight gradient.  A last tile of 128 rows is allowed
+// where the A operand comes by TMA (dW3: the rows past the end load as zeros
+// and are not stored); the gathered A of dW1 needs whole 256-row tiles.
+inline bool wide_stage(const moeblaze_shape& s, int out_rows, bool half_tail_ok) {
+  return out_rows % (half_tail_ok ? BM : 2 * BM) == 0 && (int64_t)s.L * s.K >= kWideMinRows * s.E;
 }
+// The ring: 4 stages of A (16 KB) + B operand (32 KB); the fused SwiGLU
+// stages add the saved-B tile (16 KB) to every stage and keep 3 of them;
+// wide tiles keep 3 stages of A (32 KB) + B (32 KB).  The fused stages and
+// the weight-gradient stages need no epilogue staging area.
+__host__ __device__ constexpr int a_bytes_of(int v) { return v == WIDE ? 2 * A_BYTES : A_BYTES; }
+__host__ __device__ constexpr int stages_of(int m, int v = SINGLE) { return fused_sw(m) || v == WIDE ? 3 : STAGES; }
+__host__ __device__ constexpr int stage_bytes_of(int m, int v = SINGLE) {
+  return a_bytes_of(v) + B_MAX_BYTES + (fused_sw(m) ? A_BYTES : 0);
+}
+__host__ __device__ constexpr int epi_bytes_of(int m, int v = SINGLE) {
+  return is_fused(m) || v == WIDE ? 0 : EPI_STAGE_BYTES;
+}
+__host__ __device__ constexpr int smem_bytes_of(int m, int v = SINGLE) {
+  return stages_of(m, v) * stage_bytes_of(m, v) + epi_bytes_of(m, v) + 1024 + BAR_BYTES;
+}
+static_assert(smem_bytes_of(DW12, WIDE) <= 232448, "wide ring exceeds shared memory");
 __host__ __device__ constexpr bool is_dual(int m) { return m == UP_SWIGLU || m == DW12; }
 __host__ __device__ constexpr bool a_mn_major(int m) { return is_wgrad(m); }
 __host__ __device__ constexpr bool b_k_major(int m) { return m == DH_SWIGLU || m == DH_SILU || m == DX; }
@@ -315,7 +339,7 @@ struct Tile {
 // Tile `tile` of the launch.  In the paired stages a tile id names a pair of
 // 128-row tiles of one expert (a 256-row slice of its padded segment) at one
 // n-tile, and `rank` picks this CTA's half.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool WIDE_T = false>
 __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt, int rank) {
   Tile t;
   constexpr int TN = tile_n(MODE);
@@ -334,7 +358,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt
     const int mt = g * GW + rr % gw;
     nt = rr / gw;
     t.e = p.meta.order[rank];
-    t.row0 = mt * BM;
+    t.row0 = mt * BM * (WIDE_T ? 2 : 1);
     t.pad0 = p.meta.pad_off[t.e];
     t.kblocks = (p.meta.pad_off[t.e + 1] - t.pad0) / BK;
   } else {
@@ -389,13 +413,19 @@ __host__ __device__ constexpr bool cp_a(int m) {
 }
 __host__ __device__ constexpr bool cp_b(int m) { return is_dw3(m); }
 
-template <int MODE, bool PAIR>
+template <int MODE, int VAR>
 __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __grid_constant__ Params p) {
+  constexpr bool PAIR = VAR == PAIRED;
+  // WIDE: 256-row weight-gradient tiles (two M=128 MMAs a k-step, one accumulator)
+  constexpr bool WIDE_T = VAR == WIDE;
+  static_assert(!WIDE_T || widenable(MODE), "stage has no wide tiles");
+  constexpr int NACC = WIDE_T ? 1 : 2;  // accumulator buffers in TMEM
+  constexpr int AB = a_bytes_of(VAR);   // A part of a stage
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
   // FUSED: transform warps recompute the A operand from the saved tiles
   constexpr bool FUSED = is_fused(MODE);
   constexpr int MMA_WARP = mma_warp(MODE);
-  constexpr int NST = stages_of(MODE), SB = stage_bytes_of(MODE);
+  constexpr int NST = stages_of(MODE, VAR), SB = stage_bytes_of(MODE, VAR);
   constexpr int LAG = NST - 2;  // cp.async groups a producer thread keeps in flight
   // PAIR: clusters of two CTAs share the weight tiles (multicast) and the
   // tile queue (filled by rank 0)
@@ -413,7 +443,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
   }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * SB + (FUSED ? 0 : EPI_STAGE_BYTES));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * SB + epi_bytes_of(MODE, VAR));
   // bars: full[0..3], empty[4..7], tmem_full[8..9], tmem_empty[10..11], drain[12],
   // loaded[48..51] (fused stages: the TMA part of a stage has landed)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
@@ -539,7 +569,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       long long tile = take(0);
       Tile t;
       if (tile >= 0 && tile < total) {
-        t = decode<MODE, PAIR>(p, tile, num_mt, rank);
+        t = decode<MODE, PAIR, WIDE_T>(p, tile, num_mt, rank);
         load_tile_tokens(t, rtok, wtok);
       }
       ok = tile >= 0;
@@ -553,7 +583,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         }
         Tile tn;
         if (ntile < total) {
-          tn = decode<MODE, PAIR>(p, ntile, num_mt, rank);
+          tn = decode<MODE, PAIR, WIDE_T>(p, ntile, num_mt, rank);
           load_tile_tokens(tn, rnext, wfirst);
         }
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
@@ -582,7 +612,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           const uint32_t full = bar(s);
           const uint32_t loaded = bar(48 + s);
           const uint32_t sA = smem_base + s * SB;
-          const uint32_t sB = sA + A_BYTES;
+          const uint32_t sB = sA + AB;
           const uint32_t sX = sB + B_MAX_BYTES;  // fused SwiGLU: the saved-B tile
           const int k0 = kb * BK;
           int wnext[4];
@@ -603,7 +633,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
                                          (is_down(MODE) ? (uint32_t)(nmma * BK * 2) : 0u);
               mbar_expect_tx(loaded, tma_bytes);
             } else {
-              const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)A_BYTES) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
+              const uint32_t tma_bytes = (CPA ? 0u : (uint32_t)AB) + (CPB ? 0u : (uint32_t)(nmma * BK * 2));
               if (CP) mbar_expect_tx_only(full, tma_bytes);
               else mbar_expect_tx(full, tma_bytes);
             }
@@ -625,8 +655,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               const bool second = kb >= p.ksplit;
               tma_load_2d(sA, second ? &p.tmX : &p.tmA, second ? k0 - p.ksplit * BK : k0, t.row0, full);
             } else if constexpr (MODE == DW3_H) {
-              tma_load_2d(sA, &p.tmA, t.row0, t.pad0 + k0, full);
-              tma_load_2d(sA + 8192, &p.tmA, t.row0 + 64, t.pad0 + k0, full);
+#pragma unroll
+              for (int a = 0; a < AB / 8192; ++a) tma_load_2d(sA + 8192 * a, &p.tmA, t.row0 + 64 * a, t.pad0 + k0, full);
             } else if constexpr (is_down(MODE)) {
               tma_load_2d(sA, &p.tmA, k0, t.row0, loaded);
               if constexpr (fused_sw(MODE)) tma_load_2d(sX, &p.tmX, k0, t.row0, loaded);
@@ -679,7 +709,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               // MN-major operand gathered along K: 64 routed rows x (atoms of 64 columns)
               const int col0 = CPA ? t.row0 : t.n0;
               const uint32_t dst0 = CPA ? sA : sB;
-              const int natoms = CPA ? 2 : t.nw / 64;
+              const int natoms = CPA ? AB / 8192 : t.nw / 64;
               for (int j = 0; j < natoms; ++j) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -751,7 +781,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         if (lane == 0) tile = q_take(j);
         tile = __shfl_sync(0xffffffffu, tile, 0);
         if (tile < 0 || tile >= total) break;
-        const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
+        const Tile t = decode<MODE, PAIR, WIDE_T>(p, tile, num_mt, rank);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           float g2[2] = {1.f, 1.f};
           if constexpr (is_dw3(MODE)) {
@@ -784,7 +814,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       bool ok = true;
       long long tile = q_take(0);
       Tile t;
-      if (tile >= 0 && tile < total) t = decode<MODE, PAIR>(p, tile, num_mt, rank);
+      if (tile >= 0 && tile < total) t = decode<MODE, PAIR, WIDE_T>(p, tile, num_mt, rank);
       for (int j = 0; ok; ++j) {
         if (tile < 0) {
           ok = false;
@@ -799,7 +829,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         bool fetched = false;
         auto fetch_next = [&]() {
           ntile = q_take(j + 1);
-          if (ntile >= 0 && ntile < total) tn = decode<MODE, PAIR>(p, ntile, num_mt, rank);
+          if (ntile >= 0 && ntile < total) tn = decode<MODE, PAIR, WIDE_T>(p, ntile, num_mt, rank);
           fetched = true;
         };
         const int nmma = is_dual(MODE) ? 2 * t.nw : t.nw;
@@ -813,12 +843,21 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if (!ok) break;
           tc_fence_after();
           const uint32_t sA = smem_base + s * SB;
-          const uint32_t sB = sA + A_BYTES;
+          const uint32_t sB = sA + AB;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = a_mn_major(MODE) ? smem_desc(sA + kk * 2048, 8192, 1024) : smem_desc(sA + kk * 32, 16, 1024);
             const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
-            mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            if constexpr (WIDE_T) {
+              // rows 0-127 and 128-255 of the tile: A atoms 0-1 and 2-3, accumulator columns 0 and 256
+#pragma unroll
+              for (int hm = 0; hm < 2; ++hm)
+                mma_bf16(dcol + hm * 256, smem_desc(sA + hm * 16384 + kk * 2048, 8192, 1024), bd, idesc,
+                         (kb | kk) ? 1u : 0u);
+            } else {
+              const uint64_t ad =
+                  a_mn_major(MODE) ? smem_desc(sA + kk * 2048, 8192, 1024) : smem_desc(sA + kk * 32, 16, 1024);
+              mma_bf16(dcol, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            }
           }
           if constexpr (PAIR) mma_commit_mc(bar(4 + s), (uint16_t)0x3);  // frees the stage in both CTAs
           else mma_commit(bar(4 + s));
@@ -827,7 +866,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         }
         if (!ok) break;
         mma_commit(bar(8 + abuf));
-        if (++abuf == 2) { abuf = 0; aph ^= 1u; }
+        if (++abuf == NACC) { abuf = 0; aph ^= 1u; }
         if (!fetched) fetch_next();
         tile = ntile;
         t = tn;
@@ -849,7 +888,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       if (lane == 0) tile = q_take(j);
       tile = __shfl_sync(0xffffffffu, tile, 0);
       if (tile < 0 || tile >= total) break;
-      const Tile t = decode<MODE, PAIR>(p, tile, num_mt, rank);
+      const Tile t = decode<MODE, PAIR, WIDE_T>(p, tile, num_mt, rank);
       // Per-row context that does not depend on the accumulator is fetched
       // before waiting for it, so its latency overlaps the main loop.
       constexpr bool DH = MODE == DH_SWIGLU || MODE == DH_SILU;
@@ -1001,35 +1040,41 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if (valid && p.dg) atomicAdd(p.dg + (int64_t)tok * p.K + kslot, dgp);
         }
       } else {
-        // weight gradients: rows of dW_e, plain bf16 stores
-        const int64_t orow = (int64_t)(t.row0 + r);
-        if constexpr (MODE == DW12) {
-          const int64_t base = (int64_t)t.e * p.d * p.h + orow * p.h + t.n0;
-          for (int c = 0; c < 8; ++c) {
-            __nv_bfloat16* dst = (c < 4 ? p.o0 : p.o1) + base + 32 * (c & 3);
-            if (t.kblocks > 0) {
-              MB_TMEM_LD32(tbase + 32 * c, ra);
-              tmem_wait_ld();
+        // weight gradients: rows of dW_e, plain bf16 stores (wide tiles:
+        // the second 128 rows from accumulator columns 256-511)
+#pragma unroll 1
+        for (int hm = 0; hm < (WIDE_T ? 2 : 1); ++hm) {
+          if (WIDE_T && MODE == DW3_H && t.row0 + hm * BM >= p.h) break;  // half tile past the last row of dW3
+          const int64_t orow = (int64_t)(t.row0 + hm * BM + r);
+          const uint32_t tb = tbase + hm * 256;
+          if constexpr (MODE == DW12) {
+            const int64_t base = (int64_t)t.e * p.d * p.h + orow * p.h + t.n0;
+            for (int c = 0; c < 8; ++c) {
+              __nv_bfloat16* dst = (c < 4 ? p.o0 : p.o1) + base + 32 * (c & 3);
+              if (t.kblocks > 0) {
+                MB_TMEM_LD32(tb + 32 * c, ra);
+                tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
-              store_row32(dst, va);
-            } else {
-              store_zero32(dst);
+                for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+                store_row32(dst, va);
+              } else {
+                store_zero32(dst);
+              }
             }
-          }
-        } else {
-          const int ld = MODE == DW1 ? p.h : p.d;
-          const int64_t rows_e = MODE == DW1 ? p.d : p.h;
-          const int64_t base = (int64_t)t.e * rows_e * ld + orow * ld + t.n0;
-          for (int c = 0; c < t.nw / 32; ++c) {
-            if (t.kblocks > 0) {
-              MB_TMEM_LD32(tbase + 32 * c, ra);
-              tmem_wait_ld();
+          } else {
+            const int ld = MODE == DW1 ? p.h : p.d;
+            const int64_t rows_e = MODE == DW1 ? p.d : p.h;
+            const int64_t base = (int64_t)t.e * rows_e * ld + orow * ld + t.n0;
+            for (int c = 0; c < t.nw / 32; ++c) {
+              if (t.kblocks > 0) {
+                MB_TMEM_LD32(tb + 32 * c, ra);
+                tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
-              store_row32(p.o0 + base + 32 * c, va);
-            } else {
-              store_zero32(p.o0 + base + 32 * c);
+                for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+                store_row32(p.o0 + base + 32 * c, va);
+              } else {
+                store_zero32(p.o0 + base + 32 * c);
+              }
             }
           }
         }
@@ -1037,7 +1082,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       (void)rb; (void)vb;
       tc_fence_before();
       mbar_arrive(bar(10 + abuf));
-      if (++abuf == 2) { abuf = 0; aph ^= 1u; }
+      if (++abuf == NACC) { abuf = 0; aph ^= 1u; }
     }
     // the TMA stores issued by lane 0 complete before the CTA exits
     if (lane == 0) bulk_wait<0>();
@@ -1057,12 +1102,13 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
 // Launch one GEMM stage.  `tiles_bound` bounds the number of 128-row tiles;
 // one CTA per SM, never more than there are tiles.  PAIR: clusters of two
 // CTAs on pairs of tiles (see the kernel).
-template <int MODE, bool PAIR = false>
+template <int MODE, int VAR = SINGLE>
 moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
   if (tiles_bound <= 0) return MOEBLAZE_OK;
-  auto kern = moe_gemm_kernel<MODE, PAIR>;
-  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of(MODE)));
-  if constexpr (PAIR) {
+  auto kern = moe_gemm_kernel<MODE, VAR>;
+  constexpr int smem = smem_bytes_of(MODE, VAR);
+  MB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  if constexpr (VAR == PAIRED) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1071,7 +1117,7 @@ moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * (sm_count() / 2)));
     cfg.blockDim = dim3(num_threads(MODE));
-    cfg.dynamicSmemBytes = smem_bytes_of(MODE);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -1090,7 +1136,7 @@ moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
     MB_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
   } else {
     const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
-    kern<<<(unsigned)g, num_threads(MODE), smem_bytes_of(MODE), st>>>(p);
+    kern<<<(unsigned)g, num_threads(MODE), smem, st>>>(p);
   }
   MB_CUDA(cudaGetLastError());
   count_launch();
@@ -1191,7 +1237,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.sched = sched + 1;
       const int64_t nt = mt_bound * p.n_tiles;
       const bool pair = pair_stage(p.kblocks, nt);
-      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, true>(p, nt, st) : launch<DOWN_H>(p, nt, st))
+      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, PAIRED>(p, nt, st) : launch<DOWN_H>(p, nt, st))
                                : (sw ? launch<DOWN_SWIGLU>(p, nt, st) : launch<DOWN_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
@@ -1234,13 +1280,15 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.gsrc = dY;
     p.gld = s.d;
     p.N = s.d;
-    p.m_tiles_w = s.h / BM;
+    const bool wide = !rec && wide_stage(s, s.h, true);
+    p.m_tiles_w = wide ? (s.h + 2 * BM - 1) / (2 * BM) : s.h / BM;
     p.n_tiles = (s.d + 255) / 256;
     p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW3;
     p.sched = sched + 3;
-    moeblaze_status r = !rec ? launch<DW3_H>(p, p.total_w, st)
-                             : (sw ? launch<DW3_SWIGLU>(p, p.total_w, st) : launch<DW3_SILU>(p, p.total_w, st));
+    moeblaze_status r = rec    ? (sw ? launch<DW3_SWIGLU>(p, p.total_w, st) : launch<DW3_SILU>(p, p.total_w, st))
+                        : wide ? launch<DW3_H, WIDE>(p, p.total_w, st)
+                               : launch<DW3_H>(p, p.total_w, st);
     if (r == MOEBLAZE_OK) stage_event(ev++, st);
     return r;
   };
@@ -1266,8 +1314,8 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     if (!rec && !make_map(&p.tmO1, wsHg, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
     const int64_t nt = mt_bound * p.n_tiles;
     const bool pair = pair_stage(p.kblocks, nt);
-    moeblaze_status r = sw ? (pair ? launch<DH_SWIGLU, true>(p, nt, st) : launch<DH_SWIGLU>(p, nt, st))
-                           : (pair ? launch<DH_SILU, true>(p, nt, st) : launch<DH_SILU>(p, nt, st));
+    moeblaze_status r = sw ? (pair ? launch<DH_SWIGLU, PAIRED>(p, nt, st) : launch<DH_SWIGLU>(p, nt, st))
+                           : (pair ? launch<DH_SILU, PAIRED>(p, nt, st) : launch<DH_SILU>(p, nt, st));
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(ev++, st);
@@ -1284,7 +1332,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.acc32 = wsdX32;
     p.sched = sched + 1;
     const int64_t nt = mt_bound * p.n_tiles;
-    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, true>(p, nt, st) : launch<DX>(p, nt, st);
+    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, PAIRED>(p, nt, st) : launch<DX>(p, nt, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(ev++, st);
@@ -1295,12 +1343,14 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     if (!make_map(&p.tmB0, A, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
     if (sw && !make_map(&p.tmB1, B, s.h, rows, 64, 64)) return MOEBLAZE_ERR_CUDA;
     p.N = s.h;
-    p.m_tiles_w = s.d / BM;
+    const bool wide = wide_stage(s, s.d, false);
+    p.m_tiles_w = s.d / (wide ? 2 * BM : BM);
     p.n_tiles = sw ? s.h / 128 : (s.h + 255) / 256;
     p.total_w = (int64_t)s.E * p.m_tiles_w * p.n_tiles;
     p.o0 = dW1; p.o1 = dW2;
     p.sched = sched + 2;
-    moeblaze_status r = sw ? launch<DW12>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st);
+    moeblaze_status r = sw ? (wide ? launch<DW12, WIDE>(p, p.total_w, st) : launch<DW12>(p, p.total_w, st))
+                           : (wide ? launch<DW1, WIDE>(p, p.total_w, st) : launch<DW1>(p, p.total_w, st));
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(ev++, st);
