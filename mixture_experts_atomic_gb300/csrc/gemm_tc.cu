@@ -125,7 +125,9 @@ enum Variant : int { SINGLE = 0, PAIRED = 1, WIDE = 2 };
 // share every B tile, into one 512-column accumulator (no second buffer: the
 // epilogue runs once per reduction, which is long when this is chosen).  A
 // k-block then brings 64 KB for 8.4 MFLOP instead of 48 KB for 4.2.
-__host__ __device__ constexpr bool widenable(int m) { return m == DW12 || m == DW1 || m == DW3_H; }
+__host__ __device__ constexpr bool widenable(int m) {
+  return m == DW12 || m == DW1 || m == DW3_H || m == UP_SWIGLU || m == UP_SILU;
+}
 // Measured: from 4,096 routed rows per expert (64 k-blocks a tile) the wide
 // tiles are 20-23% faster on dW1 (dW1 || dW2) and dW3 than 128-row tiles.
 constexpr int64_t kWideMinRows = 4096;  // routed rows per expert (on average) from which wide tiles are used
@@ -145,12 +147,13 @@ __host__ __device__ constexpr int stage_bytes_of(int m, int v = SINGLE) {
   return a_bytes_of(v) + B_MAX_BYTES + (fused_sw(m) ? A_BYTES : 0);
 }
 __host__ __device__ constexpr int epi_bytes_of(int m, int v = SINGLE) {
-  return is_fused(m) || v == WIDE ? 0 : EPI_STAGE_BYTES;
+  return is_fused(m) || (v == WIDE && is_wgrad(m)) ? 0 : EPI_STAGE_BYTES;
 }
 __host__ __device__ constexpr int smem_bytes_of(int m, int v = SINGLE) {
   return stages_of(m, v) * stage_bytes_of(m, v) + epi_bytes_of(m, v) + 1024 + BAR_BYTES;
 }
-static_assert(smem_bytes_of(DW12, WIDE) <= 232448, "wide ring exceeds shared memory");
+static_assert(smem_bytes_of(DW12, WIDE) <= 232448 && smem_bytes_of(UP_SWIGLU, WIDE) <= 232448,
+              "wide ring exceeds shared memory");
 __host__ __device__ constexpr bool is_dual(int m) { return m == UP_SWIGLU || m == DW12; }
 __host__ __device__ constexpr bool a_mn_major(int m) { return is_wgrad(m); }
 __host__ __device__ constexpr bool b_k_major(int m) { return m == DH_SWIGLU || m == DH_SILU || m == DX; }
@@ -343,7 +346,7 @@ template <int MODE, bool PAIR, bool WIDE_T = false>
 __device__ __forceinline__ Tile decode(const Params& p, int64_t tile, int num_mt, int rank) {
   Tile t;
   constexpr int TN = tile_n(MODE);
-  constexpr int PM = PAIR ? 2 : 1;
+  constexpr int PM = PAIR || WIDE_T ? 2 : 1;
   int nt;
   if constexpr (is_wgrad(MODE)) {
     const int64_t per_e = (int64_t)p.m_tiles_w * p.n_tiles;
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_mt = is_wgrad(MODE) ? 0 : *p.meta.num_m_tiles;
-  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)(num_mt / (PAIR ? 2 : 1)) * p.n_tiles;
+  const int64_t total = is_wgrad(MODE) ? p.total_w : (int64_t)(num_mt / (PAIR || WIDE_T ? 2 : 1)) * p.n_tiles;
   int32_t* err = p.meta.err;
   const uint64_t lim = p.wait_ns;
 
@@ -543,11 +546,12 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       const int r16 = pt >> 3; // row offset 0..15 within a group of 16 rows
       // The routed-row tokens of the next tile are loaded while this tile's
       // k-blocks are issued, so a tile change costs no load latency.
-      int rtok[8], wtok[4], rnext[8], wfirst[4];
+      constexpr int NR = AB / 2048;  // gathered rows per thread (row stages): 8, wide tiles 16
+      int rtok[NR], wtok[4], rnext[NR], wfirst[4];
       auto load_tile_tokens = [&](const Tile& tt, int* rr, int* ww) {
         if constexpr (CP && !is_wgrad(MODE)) {
 #pragma unroll
-          for (int it = 0; it < 8; ++it) rr[it] = row_token(p, tt, tt.row0 + it * 16 + r16);
+          for (int it = 0; it < NR; ++it) rr[it] = row_token(p, tt, tt.row0 + it * 16 + r16);
         }
         if constexpr (CP && is_wgrad(MODE)) {
 #pragma unroll
@@ -698,9 +702,9 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if constexpr (CP) {
             // ---------------- gathered part of the stage
             if constexpr (!is_wgrad(MODE)) {
-              // K-major A: 128 routed rows x 64 columns of x (or dY)
+              // K-major A: 128 (wide tiles 256) routed rows x 64 columns of x (or dY)
 #pragma unroll
-              for (int it = 0; it < 8; ++it) {
+              for (int it = 0; it < NR; ++it) {
                 const int r = it * 16 + r16;
                 const __nv_bfloat16* src = p.gsrc + (int64_t)rtok[it] * p.gld + k0 + c8 * 8;
                 cp_async16(sA + r * 128 + ((c8 ^ (r & 7)) << 4), src);
@@ -746,7 +750,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
         if (ntile < total) {
           t = tn;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) rtok[i] = rnext[i];
+          for (int i = 0; i < NR; ++i) rtok[i] = rnext[i];
 #pragma unroll
           for (int i = 0; i < 4; ++i) wtok[i] = wfirst[i];
         }
@@ -848,11 +852,14 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bd = b_k_major(MODE) ? smem_desc(sB + kk * 32, 16, 1024) : smem_desc(sB + kk * 2048, 8192, 1024);
             if constexpr (WIDE_T) {
-              // rows 0-127 and 128-255 of the tile: A atoms 0-1 and 2-3, accumulator columns 0 and 256
+              // rows 0-127 and 128-255 of the tile (MN-major A: atoms 0-1 and
+              // 2-3; K-major A: 16 KB apart) into accumulator columns 0 and 256
 #pragma unroll
-              for (int hm = 0; hm < 2; ++hm)
-                mma_bf16(dcol + hm * 256, smem_desc(sA + hm * 16384 + kk * 2048, 8192, 1024), bd, idesc,
-                         (kb | kk) ? 1u : 0u);
+              for (int hm = 0; hm < 2; ++hm) {
+                const uint64_t ad = a_mn_major(MODE) ? smem_desc(sA + hm * 16384 + kk * 2048, 8192, 1024)
+                                                     : smem_desc(sA + hm * 16384 + kk * 32, 16, 1024);
+                mma_bf16(dcol + hm * 256, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+              }
             } else {
               const uint64_t ad =
                   a_mn_major(MODE) ? smem_desc(sA + kk * 2048, 8192, 1024) : smem_desc(sA + kk * 32, 16, 1024);
@@ -937,36 +944,45 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       float va[32], vb[32];
 
       if constexpr (!is_wgrad(MODE)) {
-        if constexpr (MODE == UP_SWIGLU) {
-          for (int c = 0; c < t.nw / 32; ++c) {
-            MB_TMEM_LD32(tbase + 32 * c, ra);
-            MB_TMEM_LD32(tbase + 128 + 32 * c, rb);
-            tmem_wait_ld();
+        if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU) {
+          // wide tiles: rows 128-255 of the tile from accumulator columns 256-511
+#pragma unroll 1
+          for (int hm = 0; hm < (WIDE_T ? 2 : 1); ++hm) {
+            const uint32_t tb = tbase + hm * 256;
+            const int wr = wrow0 + hm * BM;
+            const bool vr = hm == 0 ? valid : (q + BM - t.pad0) < t.n_e;
+            if constexpr (MODE == UP_SWIGLU) {
+              for (int c = 0; c < t.nw / 32; ++c) {
+                MB_TMEM_LD32(tb + 32 * c, ra);
+                MB_TMEM_LD32(tb + 128 + 32 * c, rb);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              va[i] = __uint_as_float(ra[i]);
-              vb[i] = __uint_as_float(rb[i]);
-            }
-            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
-            staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, vb, valid, lane);
-            if (p.o2) {  // H for the down projection (not with MOEBLAZE_RECOMPUTE_H)
-              float vh[32];
+                for (int i = 0; i < 32; ++i) {
+                  va[i] = __uint_as_float(ra[i]);
+                  vb[i] = __uint_as_float(rb[i]);
+                }
+                staged_store(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
+                staged_store(ring, &p.tmO1, t.n0 + 32 * c, wr, vb, vr, lane);
+                if (p.o2) {  // H for the down projection (not with MOEBLAZE_RECOMPUTE_H)
+                  float vh[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
-              staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vh, valid, lane);
-            }
-          }
-        } else if constexpr (MODE == UP_SILU) {
-          for (int c = 0; c < t.nw / 32; ++c) {
-            MB_TMEM_LD32(tbase + 32 * c, ra);
-            tmem_wait_ld();
+                  for (int i = 0; i < 32; ++i) vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
+                  staged_store(ring, &p.tmO2, t.n0 + 32 * c, wr, vh, vr, lane);
+                }
+              }
+            } else {
+              for (int c = 0; c < t.nw / 32; ++c) {
+                MB_TMEM_LD32(tb + 32 * c, ra);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
-            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, va, valid, lane);
-            if (p.o2) {  // H = SiLU(a) for the down projection (not with MOEBLAZE_RECOMPUTE_H)
+                for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
+                staged_store(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
+                if (p.o2) {  // H = SiLU(a) for the down projection (not with MOEBLAZE_RECOMPUTE_H)
 #pragma unroll
-              for (int i = 0; i < 32; ++i) vb[i] = va[i] * fast_sigmoid(va[i]);
-              staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, vb, valid, lane);
+                  for (int i = 0; i < 32; ++i) vb[i] = va[i] * fast_sigmoid(va[i]);
+                  staged_store(ring, &p.tmO2, t.n0 + 32 * c, wr, vb, vr, lane);
+                }
+              }
             }
           }
         } else if constexpr (is_down(MODE) || MODE == DX) {
@@ -1219,7 +1235,11 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       if (!make_map(&p.tmO0, A, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (sw && !make_map(&p.tmO1, B, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       if (!rec && !make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
-      moeblaze_status r = sw ? launch<UP_SWIGLU>(p, mt_bound * p.n_tiles, st) : launch<UP_SILU>(p, mt_bound * p.n_tiles, st);
+      // long reductions with many tiles: 256-row tiles (pairs of 128-row tiles of one expert)
+      const int64_t nt = mt_bound * p.n_tiles;
+      const bool wide = pair_stage(p.kblocks, nt);
+      moeblaze_status r = sw ? (wide ? launch<UP_SWIGLU, WIDE>(p, nt / 2, st) : launch<UP_SWIGLU>(p, nt, st))
+                             : (wide ? launch<UP_SILU, WIDE>(p, nt / 2, st) : launch<UP_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
     stage_event(1, st);
