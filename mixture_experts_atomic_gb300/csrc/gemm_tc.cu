@@ -126,7 +126,7 @@ enum Variant : int { SINGLE = 0, PAIRED = 1, WIDE = 2 };
 // epilogue runs once per reduction, which is long when this is chosen).  A
 // k-block then brings 64 KB for 8.4 MFLOP instead of 48 KB for 4.2.
 __host__ __device__ constexpr bool widenable(int m) {
-  return m == DW12 || m == DW1 || m == DW3_H || m == UP_SWIGLU || m == UP_SILU;
+  return m == DW12 || m == DW1 || m == DW3_H || m == UP_SWIGLU || m == UP_SILU || m == DOWN_H || m == DX;
 }
 // Measured: from 4,096 routed rows per expert (64 k-blocks a tile) the wide
 // tiles are 20-23% faster on dW1 (dW1 || dW2) and dW3 than 128-row tiles.
@@ -653,11 +653,15 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
               }
             };
             if constexpr (MODE == DOWN_H) {
-              tma_load_2d(sA, &p.tmA, k0, t.row0, full);
+#pragma unroll
+              for (int a = 0; a < AB / A_BYTES; ++a) tma_load_2d(sA + a * A_BYTES, &p.tmA, k0, t.row0 + a * BM, full);
             } else if constexpr (MODE == DX) {
               // [dA | dB] along K: the first ksplit k-blocks from dA, the rest from dB
               const bool second = kb >= p.ksplit;
-              tma_load_2d(sA, second ? &p.tmX : &p.tmA, second ? k0 - p.ksplit * BK : k0, t.row0, full);
+#pragma unroll
+              for (int a = 0; a < AB / A_BYTES; ++a)
+                tma_load_2d(sA + a * A_BYTES, second ? &p.tmX : &p.tmA, second ? k0 - p.ksplit * BK : k0,
+                            t.row0 + a * BM, full);
             } else if constexpr (MODE == DW3_H) {
 #pragma unroll
               for (int a = 0; a < AB / 8192; ++a) tma_load_2d(sA + 8192 * a, &p.tmA, t.row0 + 64 * a, t.pad0 + k0, full);
@@ -902,6 +906,10 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       int q = 0, tok = 0, kslot = 0;
       bool valid = false;
       float g = 1.f;
+      // wide tiles of the combining stages: the same for row q + 128
+      int tok_1 = 0;
+      bool valid_1 = false;
+      float g_1 = 1.f;
       uint4 nA[4], nB[4];
       if constexpr (!is_wgrad(MODE)) {
         q = t.row0 + r;
@@ -910,6 +918,13 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if (valid) {
             tok = p.D1[t.off + (q - t.pad0)];
             if constexpr (MODE != DX) g = gate_of(p, tok, t.e, &kslot);
+          }
+        }
+        if constexpr (WIDE_T && (is_down(MODE) || MODE == DX)) {
+          valid_1 = (q + BM - t.pad0) < t.n_e;
+          if (valid_1) {
+            tok_1 = p.D1[t.off + (q + BM - t.pad0)];
+            if constexpr (MODE != DX) g_1 = gate_of(p, tok_1, t.e);
           }
         }
         if constexpr (DH) {
@@ -991,15 +1006,21 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
           if constexpr (is_down(MODE)) {
             if (p.rowg && t.n0 == 0) p.rowg[q] = valid ? g : 0.f;
           }
-          float* dst = p.acc32 + (int64_t)tok * p.d + t.n0;
-          for (int c = 0; c < t.nw / 32; ++c) {
-            MB_TMEM_LD32(tbase + 32 * c, ra);
-            tmem_wait_ld();
-            if (valid) {
+          // wide tiles: rows 128-255 of the tile from accumulator columns 256-511
+#pragma unroll 1
+          for (int hm = 0; hm < (WIDE_T ? 2 : 1); ++hm) {
+            const bool vr = hm == 0 ? valid : valid_1;
+            const float gr = hm == 0 ? g : g_1;
+            float* dst = p.acc32 + (int64_t)(hm == 0 ? tok : tok_1) * p.d + t.n0;
+            for (int c = 0; c < t.nw / 32; ++c) {
+              MB_TMEM_LD32(tbase + hm * 256 + 32 * c, ra);
+              tmem_wait_ld();
+              if (vr) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                red_add_v4(dst + 32 * c + i, g * __uint_as_float(ra[i]), g * __uint_as_float(ra[i + 1]),
-                           g * __uint_as_float(ra[i + 2]), g * __uint_as_float(ra[i + 3]));
+                for (int i = 0; i < 32; i += 4)
+                  red_add_v4(dst + 32 * c + i, gr * __uint_as_float(ra[i]), gr * __uint_as_float(ra[i + 1]),
+                             gr * __uint_as_float(ra[i + 2]), gr * __uint_as_float(ra[i + 3]));
+              }
             }
           }
         } else {  // DH_SWIGLU / DH_SILU
@@ -1257,7 +1278,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.sched = sched + 1;
       const int64_t nt = mt_bound * p.n_tiles;
       const bool pair = pair_stage(p.kblocks, nt);
-      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, PAIRED>(p, nt, st) : launch<DOWN_H>(p, nt, st))
+      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, WIDE>(p, nt / 2, st) : launch<DOWN_H>(p, nt, st))
                                : (sw ? launch<DOWN_SWIGLU>(p, nt, st) : launch<DOWN_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
@@ -1352,7 +1373,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.acc32 = wsdX32;
     p.sched = sched + 1;
     const int64_t nt = mt_bound * p.n_tiles;
-    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, PAIRED>(p, nt, st) : launch<DX>(p, nt, st);
+    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, WIDE>(p, nt / 2, st) : launch<DX>(p, nt, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(ev++, st);
