@@ -19,13 +19,21 @@
 // The CTAs claim tiles from a per-launch counter (weight-gradient tiles in
 // descending order of expert load), so skewed expert loads balance.
 //
-// Paired stages (down with stored H, dH, dX, when the reduction is at least
-// 64 k-blocks long): the kernel runs as clusters of two CTAs that take two
-// 128-row tiles of one expert at the same n-tile.  Both need the same weight tiles: each CTA loads half of the boxes
-// and multicasts them to both, halving the weight bytes each SM pulls from
-// L2.  A stage is free again once both CTAs' MMAs have consumed it (their
-// commits arrive in both CTAs), and the leader (rank 0) claims the pair tiles
-// and posts them into both CTAs' tile queues.
+// Wide tiles (up, down with stored H and dX from 32 k-blocks a tile; weight
+// gradients from 4,096 routed rows per expert): one CTA takes 256
+// output rows, as two M=128 MMAs per 16-deep step that share every B tile,
+// into one 512-column accumulator.  A k-block then brings 64 KB for
+// 8.4 MFLOP instead of 48 KB for 4.2; the price is that the epilogue is not
+// overlapped with the next tile's main loop (there is no second
+// accumulator), which the dH stage, with its heavy epilogue, does not repay.
+//
+// Paired stages (dH, when the reduction is at least 64 k-blocks long): the
+// kernel runs as clusters of two CTAs that take two 128-row tiles of one
+// expert at the same n-tile.  Both need the same weight tiles: each CTA
+// loads half of the boxes and multicasts them to both, halving the weight
+// bytes each SM pulls from L2.  A stage is free again once both CTAs' MMAs
+// have consumed it (their commits arrive in both CTAs), and the leader
+// (rank 0) claims the pair tiles and posts them into both CTAs' tile queues.
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
 // [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile (and
@@ -102,14 +110,25 @@ __host__ __device__ constexpr bool fused_sw(int m) { return m == DOWN_SWIGLU || 
 __host__ __device__ constexpr bool is_wgrad(int m) { return m == DW12 || m == DW1 || is_dw3(m); }
 // stages that can run as clusters of two CTAs sharing (multicasting) the
 // weight tiles; the host pairs them when the reduction is long
-__host__ __device__ constexpr bool pairable(int m) { return m == DOWN_H || m == DH_SWIGLU || m == DH_SILU || m == DX; }
+__host__ __device__ constexpr bool pairable(int m) { return m == DH_SWIGLU || m == DH_SILU; }
 // Pairing pays off on long reductions with many tiles (measured: the
-// Mixtral-like layer's dX 11% and dH 6% faster); on a small layer the
-// pairs' lockstep costs more than the shared loads save.
+// Mixtral-like layer's dH 6% faster); on a small layer the pairs' lockstep
+// costs more than the shared loads save.  The up projection, the stored-H
+// down projection and dX take wide tiles instead (faster there than pairs:
+// down 46.9 -> 33.8 ms, dX 84.1 -> 66.8 ms on the Mixtral-like layer).
 constexpr int kPairMinKblocks = 64;
 constexpr int kPairMinTilesPerSm = 16;
 inline bool pair_stage(int kblocks, int64_t tiles) {
   return kblocks >= kPairMinKblocks && tiles >= (int64_t)kPairMinTilesPerSm * sm_count();
+}
+// Wide tiles for the row stages from 32 k-blocks a tile and 4 (128-row)
+// tiles per SM (measured against pair_stage's 64 and 16: the SiLU layer's
+// down 0.251 -> 0.223 ms and dX 0.243 -> 0.225 ms, the 64-expert layer's up
+// 3.93 -> 3.72 ms and dX 3.60 -> 3.40 ms).
+constexpr int kWideMinKblocks = 32;
+constexpr int kWideMinTilesPerSm = 4;
+inline bool wide_rows(int kblocks, int64_t tiles) {
+  return kblocks >= kWideMinKblocks && tiles >= (int64_t)kWideMinTilesPerSm * sm_count();
 }
 // Warp roles: producers 0-3, in the fused stages eight transform warps
 // 4-11, then the MMA warp and four epilogue warps.
@@ -1258,7 +1277,7 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       if (!rec && !make_map(&p.tmO2, wsH, s.h, rows, 32, 32, s64)) return MOEBLAZE_ERR_CUDA;
       // long reductions with many tiles: 256-row tiles (pairs of 128-row tiles of one expert)
       const int64_t nt = mt_bound * p.n_tiles;
-      const bool wide = pair_stage(p.kblocks, nt);
+      const bool wide = wide_rows(p.kblocks, nt);
       moeblaze_status r = sw ? (wide ? launch<UP_SWIGLU, WIDE>(p, nt / 2, st) : launch<UP_SWIGLU>(p, nt, st))
                              : (wide ? launch<UP_SILU, WIDE>(p, nt / 2, st) : launch<UP_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
@@ -1277,8 +1296,8 @@ moeblaze_status tc_forward(const moeblaze_shape& s, const __nv_bfloat16* x, cons
       p.rowg = rec ? saved_row_gates(saved, s) : nullptr;
       p.sched = sched + 1;
       const int64_t nt = mt_bound * p.n_tiles;
-      const bool pair = pair_stage(p.kblocks, nt);
-      moeblaze_status r = !rec ? (pair ? launch<DOWN_H, WIDE>(p, nt / 2, st) : launch<DOWN_H>(p, nt, st))
+      const bool wide = wide_rows(p.kblocks, nt);
+      moeblaze_status r = !rec ? (wide ? launch<DOWN_H, WIDE>(p, nt / 2, st) : launch<DOWN_H>(p, nt, st))
                                : (sw ? launch<DOWN_SWIGLU>(p, nt, st) : launch<DOWN_SILU>(p, nt, st));
       if (r != MOEBLAZE_OK) return r;
     }
@@ -1373,7 +1392,7 @@ moeblaze_status tc_backward(const moeblaze_shape& s, const __nv_bfloat16* dY, co
     p.acc32 = wsdX32;
     p.sched = sched + 1;
     const int64_t nt = mt_bound * p.n_tiles;
-    moeblaze_status r = pair_stage(p.kblocks, nt) ? launch<DX, WIDE>(p, nt / 2, st) : launch<DX>(p, nt, st);
+    moeblaze_status r = wide_rows(p.kblocks, nt) ? launch<DX, WIDE>(p, nt / 2, st) : launch<DX>(p, nt, st);
     if (r != MOEBLAZE_OK) return r;
   }
   stage_event(ev++, st);

@@ -67,6 +67,16 @@ def test_bf16_layer_wide_weight_gradient_tiles(L, d, h, E, K, act, one, recomput
     full_compare(cfg, _routed_inputs(cfg, 6, one), recompute_h=recompute_h)
 
 
+def test_bf16_layer_wide_row_stages_whole_tensor():
+    """d = h = 4096 and enough rows for 16 tiles per SM: the up projection,
+    the stored-H down projection and dX run 256-row tiles, dH runs as
+    cluster pairs, and the weight gradients run 256-row tiles (6,667 rows
+    per expert); every output compared whole with the oracle (about a
+    minute of fp64 work on the host)."""
+    cfg = I.MoEConfig("t_wide_rows_swiglu", 10000, 4096, 4096, 3, 2, "swiglu", "bf16", 31, "softmax")
+    full_compare(cfg, _routed_inputs(cfg, 8))
+
+
 @pytest.mark.parametrize("recompute_h", [False, True])
 def test_bf16_layer_most_experts_empty(recompute_h):
     """60 of 64 experts (the last one among them) get no token: the weight
