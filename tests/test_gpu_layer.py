@@ -56,13 +56,17 @@ def test_bf16_layer_small(L, d, h, E, K, act, one, recompute_h):
     (24577, 256, 512, 3, 2, "swiglu", 1),     # skewed: expert 1 takes every token's first slot
     (6000, 512, 640, 5, 4, "swiglu", None),   # just above 4,096 rows per expert; d 512, h 640 (2.5 wide tiles)
     (4000, 768, 256, 6, 3, "silu", 2),        # 2,000 rows per expert: 128-row tiles still
+    (13000, 512, 2048, 6, 3, "silu", None),   # down and dX wide too (32 k-blocks, 608+ tiles)
+    (10000, 2048, 512, 4, 2, "swiglu", 1),    # up wide too (32 k-blocks), skewed
 ])
 @pytest.mark.parametrize("recompute_h", [False, True])
-def test_bf16_layer_wide_weight_gradient_tiles(L, d, h, E, K, act, one, recompute_h):
+def test_bf16_layer_wide_tiles(L, d, h, E, K, act, one, recompute_h):
     """At least 4,096 routed rows per expert on average and output rows in
     multiples of 256 (of 128 for dW3): the weight-gradient stages run
     256-row tiles (two M=128 MMAs that share every B tile, one 512-column
-    accumulator), with ragged expert segments; whole-tensor parity."""
+    accumulator), with ragged expert segments; with 32+ k-blocks a tile and
+    4+ tiles per SM the row stages (up, stored-H down, dX) do too;
+    whole-tensor parity."""
     cfg = I.MoEConfig(f"t_wide_{act}_{L}_{d}_{h}_{E}_{K}", L, d, h, E, K, act, "bf16", 12, "softmax")
     full_compare(cfg, _routed_inputs(cfg, 6, one), recompute_h=recompute_h)
 
