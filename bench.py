@@ -773,6 +773,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload with this many tokens instead (smaller profiling captures)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="run the workload with this many experts instead (smaller profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clock-log", default=None,
                     help="keep the raw nvidia-smi clock samples of the timed region at this path ({rank} is replaced)")
@@ -793,6 +795,9 @@ def main():
     cfg = I.CONFIGS[args.config]
     if args.tokens:
         cfg = cfg.scaled(L=args.tokens, name=f"{cfg.name}_tokens{args.tokens}")
+        I.CONFIGS[args.config] = cfg
+    if args.experts:
+        cfg = cfg.scaled(E=args.experts, name=f"{cfg.name}_experts{args.experts}")
         I.CONFIGS[args.config] = cfg
 
     if args.only == "dispatch":
