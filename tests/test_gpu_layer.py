@@ -58,6 +58,7 @@ def test_bf16_layer_small(L, d, h, E, K, act, one, recompute_h):
     (4000, 768, 256, 6, 3, "silu", 2),        # 2,000 rows per expert: 128-row tiles still
     (13000, 512, 2048, 6, 3, "silu", None),   # down and dX wide too (32 k-blocks, 608+ tiles)
     (10000, 2048, 512, 4, 2, "swiglu", 1),    # up wide too (32 k-blocks), skewed
+    (12000, 512, 2048, 5, 3, "swiglu", 4),    # down (stored H) and dX wide, skewed
 ])
 @pytest.mark.parametrize("recompute_h", [False, True])
 def test_bf16_layer_wide_tiles(L, d, h, E, K, act, one, recompute_h):
