@@ -72,6 +72,22 @@ def test_bf16_layer_wide_tiles(L, d, h, E, K, act, one, recompute_h):
     full_compare(cfg, _routed_inputs(cfg, 6, one), recompute_h=recompute_h)
 
 
+def test_bf16_layer_wide_row_stages_with_empty_experts():
+    """13 of 16 experts get no token while the down projection and dX run
+    256-row tiles (32 and 64 k-blocks, 640 tiles of 128 rows): the wide row
+    tiles of the three used experts' segments, and zero weight gradients
+    for the empty experts."""
+    cfg = I.MoEConfig("t_wide_sparse_experts", 10000, 1024, 2048, 16, 2, "swiglu", "bf16", 15, "softmax")
+    inp = I.make_inputs(cfg, "cpu")
+    ids3, gates = I.random_routing(cfg.L, 3, cfg.K, 9, one_expert=2)
+    used = torch.tensor([1, 7, 15], dtype=torch.int32)
+    inp["ids"], inp["gates"] = used[ids3.long()].contiguous(), gates
+    errs, layer = full_compare(cfg, inp)
+    empty = [e for e in range(cfg.E) if e not in used.tolist()]
+    assert float(layer.dW1[empty].float().abs().max()) == 0.0
+    assert float(layer.dW3[empty].float().abs().max()) == 0.0
+
+
 def test_bf16_layer_wide_row_stages_whole_tensor():
     """d = h = 4096 and enough rows for 16 tiles per SM: the up projection,
     the stored-H down projection and dX run 256-row tiles, dH runs as
