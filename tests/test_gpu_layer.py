@@ -234,14 +234,19 @@ def test_malformed_arguments_are_refused_before_launch():
     assert layer.device_error() == 0
 
 
-@pytest.mark.parametrize("act,dtype", [("swiglu", "bf16"), ("silu", "bf16"), ("swiglu", "f32"), ("identity", "bf16")])
-def test_graph_step_matches_eager_step(act, dtype):
+@pytest.mark.parametrize("act,dtype,L,d,h,E", [
+    ("swiglu", "bf16", 1000, 256, 384, 5),
+    ("silu", "bf16", 1000, 256, 384, 5),
+    ("swiglu", "f32", 1000, 256, 384, 5),
+    ("identity", "bf16", 1000, 256, 0, 5),
+    ("swiglu", "bf16", 10000, 1024, 2048, 4),  # 256-row tiles: down, dX, dW1 || dW2, dW3
+])
+def test_graph_step_matches_eager_step(act, dtype, L, d, h, E):
     """The whole step captured as one CUDA graph (GraphStep) and replayed on
     refilled inputs gives the same bits as eager steps (K = 2: every
     reduction is order-independent)."""
     from mixture_experts_atomic_gb300.layer import GraphStep, MoELayer
-    h = 0 if act == "identity" else 384
-    cfg = I.MoEConfig("t_graph", 1000, 256, h, 5, 2, act, dtype, 33, "softmax")
+    cfg = I.MoEConfig("t_graph", L, d, h, E, 2, act, dtype, 33, "softmax")
     base = {k: (v.cuda() if v is not None else None) for k, v in I.make_inputs(cfg, "cpu").items()}
     eager = MoELayer.for_config(cfg, "cuda", with_dgates=False)
     layer = MoELayer.for_config(cfg, "cuda", with_dgates=False)
