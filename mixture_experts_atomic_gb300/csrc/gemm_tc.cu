@@ -81,11 +81,13 @@ constexpr int B_MAX_BYTES = 256 * BK * 2;     // 32 KB
 constexpr int PRODUCER_WARPS = 4;
 constexpr int PRODUCER_THREADS = PRODUCER_WARPS * 32;
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
-// epilogue staging for TMA stores: per epilogue warp a ring of EPI_RING
-// buffers of 32 rows x 32 bf16 (64-byte swizzle)
-constexpr int EPI_RING = 4;
+// epilogue staging for TMA stores: a 32 KB area of buffers of 32 rows x 32
+// bf16 (64-byte swizzle), a ring of them per epilogue warp
 constexpr int EPI_BUF_BYTES = 32 * 64;
-constexpr int EPI_STAGE_BYTES = 4 * EPI_RING * EPI_BUF_BYTES;  // 32 KB
+constexpr int EPI_STAGE_BYTES = 16 * EPI_BUF_BYTES;  // 32 KB
+// Launch variants of a stage: one CTA a tile, clusters of two CTAs sharing
+// the weight tiles (row stages), or wide tiles.
+enum Variant : int { SINGLE = 0, PAIRED = 1, WIDE = 2 };
 constexpr int BAR_BYTES = 512;                // mbarriers, TMEM address, abort flag, tile queue
 // Tiles are claimed dynamically: each CTA takes its first two tiles by its
 // index and every further one from a global counter, two tiles ahead of
@@ -134,12 +136,14 @@ inline bool wide_rows(int kblocks, int64_t tiles) {
 // 4-11, then the MMA warp and four epilogue warps.
 __host__ __device__ constexpr int helper_warps(int m) { return is_fused(m) ? 8 : 0; }
 __host__ __device__ constexpr int mma_warp(int m) { return PRODUCER_WARPS + helper_warps(m); }
-__host__ __device__ constexpr int num_threads(int m) { return (mma_warp(m) + 1 + 4) * 32; }
+// Epilogue warps: eight in the wide up projection (one set of four per
+// 128-row half of the tile, so the epilogue its single accumulator leaves
+// exposed takes half as long), else four.  Their TMA-store staging area
+// stays 32 KB: two buffers a warp instead of four.
+__host__ __device__ constexpr int epi_warps(int m, int v) { return v == WIDE && (m == UP_SWIGLU || m == UP_SILU) ? 8 : 4; }
+__host__ __device__ constexpr int num_threads(int m, int v = SINGLE) { return (mma_warp(m) + 1 + epi_warps(m, v)) * 32; }
 // threads that recompute the A operand of a fused stage
 __host__ __device__ constexpr int transform_threads(int m) { return helper_warps(m) * 32; }
-// Launch variants of a stage: one CTA a tile, clusters of two CTAs sharing
-// the weight tiles (row stages), or wide weight-gradient tiles.
-enum Variant : int { SINGLE = 0, PAIRED = 1, WIDE = 2 };
 // Wide weight-gradient tiles: 256 output rows a CTA, as two M=128 MMAs that
 // share every B tile, into one 512-column accumulator (no second buffer: the
 // epilogue runs once per reduction, which is long when this is chosen).  A
@@ -225,10 +229,11 @@ struct StoreRing {
   uint32_t base;
   int slot;
 };
+template <int RING>
 __device__ __forceinline__ void staged_store(StoreRing& ring, const CUtensorMap* map, int col, int row0, const float* v,
                                              bool valid, int lane) {
   const uint32_t buf = ring.base + ring.slot * EPI_BUF_BYTES;
-  if (lane == 0) bulk_wait_read<EPI_RING - 1>();  // this buffer's previous store has been read
+  if (lane == 0) bulk_wait_read<RING - 1>();  // this buffer's previous store has been read
   __syncwarp();
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -247,7 +252,7 @@ __device__ __forceinline__ void staged_store(StoreRing& ring, const CUtensorMap*
     tma_store_2d(map, buf, col, row0);
     bulk_commit();
   }
-  ring.slot = (ring.slot + 1) % EPI_RING;
+  ring.slot = (ring.slot + 1) % RING;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -439,13 +444,15 @@ __host__ __device__ constexpr bool cp_a(int m) {
 __host__ __device__ constexpr bool cp_b(int m) { return is_dw3(m); }
 
 template <int MODE, int VAR>
-__global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(num_threads(MODE, VAR), 1) moe_gemm_kernel(const __grid_constant__ Params p) {
   constexpr bool PAIR = VAR == PAIRED;
   // WIDE: 256-row weight-gradient tiles (two M=128 MMAs a k-step, one accumulator)
   constexpr bool WIDE_T = VAR == WIDE;
   static_assert(!WIDE_T || widenable(MODE), "stage has no wide tiles");
   constexpr int NACC = WIDE_T ? 1 : 2;  // accumulator buffers in TMEM
   constexpr int AB = a_bytes_of(VAR);   // A part of a stage
+  constexpr int EW = epi_warps(MODE, VAR);                 // epilogue warps
+  constexpr int ER = EPI_STAGE_BYTES / (EW * EPI_BUF_BYTES);  // staging buffers per epilogue warp
   constexpr bool CPA = cp_a(MODE), CPB = cp_b(MODE), CP = CPA || CPB;
   // FUSED: transform warps recompute the A operand from the saved tiles
   constexpr bool FUSED = is_fused(MODE);
@@ -491,8 +498,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
     }
     mbar_init(bar(8), 1);
     mbar_init(bar(9), 1);
-    mbar_init(bar(10), 128);
-    mbar_init(bar(11), 128);
+    mbar_init(bar(10), 32 * EW);
+    mbar_init(bar(11), 32 * EW);
     mbar_init(bar(12), 1);
     for (int i = 0; i < TQ; ++i) {
       mbar_init(bar(32 + i), 1);
@@ -500,7 +507,7 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
       // TMA-only stages), the transform warps (fused stages), the MMA thread
       // and the four epilogue warps; in a pair rank 0's slot is also freed by
       // the peer's readers (rank 1 posts nothing)
-      mbar_init(bar(40 + i), ((CP ? PRODUCER_WARPS : 1) + helper_warps(MODE) + 1 + 4) * (PAIR ? 2 : 1));
+      mbar_init(bar(40 + i), ((CP ? PRODUCER_WARPS : 1) + helper_warps(MODE) + 1 + EW) * (PAIR ? 2 : 1));
     }
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -913,7 +920,8 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
     // ================================================================ epilogue
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter ...
     const int r = quarter * 32 + lane;            // accumulator row of this thread
-    StoreRing ring{smem_base + NST * SB + (warp - MMA_WARP - 1) * EPI_RING * EPI_BUF_BYTES, 0};
+    const int ew = warp - MMA_WARP - 1;           // epilogue warp 0 .. EW-1
+    StoreRing ring{smem_base + NST * SB + ew * ER * EPI_BUF_BYTES, 0};
     int abuf = 0;
     uint32_t aph = 0;
     for (int j = 0;; ++j) {
@@ -982,9 +990,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
 
       if constexpr (!is_wgrad(MODE)) {
         if constexpr (MODE == UP_SWIGLU || MODE == UP_SILU) {
-          // wide tiles: rows 128-255 of the tile from accumulator columns 256-511
+          // wide tiles: rows 128-255 of the tile from accumulator columns
+          // 256-511 (with eight epilogue warps, by the second four)
+          const int hm0 = EW == 8 ? ew / 4 : 0;
 #pragma unroll 1
-          for (int hm = 0; hm < (WIDE_T ? 2 : 1); ++hm) {
+          for (int hm = hm0; hm < (EW == 8 ? hm0 + 1 : WIDE_T ? 2 : 1); ++hm) {
             const uint32_t tb = tbase + hm * 256;
             const int wr = wrow0 + hm * BM;
             const bool vr = hm == 0 ? valid : (q + BM - t.pad0) < t.n_e;
@@ -998,13 +1008,13 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
                   va[i] = __uint_as_float(ra[i]);
                   vb[i] = __uint_as_float(rb[i]);
                 }
-                staged_store(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
-                staged_store(ring, &p.tmO1, t.n0 + 32 * c, wr, vb, vr, lane);
+                staged_store<ER>(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
+                staged_store<ER>(ring, &p.tmO1, t.n0 + 32 * c, wr, vb, vr, lane);
                 if (p.o2) {  // H for the down projection (not with MOEBLAZE_RECOMPUTE_H)
                   float vh[32];
 #pragma unroll
                   for (int i = 0; i < 32; ++i) vh[i] = va[i] * fast_sigmoid(va[i]) * vb[i];
-                  staged_store(ring, &p.tmO2, t.n0 + 32 * c, wr, vh, vr, lane);
+                  staged_store<ER>(ring, &p.tmO2, t.n0 + 32 * c, wr, vh, vr, lane);
                 }
               }
             } else {
@@ -1013,11 +1023,11 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) va[i] = __uint_as_float(ra[i]);
-                staged_store(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
+                staged_store<ER>(ring, &p.tmO0, t.n0 + 32 * c, wr, va, vr, lane);
                 if (p.o2) {  // H = SiLU(a) for the down projection (not with MOEBLAZE_RECOMPUTE_H)
 #pragma unroll
                   for (int i = 0; i < 32; ++i) vb[i] = va[i] * fast_sigmoid(va[i]);
-                  staged_store(ring, &p.tmO2, t.n0 + 32 * c, wr, vb, vr, lane);
+                  staged_store<ER>(ring, &p.tmO2, t.n0 + 32 * c, wr, vb, vr, lane);
                 }
               }
             }
@@ -1091,10 +1101,10 @@ __global__ void __launch_bounds__(num_threads(MODE), 1) moe_gemm_kernel(const __
                 dgp += sl * __uint_as_float(ra[i]);
               }
             }
-            staged_store(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
-            if constexpr (SW) staged_store(ring, &p.tmO2, t.n0 + 32 * c, wrow0, dB, valid, lane);
+            staged_store<ER>(ring, &p.tmO0, t.n0 + 32 * c, wrow0, dA, valid, lane);
+            if constexpr (SW) staged_store<ER>(ring, &p.tmO2, t.n0 + 32 * c, wrow0, dB, valid, lane);
             // Hg for the dW3 GEMM (not with MOEBLAZE_RECOMPUTE_H)
-            if (p.o1) staged_store(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
+            if (p.o1) staged_store<ER>(ring, &p.tmO1, t.n0 + 32 * c, wrow0, Hg, valid, lane);
           }
           if (valid && p.dg) atomicAdd(p.dg + (int64_t)tok * p.K + kslot, dgp);
         }
@@ -1175,7 +1185,7 @@ moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * (sm_count() / 2)));
-    cfg.blockDim = dim3(num_threads(MODE));
+    cfg.blockDim = dim3(num_threads(MODE, VAR));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -1195,7 +1205,7 @@ moeblaze_status launch(Params& p, int64_t tiles_bound, cudaStream_t st) {
     MB_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
   } else {
     const int64_t g = tiles_bound < sm_count() ? tiles_bound : sm_count();
-    kern<<<(unsigned)g, num_threads(MODE), smem, st>>>(p);
+    kern<<<(unsigned)g, num_threads(MODE, VAR), smem, st>>>(p);
   }
   MB_CUDA(cudaGetLastError());
   count_launch();
