@@ -12,8 +12,10 @@
 //   warp 4      TMEM allocator and MMA issuer: one thread issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N<=256, K=16),
 //               fp32 accumulators in TMEM, two accumulator buffers so the
-//               epilogue of tile i overlaps the main loop of tile i+1.
-//   warps 5-8   epilogue: tcgen05.ld of the accumulator rows and the fused
+//               epilogue of tile i overlaps the main loop of tile i+1 (one
+//               buffer of 512 columns in the wide tiles below).
+//   warps 5-8   epilogue (5-12 in the wide up projection, four per 128-row
+//               half of its tile): tcgen05.ld of the accumulator rows and the fused
 //               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward
 //               with the gate gradients, plain stores).
 // The CTAs claim tiles from a per-launch counter (weight-gradient tiles in
