@@ -138,11 +138,14 @@ inline bool wide_rows(int kblocks, int64_t tiles) {
 // 4-11, then the MMA warp and four epilogue warps.
 __host__ __device__ constexpr int helper_warps(int m) { return is_fused(m) ? 8 : 0; }
 __host__ __device__ constexpr int mma_warp(int m) { return PRODUCER_WARPS + helper_warps(m); }
-// Epilogue warps: eight in the wide up projection (one set of four per
-// 128-row half of the tile, so the epilogue its single accumulator leaves
-// exposed takes half as long), else four.  Their TMA-store staging area
-// stays 32 KB: two buffers a warp instead of four.
-__host__ __device__ constexpr int epi_warps(int m, int v) { return v == WIDE && (m == UP_SWIGLU || m == UP_SILU) ? 8 : 4; }
+// Epilogue warps: eight in the wide row stages with a stored or combined
+// output (one set of four per 128-row half of the tile, so the epilogue
+// their single accumulator leaves exposed takes half as long), else four.
+// Their TMA-store staging area stays 32 KB: two buffers a warp instead of
+// four.
+__host__ __device__ constexpr int epi_warps(int m, int v) {
+  return v == WIDE && (m == UP_SWIGLU || m == UP_SILU || m == DOWN_H || m == DX) ? 8 : 4;
+}
 __host__ __device__ constexpr int num_threads(int m, int v = SINGLE) { return (mma_warp(m) + 1 + epi_warps(m, v)) * 32; }
 // threads that recompute the A operand of a fused stage
 __host__ __device__ constexpr int transform_threads(int m) { return helper_warps(m) * 32; }
@@ -1040,9 +1043,11 @@ __global__ void __launch_bounds__(num_threads(MODE, VAR), 1) moe_gemm_kernel(con
           if constexpr (is_down(MODE)) {
             if (p.rowg && t.n0 == 0) p.rowg[q] = valid ? g : 0.f;
           }
-          // wide tiles: rows 128-255 of the tile from accumulator columns 256-511
+          // wide tiles: rows 128-255 of the tile from accumulator columns
+          // 256-511 (with eight epilogue warps, by the second four)
+          const int hm0 = EW == 8 ? ew / 4 : 0;
 #pragma unroll 1
-          for (int hm = 0; hm < (WIDE_T ? 2 : 1); ++hm) {
+          for (int hm = hm0; hm < (EW == 8 ? hm0 + 1 : WIDE_T ? 2 : 1); ++hm) {
             const bool vr = hm == 0 ? valid : valid_1;
             const float gr = hm == 0 ? g : g_1;
             float* dst = p.acc32 + (int64_t)(hm == 0 ? tok : tok_1) * p.d + t.n0;
