@@ -11,6 +11,11 @@ device copies of x, ids, gates, dY and device -> host copies of y and dX
 inside the timed region, overlapped with the neighbouring steps); `roofline`
 describes the dominant kernel, timed live from the library's stage events;
 `cpu_baseline` times the CPU oracle on a bounded sample of the workload.
+Beside the step: the router legs (timed first), the step replayed as one
+captured CUDA graph (`graph_step`), the step without H / Hg temporaries
+(`recompute_h`), and the dispatch build and identity gather/combine on the
+2M-token routing stress case.  --tokens and --experts shrink the workload
+for profiling captures.
 With --gpus N > 1 every rank runs an independent replica on its own batch
 (weak scaling; the step has no cross-rank exchange in the timed region).
 """
