@@ -14,10 +14,10 @@
 //               fp32 accumulators in TMEM, two accumulator buffers so the
 //               epilogue of tile i overlaps the main loop of tile i+1 (one
 //               buffer of 512 columns in the wide tiles below).
-//   warps 5-8   epilogue (5-12 in the wide up projection, four per 128-row
-//               half of its tile): tcgen05.ld of the accumulator rows and the fused
-//               per-row work (SwiGLU, gate-weighted combine, SwiGLU backward
-//               with the gate gradients, plain stores).
+//   warps 5-8   epilogue (5-12 in the wide up, down and dX tiles, four per
+//               128-row half): tcgen05.ld of the accumulator rows and the
+//               fused per-row work (SwiGLU, gate-weighted combine, SwiGLU
+//               backward with the gate gradients, plain stores).
 // The CTAs claim tiles from a per-launch counter (weight-gradient tiles in
 // descending order of expert load), so skewed expert loads balance.
 //
@@ -39,7 +39,7 @@
 //
 // Row space: an expert's routed rows form a segment of a padded row space,
 // [pad_off[e], pad_off[e+1]), 256-row aligned, so every 128-row M tile (and
-// every pair of them, see below)
+// every aligned pair of them: a wide tile, or a cluster pair's tiles)
 // belongs to one expert.  Row q of expert e with i = q - pad_off[e] < n_e is
 // routed row off[e]+i of token expert_token_indices[off[e]+i]; padding rows
 // gather a valid token and are zero where they feed a reduction.
