@@ -53,6 +53,7 @@ def test_bf16_layer_small(L, d, h, E, K, act, one, recompute_h):
     (16384, 256, 256, 2, 2, "swiglu", None),  # dW1 || dW2 and dW3 in 256-row tiles
     (16384, 256, 384, 2, 2, "swiglu", None),  # h % 256 == 128: dW3's last wide tile is half empty
     (16384, 512, 256, 2, 2, "silu", None),    # dW1 alone (SiLU)
+    (16384, 384, 256, 2, 1, "swiglu", None),  # d % 256 == 128: dW1 || dW2 keeps 128-row tiles, dW3 wide
     (24577, 256, 512, 3, 2, "swiglu", 1),     # skewed: expert 1 takes every token's first slot
     (6000, 512, 640, 5, 4, "swiglu", None),   # just above 4,096 rows per expert; d 512, h 640 (2.5 wide tiles)
     (4000, 768, 256, 6, 3, "silu", 2),        # 2,000 rows per expert: 128-row tiles still
